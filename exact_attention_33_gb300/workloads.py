@@ -1,0 +1,243 @@
+"""Seeded synthetic inputs and work counters for the attention workloads.
+
+This module only draws random numbers, rounds them to bfloat16 and lays them
+out; it holds none of the attention arithmetic.  Both the CUDA path (through
+the tests and ``bench.py``) and the CPU oracle (through the tests) take their
+inputs from here, so the two sides see identical bf16 bits.
+
+Recipe (all values iid N(0, 1) drawn as float32 and rounded to bf16, round to
+nearest even):
+
+* every tensor is generated in chunks of ``CHUNK`` elements; chunk ``c`` of
+  stream ``s`` under seed ``seed`` comes from
+  ``numpy.random.default_rng(SeedSequence([seed, s, c])).standard_normal``,
+  so the bits do not depend on how many threads fill the chunks;
+* Q, K, V use seed 0 with streams 0, 1, 2;
+* long-context prefill: for each (batch, kv head), ceil(1% of N) key rows
+  chosen uniformly without replacement under seed 1 are multiplied by 8
+  (exact in bf16), which moves the running row maximum late in many rows;
+* varlen: 32 sequence lengths ``rng.integers(64, 4097)`` under seed 2;
+* paged decode: context lengths ``rng.integers(512, 32769)`` under seed 3;
+  the pool holds exactly sum(ceil(ctx / 16)) blocks and the block table is
+  a permutation of the pool under seed 4 (unused table slots hold -1).
+"""
+
+from __future__ import annotations
+
+import math
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, field
+
+import numpy as np
+
+CHUNK = 1 << 22
+
+# The benchmark/parity workloads, named by what they are.
+WORKLOADS = {
+    "pr1": dict(kind="dense", B=1, H=1, Hkv=1, N=256, d=64, causal=False),
+    "dense_d64": dict(kind="dense", B=4, H=16, Hkv=16, N=2048, d=64, causal=None),
+    "long_causal_d128": dict(kind="dense", B=2, H=32, Hkv=32, N=8192, d=128, causal=True,
+                             outlier_frac=0.01, outlier_scale=8.0),
+    "varlen_gqa_d128": dict(kind="varlen", num_seqs=32, len_lo=64, len_hi=4096, H=16, Hkv=4,
+                            d=128, causal=True),
+    "paged_decode_gqa_d128": dict(kind="decode", batch=64, H=32, Hkv=8, d=128, block_size=16,
+                                  ctx_lo=512, ctx_hi=32768),
+}
+
+
+def _threads() -> int:
+    return max(1, min(32, os.cpu_count() or 1))
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bfloat16 (nearest, ties to even); returns uint16 bits."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    rounded = u + (np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1)))
+    return (rounded >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bits to float32."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    return bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def normal_bf16_bits(shape, seed: int, stream: int) -> np.ndarray:
+    """N(0,1) samples rounded to bf16, as uint16 bits, chunked and seeded."""
+    shape = tuple(int(s) for s in shape)
+    n = int(np.prod(shape)) if shape else 1
+    out = np.empty(n, dtype=np.uint16)
+    n_chunks = (n + CHUNK - 1) // CHUNK
+
+    def fill(c):
+        a = c * CHUNK
+        e = min(n, a + CHUNK)
+        rng = np.random.default_rng(np.random.SeedSequence([seed, stream, c]))
+        out[a:e] = f32_to_bf16_bits(rng.standard_normal(e - a, dtype=np.float32))
+
+    if n_chunks <= 1:
+        for c in range(n_chunks):
+            fill(c)
+    else:
+        with ThreadPoolExecutor(max_workers=_threads()) as ex:
+            list(ex.map(fill, range(n_chunks)))
+    return out.reshape(shape)
+
+
+def scale_bf16_bits_pow2(bits: np.ndarray, factor: float) -> np.ndarray:
+    """Multiply bf16 values by a power of two (exact, no overflow here)."""
+    return f32_to_bf16_bits(bf16_bits_to_f32(bits) * np.float32(factor))
+
+
+@dataclass
+class DenseInputs:
+    B: int
+    N: int
+    H: int
+    Hkv: int
+    d: int
+    q: np.ndarray   # uint16 bf16 bits [B, N, H, d]
+    k: np.ndarray   # [B, N, Hkv, d]
+    v: np.ndarray   # [B, N, Hkv, d]
+    outlier_rows: dict = field(default_factory=dict)
+
+
+def dense_inputs(B, N, H, Hkv, d, seed=0, outlier_frac=0.0, outlier_scale=8.0,
+                 outlier_seed=1) -> DenseInputs:
+    q = normal_bf16_bits((B, N, H, d), seed, 0)
+    k = normal_bf16_bits((B, N, Hkv, d), seed, 1)
+    v = normal_bf16_bits((B, N, Hkv, d), seed, 2)
+    rows = {}
+    if outlier_frac > 0.0:
+        rng = np.random.default_rng(outlier_seed)
+        n_out = int(math.ceil(outlier_frac * N))
+        for b in range(B):
+            for g in range(Hkv):
+                idx = np.sort(rng.choice(N, size=n_out, replace=False))
+                rows[(b, g)] = idx
+                k[b, idx, g, :] = scale_bf16_bits_pow2(k[b, idx, g, :], outlier_scale)
+    return DenseInputs(B, N, H, Hkv, d, q, k, v, rows)
+
+
+def varlen_lengths(num_seqs=32, lo=64, hi=4096, seed=2) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    return rng.integers(lo, hi + 1, size=num_seqs).astype(np.int64)
+
+
+def cu_seqlens_from(lengths) -> np.ndarray:
+    lengths = np.asarray(lengths, dtype=np.int64)
+    return np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+
+
+@dataclass
+class VarlenInputs:
+    lengths: np.ndarray
+    cu_seqlens: np.ndarray
+    H: int
+    Hkv: int
+    d: int
+    q: np.ndarray   # [T, H, d]
+    k: np.ndarray   # [T, Hkv, d]
+    v: np.ndarray
+
+    @property
+    def total_tokens(self) -> int:
+        return int(self.cu_seqlens[-1])
+
+    @property
+    def max_seqlen(self) -> int:
+        return int(self.lengths.max()) if len(self.lengths) else 0
+
+
+def varlen_inputs(lengths, H, Hkv, d, seed=0) -> VarlenInputs:
+    lengths = np.asarray(lengths, dtype=np.int64)
+    cu = cu_seqlens_from(lengths)
+    t = int(cu[-1])
+    return VarlenInputs(lengths, cu, H, Hkv, d,
+                        normal_bf16_bits((t, H, d), seed, 0),
+                        normal_bf16_bits((t, Hkv, d), seed, 1),
+                        normal_bf16_bits((t, Hkv, d), seed, 2))
+
+
+def decode_ctx_lens(batch=64, lo=512, hi=32768, seed=3) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    return rng.integers(lo, hi + 1, size=batch).astype(np.int32)
+
+
+def paged_block_table(ctx_lens, block_size=16, seed=4, max_blocks_per_seq=None):
+    """Random-permutation block table; returns (table int32 [batch, max_blocks], num_blocks)."""
+    ctx = np.asarray(ctx_lens, dtype=np.int64)
+    nblk = (ctx + block_size - 1) // block_size
+    num_blocks = int(nblk.sum())
+    mb = int(nblk.max()) if len(nblk) else 0
+    if max_blocks_per_seq is not None:
+        mb = max(mb, int(max_blocks_per_seq))
+    perm = np.random.default_rng(seed).permutation(num_blocks).astype(np.int32)
+    table = np.full((len(ctx), max(mb, 1)), -1, dtype=np.int32)
+    pos = 0
+    for b, n in enumerate(nblk):
+        table[b, :n] = perm[pos:pos + n]
+        pos += n
+    return table, num_blocks
+
+
+@dataclass
+class DecodeInputs:
+    batch: int
+    H: int
+    Hkv: int
+    d: int
+    block_size: int
+    ctx_lens: np.ndarray      # int32 [batch]
+    block_table: np.ndarray   # int32 [batch, max_blocks]
+    num_blocks: int
+    q: np.ndarray             # bf16 bits [batch, H, d]
+    k_pool: np.ndarray        # bf16 bits [num_blocks, block_size, Hkv, d]
+    v_pool: np.ndarray
+
+    @property
+    def max_ctx_len(self) -> int:
+        return int(self.ctx_lens.max()) if len(self.ctx_lens) else 0
+
+
+def decode_inputs(ctx_lens, H, Hkv, d, block_size=16, seed=0, table_seed=4,
+                  extra_blocks=0) -> DecodeInputs:
+    ctx = np.asarray(ctx_lens, dtype=np.int32)
+    table, nb = paged_block_table(ctx, block_size, table_seed)
+    nb_total = max(nb + int(extra_blocks), 1)
+    return DecodeInputs(len(ctx), H, Hkv, d, block_size, ctx, table, nb_total,
+                        normal_bf16_bits((len(ctx), H, d), seed, 0),
+                        normal_bf16_bits((nb_total, block_size, Hkv, d), seed, 1),
+                        normal_bf16_bits((nb_total, block_size, Hkv, d), seed, 2))
+
+
+# ---------------------------------------------------------------- counters
+
+def prefill_flops(B, N, H, d, causal) -> float:
+    """Exact attention work, 4*N^2*d per (batch, head), halved for causal."""
+    f = 4.0 * N * N * d * H * B
+    return f / 2 if causal else f
+
+
+def varlen_flops(lengths, H, d, causal) -> float:
+    return float(sum(prefill_flops(1, int(L), H, d, causal) for L in lengths))
+
+
+def decode_bytes(ctx_lens, H, Hkv, d, max_blocks_per_seq, block_size=16) -> int:
+    """Algorithmic HBM bytes of one paged decode step.
+
+    K and V rows of every cached token (bf16), the query and output rows
+    (bf16), the fp32 LSE, the context lengths and the block-table entries
+    that are actually read.
+    """
+    ctx = np.asarray(ctx_lens, dtype=np.int64)
+    kv = int(ctx.sum()) * Hkv * d * 2 * 2
+    qo = len(ctx) * H * d * 2 * 2
+    lse = len(ctx) * H * 4
+    table = int(((ctx + block_size - 1) // block_size).sum()) * 4
+    return kv + qo + lse + len(ctx) * 4 + table
