@@ -1,0 +1,548 @@
+#!/usr/bin/env python3
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step = one pass over every part of the hot path, each on its own seeded
+synthetic workload (inputs resident in HBM, all larger than L2):
+
+  * long-context causal prefill  fa_fwd          B=2, H=Hkv=32, N=8192, d=128,
+                                                 1% key rows x8 outliers
+  * packed varlen causal prefill fa_fwd_varlen   32 seqs, len U[64,4096], GQA 16/4, d=128
+  * paged GQA flash-decoding     fa_decode_paged batch 64, 32q/8kv heads, d=128,
+                                                 ctx U[512,32768], 16-token blocks
+
+Reported (one JSON line from rank 0):
+  value    prefill TFLOP/s over both prefill launches (algorithmic FLOPs,
+           4*N^2*d*H*B halved for causal, summed per sequence for varlen)
+  decode   HBM GB/s of the decode step (algorithmic bytes: K/V of every cached
+           token, q, out, lse, ctx lengths and block-table entries)
+  roofline / roofline_decode   the two kernels against the measured peaks
+  e2e      the same metrics with pinned-host inputs copied in and outputs
+           copied back inside the timed region
+  cpu_baseline  the fp64 oracle (NumPy) timed on the host cores on a bounded
+           sample of the long-context workload
+
+``--impl reference`` times the oracle instead (the slow reference arm).
+Multi-GPU: one process per GPU (torchrun); every rank runs the full step on
+its own GPU (weak scaling, no collective on the data path); the timed region
+is bracketed by barriers and the max over ranks is taken.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from exact_attention_33_gb300 import workloads as W  # noqa: E402
+
+METRIC = "prefill TFLOP/s & % bf16 tensor peak; paged-decode HBM GB/s & % of 8 TB/s"
+NOMINAL_HBM_GBS = 8000.0
+PROFILES = os.path.join(ROOT, "profiles")
+KERNEL_SOURCES = {
+    "prefill": ["exact_attention_33_gb300/csrc/prefill.cu", "exact_attention_33_gb300/csrc/ptx.cuh",
+                "exact_attention_33_gb300/csrc/fa_internal.h"],
+    "decode": ["exact_attention_33_gb300/csrc/decode.cu", "exact_attention_33_gb300/csrc/ptx.cuh",
+               "exact_attention_33_gb300/csrc/fa_internal.h"],
+}
+
+
+# ----------------------------------------------------------------- ranks
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a scalar over all ranks (identity for one rank)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: units processed by all ranks over the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+# ----------------------------------------------------------------- peaks, clocks, profiles
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def source_sha(kind: str) -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kind: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    name = {"prefill": "prefill_long_causal_d128.txt", "decode": "decode_paged_gqa_d128.txt"}[kind]
+    path = os.path.join(PROFILES, name)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_sha = re.search(r"source_sha:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_tr or m_sha.group(1) != source_sha(kind):
+        return None
+    return float(m_tr.group(1))
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- workloads on the device
+
+def to_dev(bits, torch, device):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def build_step(torch, device):
+    """Create the three workloads on the device; returns a dict of legs."""
+    cfg_l = W.WORKLOADS["long_causal_d128"]
+    long_in = W.dense_inputs(cfg_l["B"], cfg_l["N"], cfg_l["H"], cfg_l["Hkv"], cfg_l["d"], seed=0,
+                             outlier_frac=cfg_l["outlier_frac"],
+                             outlier_scale=cfg_l["outlier_scale"])
+    cfg_v = W.WORKLOADS["varlen_gqa_d128"]
+    lengths = W.varlen_lengths(cfg_v["num_seqs"], cfg_v["len_lo"], cfg_v["len_hi"])
+    var_in = W.varlen_inputs(lengths, cfg_v["H"], cfg_v["Hkv"], cfg_v["d"], seed=0)
+    cfg_d = W.WORKLOADS["paged_decode_gqa_d128"]
+    ctx = W.decode_ctx_lens(cfg_d["batch"], cfg_d["ctx_lo"], cfg_d["ctx_hi"])
+    dec_in = W.decode_inputs(ctx, cfg_d["H"], cfg_d["Hkv"], cfg_d["d"], cfg_d["block_size"], seed=0)
+
+    legs = {}
+    legs["long"] = dict(
+        host={"q": long_in.q, "k": long_in.k, "v": long_in.v},
+        flops=W.prefill_flops(cfg_l["B"], cfg_l["N"], cfg_l["H"], cfg_l["d"], True),
+        shape=(cfg_l["B"], cfg_l["N"], cfg_l["H"], cfg_l["Hkv"], cfg_l["d"]))
+    legs["varlen"] = dict(
+        host={"q": var_in.q, "k": var_in.k, "v": var_in.v},
+        cu=var_in.cu_seqlens, max_seqlen=var_in.max_seqlen,
+        flops=W.varlen_flops(lengths, cfg_v["H"], cfg_v["d"], True),
+        total_tokens=var_in.total_tokens)
+    legs["decode"] = dict(
+        host={"q": dec_in.q, "k_pool": dec_in.k_pool, "v_pool": dec_in.v_pool},
+        table=dec_in.block_table, ctx=dec_in.ctx_lens, max_ctx=dec_in.max_ctx_len,
+        bytes=W.decode_bytes(dec_in.ctx_lens, cfg_d["H"], cfg_d["Hkv"], cfg_d["d"],
+                             dec_in.block_table.shape[1], cfg_d["block_size"]))
+    for leg in legs.values():
+        leg["dev"] = {k: to_dev(v, torch, device) for k, v in leg["host"].items()}
+    legs["varlen"]["cu_dev"] = torch.from_numpy(legs["varlen"]["cu"]).to(device)
+    legs["decode"]["table_dev"] = torch.from_numpy(dec_in.block_table).to(device)
+    legs["decode"]["ctx_dev"] = torch.from_numpy(dec_in.ctx_lens).to(device)
+    # outputs and workspace, allocated once
+    import exact_attention_33_gb300 as fa
+    lq = legs["long"]["dev"]["q"]
+    B, N, H, Hkv, d = legs["long"]["shape"]
+    legs["long"]["out"] = torch.empty_like(lq)
+    legs["long"]["lse"] = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    vq = legs["varlen"]["dev"]["q"]
+    legs["varlen"]["out"] = torch.empty_like(vq)
+    legs["varlen"]["lse"] = torch.empty((vq.shape[1], vq.shape[0]), dtype=torch.float32,
+                                        device=device)
+    dq = legs["decode"]["dev"]["q"]
+    legs["decode"]["out"] = torch.empty_like(dq)
+    legs["decode"]["lse"] = torch.empty(dq.shape[:2], dtype=torch.float32, device=device)
+    ws = fa.fa_decode_workspace_size(dq.shape[0], dq.shape[1], cfg_d["Hkv"], cfg_d["d"],
+                                     dec_in.max_ctx_len, cfg_d["block_size"])
+    legs["decode"]["ws"] = torch.empty(ws, dtype=torch.uint8, device=device)
+    return legs
+
+
+def run_leg(fa, name, leg, dev):
+    if name == "long":
+        fa.fa_fwd(dev["q"], dev["k"], dev["v"], causal=True, out=leg["out"], lse=leg["lse"])
+    elif name == "varlen":
+        fa.fa_fwd_varlen(dev["q"], dev["k"], dev["v"], leg["cu_dev"], leg["max_seqlen"],
+                         causal=True, out=leg["out"], lse=leg["lse"])
+    else:
+        fa.fa_decode_paged(dev["q"], dev["k_pool"], dev["v_pool"], leg["table_dev"],
+                           leg["ctx_dev"], leg["max_ctx"], out=leg["out"], lse=leg["lse"],
+                           workspace=leg["ws"])
+
+
+LEG_ORDER = ("long", "varlen", "decode")
+LAUNCHES_PER_STEP = {"long": 1, "varlen": 1, "decode": 2}
+
+
+# ----------------------------------------------------------------- oracle timing
+
+def oracle_sample_tflops(max_seconds=20.0, rows_per_pair=None, pairs=4, seed=5):
+    """Time the fp64 oracle on a seeded sample of the long-context workload.
+
+    Each sampled (batch, head) pair runs the oracle on all 8192 query rows
+    (or ``rows_per_pair`` seeded rows); the work counted is the causal
+    algorithmic FLOPs of the rows evaluated.  Returns (TFLOP/s, sample text).
+    """
+    import oracle
+    cfg = W.WORKLOADS["long_causal_d128"]
+    N, d, H = cfg["N"], cfg["d"], cfg["H"]
+    rng = np.random.default_rng(seed)
+    done_flops, spent, used = 0.0, 0.0, []
+    # one (batch, head) slice at a time keeps host memory small
+    for idx in rng.choice(cfg["B"] * H, pairs, replace=False):
+        b, h = int(idx) // H, int(idx) % H
+        q = W.bf16_bits_to_f64(W.normal_bf16_bits((N, H, d), 0, 0)[:, h:h + 1]) if False else None
+        inp = _long_slice(b, h)
+        rows = None
+        if rows_per_pair is not None:
+            rows = np.sort(np.random.default_rng(seed + 1).choice(N, rows_per_pair, replace=False))
+        t0 = time.perf_counter()
+        oracle.attention_one(inp[0], inp[1], inp[2], causal=True, rows=rows)
+        dt = time.perf_counter() - t0
+        r = np.arange(N) if rows is None else rows
+        done_flops += 4.0 * d * float(np.sum(r + 1))
+        spent += dt
+        used.append((b, h))
+        if spent > max_seconds:
+            break
+    desc = (f"oracle on {len(used)} (batch, head) pairs {used} of the long-context causal "
+            f"workload, {'all' if rows_per_pair is None else rows_per_pair} query rows each")
+    return done_flops / spent / 1e12, desc, spent
+
+
+_LONG_CACHE = {}
+
+
+def _long_slice(b, h):
+    """fp64 (q, k, v) of one (batch, head) of the long-context workload."""
+    if "inp" not in _LONG_CACHE:
+        cfg = W.WORKLOADS["long_causal_d128"]
+        _LONG_CACHE["inp"] = W.dense_inputs(cfg["B"], cfg["N"], cfg["H"], cfg["Hkv"], cfg["d"],
+                                            seed=0, outlier_frac=cfg["outlier_frac"],
+                                            outlier_scale=cfg["outlier_scale"])
+    inp = _LONG_CACHE["inp"]
+    g = h // (inp.H // inp.Hkv)
+    f = W.bf16_bits_to_f64
+    return (f(inp.q[b][:, h:h + 1]), f(inp.k[b][:, g:g + 1]), f(inp.v[b][:, g:g + 1]))
+
+
+def blas_threads():
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            try:
+                return int(os.environ[var])
+            except ValueError:
+                pass
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------- arms
+
+def bench_reference(args, rank, world):
+    """The oracle as it stands, on the host cores, each step a bounded sample."""
+    if rank != 0:
+        return 0
+    # each step: one (batch, head) pair, 1024 seeded query rows (about 1-3 s)
+    steps, warmup = args.steps, args.warmup
+    per_step, total_flops, total_t, desc = [], 0.0, 0.0, ""
+    for it in range(warmup + steps):
+        tf, desc, spent = oracle_sample_tflops(max_seconds=0.0, rows_per_pair=1024, pairs=1,
+                                               seed=100 + it)
+        if it >= warmup:
+            per_step.append(spent)
+            total_t += spent
+            total_flops += tf * 1e12 * spent
+    value = total_flops / total_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": 1e3 * total_t / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "long-context causal prefill B2 H32 N8192 d128 (oracle sample)",
+                   "sample": "per step: one seeded (batch, head) pair, 1024 seeded query rows"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_ours(args, rank, world, local):
+    import torch
+    import exact_attention_33_gb300 as fa
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    fa.load_library()
+    fa.fa_device_status(clear=True)
+    legs = build_step(torch, device)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        for i, name in enumerate(LEG_ORDER):
+            if ev is not None:
+                ev[i][0].record(stream)
+            run_leg(fa, name, legs[name], legs[name]["dev"])
+            if ev is not None:
+                ev[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in LEG_ORDER]
+              for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)
+        barrier(world)
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        for it in range(args.steps):
+            step(events[it])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        time.sleep(0.2)
+    total_ms = t_start.elapsed_time(t_end)
+    leg_ms = {name: [events[it][i][0].elapsed_time(events[it][i][1]) for it in range(args.steps)]
+              for i, name in enumerate(LEG_ORDER)}
+    status = fa.fa_device_status(clear=True)
+    if status != 0:
+        raise RuntimeError(f"device status word set during the bench: {status:#x}")
+
+    # ---- end to end: pinned host inputs in, results out, inside the timed region
+    pinned = {name: {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16))
+                     .view(torch.bfloat16).pin_memory()
+                     for k, v in legs[name]["host"].items()} for name in LEG_ORDER}
+    host_out = {name: (torch.empty(legs[name]["out"].shape, dtype=torch.bfloat16).pin_memory(),
+                       torch.empty(legs[name]["lse"].shape, dtype=torch.float32).pin_memory())
+                for name in LEG_ORDER}
+    h2d = sum(t.numel() * t.element_size() for n in LEG_ORDER for t in pinned[n].values())
+    d2h = sum(o.numel() * o.element_size() + l.numel() * l.element_size()
+              for o, l in host_out.values())
+    e2e_steps = max(1, min(args.steps, 10))
+    e2e_ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in LEG_ORDER]
+              for _ in range(e2e_steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for it in range(e2e_steps):
+        for i, name in enumerate(LEG_ORDER):
+            leg = legs[name]
+            e2e_ev[it][i][0].record(stream)
+            for k, t in pinned[name].items():
+                leg["dev"][k].copy_(t, non_blocking=True)
+            run_leg(fa, name, leg, leg["dev"])
+            host_out[name][0].copy_(leg["out"], non_blocking=True)
+            host_out[name][1].copy_(leg["lse"], non_blocking=True)
+            e2e_ev[it][i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = {name: [e2e_ev[it][i][0].elapsed_time(e2e_ev[it][i][1]) for it in range(e2e_steps)]
+              for i, name in enumerate(LEG_ORDER)}
+
+    # ---- numbers (max over ranks of the time)
+    dev_idx = device
+    t_long = max_over_ranks(sum(leg_ms["long"]) / 1e3, world, dev_idx)
+    t_var = max_over_ranks(sum(leg_ms["varlen"]) / 1e3, world, dev_idx)
+    t_dec = max_over_ranks(sum(leg_ms["decode"]) / 1e3, world, dev_idx)
+    t_total = max_over_ranks(total_ms / 1e3, world, dev_idx)
+    K = args.steps
+    f_long, f_var = legs["long"]["flops"], legs["varlen"]["flops"]
+    dbytes = legs["decode"]["bytes"]
+    prefill_tflops = weak_scaling_value((f_long + f_var) * K, world, t_long + t_var) / 1e12
+    decode_gbs = weak_scaling_value(dbytes * K, world, t_dec) / 1e9
+    e2e_pre = max_over_ranks((sum(e2e_ms["long"]) + sum(e2e_ms["varlen"])) / 1e3, world, dev_idx)
+    e2e_dec = max_over_ranks(sum(e2e_ms["decode"]) / 1e3, world, dev_idx)
+    e2e_tflops = weak_scaling_value((f_long + f_var) * e2e_steps, world, e2e_pre) / 1e12
+    e2e_gbs = weak_scaling_value(dbytes * e2e_steps, world, e2e_dec) / 1e9
+
+    if rank != 0:
+        return 0
+    peaks = measured_peaks()
+    clk = clocks.summary()
+    long_launch_s = statistics.mean(leg_ms["long"]) / 1e3
+    dec_launch_s = statistics.mean(leg_ms["decode"]) / 1e3
+    timed_s = total_ms / 1e3
+    tensor_peak = peaks["bf16_tflops_sustained"] if timed_s > 2.0 else peaks["bf16_tflops"]
+    ach_long = f_long / long_launch_s / 1e12
+    ach_dec = dbytes / dec_launch_s / 1e9
+    tr_p = profiled_traffic("prefill")
+    tr_d = profiled_traffic("decode")
+    cpu_tf, cpu_desc, _ = oracle_sample_tflops(max_seconds=args.cpu_seconds)
+    line = {
+        "metric": METRIC,
+        "value": prefill_tflops,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": 1e3 * t_total / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": "exact-attention hot path: long-context causal prefill B2 H32 N8192 d128 "
+                        "(1% x8 key outliers) + packed varlen causal prefill 32 seqs U[64,4096] "
+                        "H16/Hkv4 d128 + paged GQA decode batch64 H32/Hkv8 d128 ctx U[512,32768] "
+                        "block16",
+            "prefill_flops_per_step": f_long + f_var,
+            "decode_bytes_per_step": dbytes,
+            "l2": "every input is larger than L2 (no flush needed)",
+            "parallelism": f"replicas x{world}",
+        },
+        "decode": {"value": decode_gbs, "unit": "GB/s",
+                   "frac_of_8tbs": decode_gbs / world / NOMINAL_HBM_GBS,
+                   "frac_of_measured": decode_gbs / world / peaks["hbm_gbs"],
+                   "ms_per_step": 1e3 * t_dec / K},
+        "legs": {
+            "long_causal_prefill": {"ms": 1e3 * t_long / K, "tflops": f_long * K / t_long / 1e12},
+            "varlen_causal_prefill": {"ms": 1e3 * t_var / K, "tflops": f_var * K / t_var / 1e12},
+            "paged_decode": {"ms": 1e3 * t_dec / K, "gbs": dbytes * K / t_dec / 1e9},
+        },
+        "roofline": {"bound": "tensor", "kernel": "prefill_kernel<128,causal> (long-context launch)",
+                     "achieved": ach_long, "peak": tensor_peak, "unit": "TFLOP/s",
+                     "frac": ach_long / tensor_peak, "traffic": tr_p,
+                     "peak_source": peaks["source"] + (" sustained" if timed_s > 2.0 else " burst")},
+        "roofline_decode": {"bound": "hbm", "kernel": "decode_split_kernel + decode_combine_kernel",
+                            "achieved": ach_dec, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": ach_dec / peaks["hbm_gbs"], "traffic": tr_d,
+                            "peak_source": peaks["source"]},
+        "e2e": {"value": e2e_tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "decode_gbs": e2e_gbs, "steps": e2e_steps},
+        "gpu_launches": sum(LAUNCHES_PER_STEP.values()) * K,
+        "clocks": clk,
+        "cpu_baseline": {"value": cpu_tf, "unit": "TFLOP/s", "cores": blas_threads(),
+                         "kind": "oracle", "sample": cpu_desc},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="budget of the oracle CPU-baseline sample")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return bench_reference(args, rank, world)
+    return bench_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,217 @@
+"""Exact attention for GB300 (sm_103a): thin Python binding of libfa.so.
+
+Every function here only marshals torch tensors into the C ABI declared in
+``include/fa.h`` (device pointers, sizes, the current CUDA stream) and checks
+the returned status; all arithmetic runs in the library's CUDA kernels.  There
+is no fallback: if ``libfa.so`` is missing or a call fails, an exception is
+raised.
+
+Functions keep the C names: :func:`fa_fwd`, :func:`fa_fwd_varlen`,
+:func:`fa_decode_paged`, :func:`fa_decode_workspace_size`,
+:func:`fa_status_string`, :func:`fa_device_status`.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+__all__ = [
+    "FaError", "library_path", "load_library", "fa_fwd", "fa_fwd_varlen",
+    "fa_decode_paged", "fa_decode_workspace_size", "fa_status_string", "fa_device_status",
+    "fa_version", "FA_DEV_TIMEOUT", "FA_DEV_BAD_BLOCK", "FA_DEV_BAD_CTX", "FA_DEV_BAD_SEQLEN",
+]
+
+FA_OK = 0
+FA_DEV_TIMEOUT = 1
+FA_DEV_BAD_BLOCK = 2
+FA_DEV_BAD_CTX = 4
+FA_DEV_BAD_SEQLEN = 8
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_lock = threading.Lock()
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, func: str, status: int):
+        self.status = status
+        super().__init__(f"{func} failed: {status} ({fa_status_string(status)})")
+
+
+def library_path() -> str:
+    return os.path.join(_PKG, "libfa.so")
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libfa.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -m exact_attention_33_gb300.build` "
+                "(or __graft_entry__.build()); there is no non-CUDA fallback")
+        lib = ctypes.CDLL(path)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        lib.fa_fwd.restype = i
+        lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+        lib.fa_fwd_varlen.restype = i
+        lib.fa_decode_workspace_size.argtypes = [i, i, i, i, i, i]
+        lib.fa_decode_workspace_size.restype = sz
+        lib.fa_decode_paged.argtypes = [vp, vp, vp, vp, i, vp, i, i, i, i, i, i, i, f, vp, vp,
+                                        vp, sz, vp]
+        lib.fa_decode_paged.restype = i
+        lib.fa_status_string.argtypes = [i]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i]
+        lib.fa_device_status.restype = i
+        lib.fa_version.argtypes = []
+        lib.fa_version.restype = i
+        _lib = lib
+        return lib
+
+
+def fa_status_string(status: int) -> str:
+    return load_library().fa_status_string(int(status)).decode()
+
+
+def fa_version() -> int:
+    return int(load_library().fa_version())
+
+
+def fa_device_status(clear: bool = True) -> int:
+    """Sticky device status word (FA_DEV_* bits); synchronises the device."""
+    v = ctypes.c_uint(0)
+    rc = load_library().fa_device_status(ctypes.byref(v), 1 if clear else 0)
+    if rc != FA_OK:
+        raise FaError("fa_device_status", rc)
+    return int(v.value)
+
+
+# ----------------------------------------------------------------- helpers
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream=None):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(int(s.cuda_stream))
+
+
+def _ptr(t):
+    return ctypes.c_void_p(0 if t is None else int(t.data_ptr()))
+
+
+def _check_bf16_cuda(name, t, ndim):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be bfloat16")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-D tensor")
+
+
+def _scale(scale, d):
+    return float(1.0 / math.sqrt(d)) if scale is None else float(scale)
+
+
+# ----------------------------------------------------------------- calls
+
+def fa_fwd(q, k, v, causal=False, scale=None, out=None, lse=None, want_lse=True, stream=None):
+    """Dense prefill.  q [B,N,H,d], k/v [B,N,Hkv,d] bf16 CUDA tensors.
+
+    Returns (out [B,N,H,d] bf16, lse [B,H,N] fp32 or None).
+    """
+    torch = _torch()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_bf16_cuda(name, t, 4)
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    if k.shape != (B, N, Hkv, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, N, Hkv, d] matching q")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    rc = load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, N, d,
+                               _scale(scale, d), 1 if causal else 0, _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError("fa_fwd", rc)
+    return out, lse
+
+
+def fa_fwd_varlen(q, k, v, cu_seqlens, max_seqlen, causal=False, scale=None, out=None,
+                  lse=None, want_lse=True, stream=None):
+    """Packed varlen prefill.  q [T,H,d], k/v [T,Hkv,d], cu_seqlens int32 [S+1] on device.
+
+    Returns (out [T,H,d] bf16, lse [H,T] fp32 or None).
+    """
+    torch = _torch()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_bf16_cuda(name, t, 3)
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
+        raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
+    T, H, d = q.shape
+    Hkv = k.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    rc = load_library().fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                      _ptr(cu_seqlens), cu_seqlens.numel() - 1, T,
+                                      int(max_seqlen), H, Hkv, d, _scale(scale, d),
+                                      1 if causal else 0, _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError("fa_fwd_varlen", rc)
+    return out, lse
+
+
+def fa_decode_workspace_size(batch, H, Hkv, d, max_ctx_len, block_size=16) -> int:
+    return int(load_library().fa_decode_workspace_size(batch, H, Hkv, d, max_ctx_len,
+                                                       block_size))
+
+
+def fa_decode_paged(q, k_pool, v_pool, block_table, ctx_lens, max_ctx_len, scale=None,
+                    out=None, lse=None, workspace=None, want_lse=True, stream=None):
+    """Paged GQA flash-decoding.
+
+    q [batch,H,d]; pools [num_blocks,block_size,Hkv,d] bf16; block_table int32
+    [batch, max_blocks]; ctx_lens int32 [batch]; all on the device.
+    Returns (out [batch,H,d] bf16, lse [batch,H] fp32 or None).
+    """
+    torch = _torch()
+    _check_bf16_cuda("q", q, 3)
+    _check_bf16_cuda("k_pool", k_pool, 4)
+    _check_bf16_cuda("v_pool", v_pool, 4)
+    for name, t in (("block_table", block_table), ("ctx_lens", ctx_lens)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    batch, H, d = q.shape
+    num_blocks, block_size, Hkv, _ = k_pool.shape
+    need = fa_decode_workspace_size(batch, H, Hkv, d, max_ctx_len, block_size)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((batch, H), dtype=torch.float32, device=q.device)
+    rc = load_library().fa_decode_paged(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), block_table.shape[1],
+        _ptr(ctx_lens), int(max_ctx_len), batch, H, Hkv, d, block_size, num_blocks,
+        _scale(scale, d), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+        _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError("fa_decode_paged", rc)
+    return out, lse

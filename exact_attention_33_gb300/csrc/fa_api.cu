@@ -1,0 +1,332 @@
+// fa_api.cu - the C ABI of libfa.so: argument validation, TMA tensor-map
+// construction and kernel dispatch.  The host side keeps the strides, dtypes,
+// masking mode and sequence layout of every call and hands the kernels a
+// plain parameter block (the bridge described in "How the Repo Connects
+// Python to Bare-Metal CUDA" of the explainer article on the FlashAttention
+// repository); nothing here allocates device memory or synchronises.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace fa {
+
+__device__ unsigned int g_status = 0;
+
+cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                           const PrefillParams &p, int d, bool causal, bool varlen, int grid,
+                           cudaStream_t stream);
+cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
+                          int d, cudaStream_t stream);
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// bf16 tensor [outer][rows][heads][d] (d innermost) as a 4-D TMA map with
+// dims {d, heads, rows, outer}; each copy moves a box of {64, 1, box_rows, 1}
+// with 128-byte swizzle.  Out-of-range rows read as zero.
+int make_map(CUtensorMap *map, const void *base, int d, int heads, long long rows,
+             long long outer, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return FA_ERR_CUDA;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                              static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(outer)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(heads) * d * 2,
+                                 static_cast<cuuint64_t>(rows) * heads * d * 2};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+// Paged pool [num_blocks * block_size tokens][Hkv][d] as a 3-D map.
+int make_pool_map(CUtensorMap *map, const void *base, int d, int heads, long long tokens) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return FA_ERR_CUDA;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                              static_cast<cuuint64_t>(tokens)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(heads) * d * 2};
+  const cuuint32_t box[3] = {64, 1, kDecodeBlock};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
+
+// Device address of the sticky status word of the current device (looked up
+// once per device).
+unsigned int *status_ptr() {
+  constexpr int kMaxDev = 64;
+  static unsigned int *ptrs[kMaxDev] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (ptrs[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<unsigned int *>(p);
+  }
+  return ptrs[dev];
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// Keys per split of the decode kernel.  Large splits keep the partial-state
+// traffic small; the split shrinks (down to 64 keys) while the number of
+// (sequence, KV head, split) work items would not fill about two waves of
+// split CTAs (seven resident per SM).
+int decode_split_tokens(int batch, int Hkv, int max_ctx_len) {
+  int sms = sm_count();
+  if (sms <= 0) sms = 148;
+  const long long want = 2LL * 7 * sms;
+  int split = kDecodeMaxSplitTokens;
+  while (split > 64) {
+    const long long items =
+        static_cast<long long>(batch) * Hkv * ((max_ctx_len + split - 1) / split);
+    if (items >= want) break;
+    split >>= 1;
+  }
+  return split;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct DecodeWs {
+  int split_tokens;
+  int max_splits;
+  size_t o_bytes;
+  size_t ml_bytes;
+};
+
+DecodeWs decode_ws(int batch, int H, int Hkv, int d, int max_ctx_len) {
+  DecodeWs w;
+  w.split_tokens = decode_split_tokens(batch, Hkv, max_ctx_len);
+  w.max_splits = std::max(1, (max_ctx_len + w.split_tokens - 1) / w.split_tokens);
+  const size_t rows = static_cast<size_t>(batch) * H * w.max_splits;
+  w.o_bytes = round_up(rows * d * sizeof(float), 256);
+  w.ml_bytes = round_up(rows * 2 * sizeof(float), 256);
+  return w;
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_version(void) { return 100; }
+
+const char *fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    default: return "unknown status";
+  }
+}
+
+int fa_device_status(unsigned int *status, int clear) {
+  if (status == nullptr) return FA_ERR_INVALID_ARG;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(v)) != cudaSuccess) return FA_ERR_CUDA;
+  *status = v;
+  if (clear) {
+    const unsigned int z = 0;
+    if (cudaMemcpyToSymbol(g_status, &z, sizeof(z)) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+int fa_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
+           int Hkv, int N, int d, float scale, int causal, fa_stream_t stream) {
+  if (!q || !k || !v || !out) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+    return FA_ERR_INVALID_ARG;
+  if (lse && !aligned(lse, 4)) return FA_ERR_INVALID_ARG;
+  if (B < 0 || N < 0 || H < 1 || Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (B == 0 || N == 0) return FA_OK;
+  const long long pairs = (N + kPrefillRowsPerCta - 1) / kPrefillRowsPerCta;
+  const long long grid = pairs * B * H;
+  if (grid > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(N) * H * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
+
+  CUtensorMap tq, tk, tv;
+  int rc = make_map(&tq, q, d, H, N, B, kPrefillBM);
+  if (rc == FA_OK) rc = make_map(&tk, k, d, Hkv, N, B, kPrefillBN);
+  if (rc == FA_OK) rc = make_map(&tv, v, d, Hkv, N, B, kPrefillBN);
+  if (rc != FA_OK) return rc;
+
+  PrefillParams p{};
+  p.status = status_ptr();
+  if (p.status == nullptr) return FA_ERR_CUDA;
+  p.out = out;
+  p.lse = lse;
+  p.cu_seqlens = nullptr;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.group = H / Hkv;
+  p.N = N;
+  p.max_pairs = static_cast<int>(pairs);
+  p.total_tokens = 0;
+  p.scale_log2 = scale * kLog2e;
+  p.causal = causal;
+  cudaError_t e = launch_prefill(tq, tk, tv, p, d, causal != 0, false, static_cast<int>(grid),
+                                 reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float *lse,
+                  const int32_t *cu_seqlens, int num_seqs, int total_tokens, int max_seqlen,
+                  int H, int Hkv, int d, float scale, int causal, fa_stream_t stream) {
+  if (!q || !k || !v || !out || !cu_seqlens) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+    return FA_ERR_INVALID_ARG;
+  if (!aligned(cu_seqlens, 4) || (lse && !aligned(lse, 4))) return FA_ERR_INVALID_ARG;
+  if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0) return FA_ERR_INVALID_ARG;
+  if (H < 1 || Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (num_seqs == 0 || total_tokens == 0 || max_seqlen == 0) return FA_OK;
+  if (max_seqlen > total_tokens) max_seqlen = total_tokens;
+  const long long pairs = (max_seqlen + kPrefillRowsPerCta - 1) / kPrefillRowsPerCta;
+  const long long grid = pairs * num_seqs * H;
+  if (grid > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(total_tokens) * H * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
+
+  CUtensorMap tq, tk, tv;
+  int rc = make_map(&tq, q, d, H, total_tokens, 1, kPrefillBM);
+  if (rc == FA_OK) rc = make_map(&tk, k, d, Hkv, total_tokens, 1, kPrefillBN);
+  if (rc == FA_OK) rc = make_map(&tv, v, d, Hkv, total_tokens, 1, kPrefillBN);
+  if (rc != FA_OK) return rc;
+
+  PrefillParams p{};
+  p.status = status_ptr();
+  if (p.status == nullptr) return FA_ERR_CUDA;
+  p.out = out;
+  p.lse = lse;
+  p.cu_seqlens = cu_seqlens;
+  p.B = num_seqs;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.group = H / Hkv;
+  p.N = total_tokens;
+  p.max_pairs = static_cast<int>(pairs);
+  p.total_tokens = total_tokens;
+  p.scale_log2 = scale * kLog2e;
+  p.causal = causal;
+  cudaError_t e = launch_prefill(tq, tk, tv, p, d, causal != 0, true, static_cast<int>(grid),
+                                 reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_decode_workspace_size(int batch, int H, int Hkv, int d, int max_ctx_len,
+                                int block_size) {
+  if (batch < 0 || H < 1 || Hkv < 1 || H % Hkv != 0 || max_ctx_len < 0) return 0;
+  if ((d != 64 && d != 128) || block_size != kDecodeBlock) return 0;
+  const DecodeWs w = decode_ws(batch, H, Hkv, d, max_ctx_len);
+  return w.o_bytes + w.ml_bytes;
+}
+
+int fa_decode_paged(const void *q, const void *k_pool, const void *v_pool,
+                    const int32_t *block_table, int max_blocks_per_seq, const int32_t *ctx_lens,
+                    int max_ctx_len, int batch, int H, int Hkv, int d, int block_size,
+                    int num_blocks, float scale, void *out, float *lse, void *workspace,
+                    size_t workspace_bytes, fa_stream_t stream) {
+  if (!q || !k_pool || !v_pool || !block_table || !ctx_lens || !out) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16))
+    return FA_ERR_INVALID_ARG;
+  if (!aligned(block_table, 4) || !aligned(ctx_lens, 4) || (lse && !aligned(lse, 4)))
+    return FA_ERR_INVALID_ARG;
+  if (batch < 0 || H < 1 || Hkv < 1 || H % Hkv != 0 || num_blocks < 1 ||
+      max_blocks_per_seq < 1 || max_ctx_len < 0)
+    return FA_ERR_INVALID_ARG;
+  if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (block_size != kDecodeBlock) return FA_ERR_UNSUPPORTED;
+  if (H / Hkv > 16) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(max_blocks_per_seq) * block_size < max_ctx_len)
+    return FA_ERR_INVALID_ARG;
+  if (batch > 65535 || Hkv > 65535) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (batch == 0) return FA_OK;
+  const DecodeWs w = decode_ws(batch, H, Hkv, d, max_ctx_len);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.o_bytes + w.ml_bytes)
+    return FA_ERR_WORKSPACE;
+
+  CUtensorMap tk, tv;
+  const long long tokens = static_cast<long long>(num_blocks) * block_size;
+  int rc = make_pool_map(&tk, k_pool, d, Hkv, tokens);
+  if (rc == FA_OK) rc = make_pool_map(&tv, v_pool, d, Hkv, tokens);
+  if (rc != FA_OK) return rc;
+
+  DecodeParams p{};
+  p.status = status_ptr();
+  if (p.status == nullptr) return FA_ERR_CUDA;
+  p.q = q;
+  p.block_table = block_table;
+  p.ctx_lens = ctx_lens;
+  p.o_part = static_cast<float *>(workspace);
+  p.ml_part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + w.o_bytes);
+  p.out = out;
+  p.lse = lse;
+  p.batch = batch;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.group = H / Hkv;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.max_ctx_len = max_ctx_len;
+  p.num_blocks = num_blocks;
+  p.split_tokens = w.split_tokens;
+  p.max_splits = w.max_splits;
+  p.scale_log2 = scale * kLog2e;
+  cudaError_t e = launch_decode(tk, tv, p, d, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // extern "C"

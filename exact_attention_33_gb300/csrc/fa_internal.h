@@ -1,0 +1,64 @@
+// fa_internal.h - parameter blocks and constants shared by the host glue
+// (fa_api.cu) and the kernels.  Plain structs passed to kernels by value.
+#pragma once
+
+#include <stdint.h>
+
+#include "../../include/fa.h"
+
+namespace fa {
+
+// Bound for every on-chip spin-wait (nanoseconds of %globaltimer).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// ------------------------------------------------------------------ prefill
+
+// Tile shape of the prefill kernel: each CTA owns two 128-row query tiles
+// (one per softmax warpgroup) of one (sequence, head) and streams 128-key
+// K/V tiles through shared memory.
+constexpr int kPrefillBM = 128;
+constexpr int kPrefillBN = 128;
+constexpr int kPrefillQTiles = 2;
+constexpr int kPrefillRowsPerCta = kPrefillBM * kPrefillQTiles;
+constexpr int kPrefillThreads = 320;  // 8 softmax warps + 1 MMA warp + 1 TMA warp
+
+struct PrefillParams {
+  unsigned int *status;   // per-device sticky FA_DEV_* word
+  void *out;              // bf16 [rows, H, d] (dense rows = B*N, varlen rows = T)
+  float *lse;             // fp32, may be null
+  const int32_t *cu_seqlens;  // varlen only
+  int B;                  // dense: batch; varlen: number of sequences
+  int H, Hkv, group;      // group = H / Hkv
+  int N;                  // dense: sequence length; varlen: total tokens
+  int max_pairs;          // number of 256-row query-tile pairs of the longest sequence
+  int total_tokens;       // varlen: T
+  float scale_log2;       // scale * log2(e)
+  int causal;
+};
+
+// ------------------------------------------------------------------- decode
+
+constexpr int kDecodeBlock = 16;     // tokens per KV block (paged pool granularity)
+constexpr int kDecodeStages = 4;     // KV blocks in flight per CTA
+constexpr int kCombineWarps = 4;
+constexpr int kDecodeMaxSplitTokens = 512;  // one block-table entry per lane of the split warp
+
+struct DecodeParams {
+  unsigned int *status;     // per-device sticky FA_DEV_* word
+  const void *q;            // bf16 [batch, H, d]
+  const int32_t *block_table;
+  const int32_t *ctx_lens;
+  float *o_part;            // fp32 [batch, H, max_splits, d]
+  float *ml_part;           // fp32 [batch, H, max_splits, 2]  (m in log2 units, l)
+  void *out;                // bf16 [batch, H, d]
+  float *lse;               // fp32 [batch, H] or null
+  int batch, H, Hkv, group;
+  int max_blocks_per_seq;
+  int max_ctx_len;
+  int num_blocks;
+  int split_tokens;         // multiple of kDecodeBlock
+  int max_splits;
+  float scale_log2;
+};
+
+}  // namespace fa

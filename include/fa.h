@@ -1,0 +1,156 @@
+/*
+ * fa.h - C ABI of the GB300 (sm_103a) exact-attention library (libfa.so).
+ *
+ * Exact scaled-dot-product attention computed as a tiled, IO-aware
+ * streaming recurrence: key/value tiles are staged on chip, the score tile
+ * S = scale * Q K^T is formed per tile and never written to device memory,
+ * and the softmax is folded in online with a running row maximum m, a
+ * running sum l and the rescale factor alpha = exp(m_old - m_new); the
+ * output accumulator o is finished as o / l.
+ *   Sources: "S12 FlashAttention" (llminference.xinbetween.com/en/s12/),
+ *   sections "Core idea", "How it works" (the recurrence diagram),
+ *   "What this unlocks beyond speed" and "Implementation"; the FlashAttention
+ *   explainer (tachyon.techntrek.in/learn/flash-attention), "Show the maths";
+ *   and "FlashAttention: The Algorithm That Beat the Memory Wall"
+ *   (repo-explainer.com/hillfate/flash-attention), sections "A Tile, a
+ *   Register File, and a Trick Called Online Softmax" and "Varlen Is the
+ *   Quiet Superpower".
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All tensor arguments are DEVICE pointers owned by the caller; the
+ *    library never allocates, frees or synchronises on the compute path.
+ *    Every call is asynchronous on `stream` (NULL = legacy default stream).
+ *  - bf16 = IEEE bfloat16; fp32 accumulation; outputs are rounded to
+ *    bf16 (round to nearest even), the log-sum-exp is fp32.
+ *  - Element layouts are dense row-major with the innermost dimension last;
+ *    q/k/v/out and pools must be 16-byte aligned (TMA requirement).
+ *  - GQA: query head h reads key/value head h / (H / Hkv).
+ *  - `scale` multiplies q.k before the softmax; it must be finite and > 0
+ *    (the usual value is 1/sqrt(d)).
+ *  - lse (optional, may be NULL) receives the natural-log log-sum-exp of the
+ *    scaled scores of each query row: LSE = m + ln(l).
+ *  - Return value: FA_OK, or a negative fa_status.  Argument errors are
+ *    detected on the host before any launch and launch nothing.  Launch
+ *    failures return FA_ERR_CUDA.  Data errors that only the device can see
+ *    (an out-of-range block id, a bad context length, a pipeline wait that
+ *    ran out of time) set bits of a per-device sticky status word that
+ *    fa_device_status() reads; the affected work is skipped, never trapped.
+ *  - Supported head sizes: d in {64, 128}.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same underlying type as cudaStream_t. */
+typedef struct CUstream_st *fa_stream_t;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = -1, /* null pointer, bad size, misalignment, H % Hkv != 0 ... */
+  FA_ERR_UNSUPPORTED = -2, /* valid request outside what is built (e.g. d = 96)      */
+  FA_ERR_CUDA = -3,        /* a CUDA runtime/driver call or a launch failed          */
+  FA_ERR_WORKSPACE = -4    /* decode workspace missing, misaligned or too small      */
+} fa_status;
+
+/* Bits of the per-device sticky status word. */
+#define FA_DEV_TIMEOUT 1u     /* a bounded on-chip pipeline wait gave up             */
+#define FA_DEV_BAD_BLOCK 2u   /* block_table entry outside [0, num_blocks)           */
+#define FA_DEV_BAD_CTX 4u     /* ctx_len < 0 or > max_blocks_per_seq * block_size    */
+#define FA_DEV_BAD_SEQLEN 8u  /* cu_seqlens not non-decreasing / beyond total_tokens */
+
+/*
+ * Dense prefill forward (causal or not).
+ *   q, out : [B, N, H, d]   bf16
+ *   k, v   : [B, N, Hkv, d] bf16
+ *   lse    : [B, H, N]      fp32, may be NULL
+ *   causal : 0 or 1; masking is bottom-right aligned (key j visible to query
+ *            i iff j <= i + (Nk - Nq)), which is j <= i here since Nq = Nk.
+ * The recurrence of "S12 FlashAttention" ("Core idea"; exercise 2 for the
+ * causal variant) over tiles of 128 keys, for tiles of 128 query rows.
+ * B == 0 or N == 0 is a no-op.
+ */
+int fa_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
+           int B, int H, int Hkv, int N, int d, float scale, int causal,
+           fa_stream_t stream);
+
+/*
+ * Packed variable-length prefill ("Varlen Is the Quiet Superpower"): the
+ * sequences are concatenated along the token axis with no padding.
+ *   q, out     : [total_tokens, H, d]   bf16
+ *   k, v       : [total_tokens, Hkv, d] bf16
+ *   lse        : [H, total_tokens]      fp32, may be NULL
+ *   cu_seqlens : int32 DEVICE array [num_seqs + 1], non-decreasing,
+ *                cu_seqlens[0] == 0, cu_seqlens[num_seqs] == total_tokens.
+ *   max_seqlen : an upper bound of every sequence length (sizes the launch).
+ * Sequence s attends only to its own tokens [cu[s], cu[s+1]); the causal
+ * rule applies per sequence.  Work items are (sequence, q-tile, head) with
+ * no padding tiles.  A cu_seqlens array that breaks the rules above sets
+ * FA_DEV_BAD_SEQLEN and the offending sequence is skipped.
+ */
+int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float *lse,
+                  const int32_t *cu_seqlens, int num_seqs, int total_tokens,
+                  int max_seqlen, int H, int Hkv, int d, float scale, int causal,
+                  fa_stream_t stream);
+
+/*
+ * Bytes of caller-owned workspace that fa_decode_paged needs for the split
+ * partial states (m, l, o) of every (sequence, query head, key split).
+ * Returns 0 for invalid arguments.  The split size depends only on these
+ * arguments and on the current device's SM count.
+ */
+size_t fa_decode_workspace_size(int batch, int H, int Hkv, int d, int max_ctx_len,
+                                int block_size);
+
+/*
+ * Paged GQA flash-decoding: one query token per sequence against a paged
+ * KV cache ("S12 FlashAttention": "Implementation" - the block table in front
+ * of the key access; "What this unlocks beyond speed" - split the keys across
+ * thread blocks and combine the partial (m, l, o) states; "How this composes
+ * with what you already built" - paging, GQA head sharing and the recurrence
+ * in one loop).
+ *   q, out      : [batch, H, d] bf16
+ *   k_pool,
+ *   v_pool      : [num_blocks, block_size, Hkv, d] bf16
+ *   block_table : int32 [batch, max_blocks_per_seq]; logical block j of
+ *                 sequence b is physical block block_table[b][j]
+ *   ctx_lens    : int32 [batch], 0 <= ctx_lens[b] <= max_ctx_len
+ *   lse         : [batch, H] fp32, may be NULL
+ *   workspace   : >= fa_decode_workspace_size(...) bytes, 256-byte aligned,
+ *                 owned by the caller; its contents on entry are ignored.
+ * A sequence with ctx_len 0 gets out = 0 and lse = -inf.  Slots of the last
+ * block past ctx_len are never read into the result.  Supported: block_size
+ * == 16, H / Hkv <= 16.  Two kernels run in stream order: the split kernel
+ * and the (m, l, o) combine.
+ */
+int fa_decode_paged(const void *q, const void *k_pool, const void *v_pool,
+                    const int32_t *block_table, int max_blocks_per_seq,
+                    const int32_t *ctx_lens, int max_ctx_len, int batch, int H,
+                    int Hkv, int d, int block_size, int num_blocks, float scale,
+                    void *out, float *lse, void *workspace, size_t workspace_bytes,
+                    fa_stream_t stream);
+
+/* Human-readable text of an fa_status value (static storage). */
+const char *fa_status_string(int status);
+
+/*
+ * Read the sticky device status word of the current device into *status
+ * (FA_DEV_* bits; 0 = no device-side error since the last clear) and clear
+ * it when `clear` != 0.  This call synchronises the device.
+ */
+int fa_device_status(unsigned int *status, int clear);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,104 @@
+"""CPU-only checks of the C ABI: the library builds, loads, exports every
+symbol declared in include/fa.h, and rejects bad arguments on the host
+before touching the GPU (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_33_gb300.build import build
+    path = build()
+    import exact_attention_33_gb300 as fa
+    assert os.path.samefile(path, fa.library_path())
+    return fa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(fa_[a-z_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["fa_fwd", "fa_fwd_varlen", "fa_decode_paged", "fa_decode_workspace_size",
+              "fa_status_string", "fa_device_status", "fa_version"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in fa.h but not exported"
+
+
+def test_status_strings(lib):
+    import exact_attention_33_gb300 as fa
+    assert fa.fa_status_string(0) == "ok"
+    for s in (-1, -2, -3, -4):
+        assert fa.fa_status_string(s) not in ("ok", "unknown status")
+    assert fa.fa_version() >= 100
+
+
+P = ctypes.c_void_p(0x10000)   # never dereferenced: validation fails first
+P_BAD = ctypes.c_void_p(0x10008)
+NULL = ctypes.c_void_p(0)
+
+
+def fwd(lib, q=P, k=P, v=P, out=P, lse=NULL, B=1, H=2, Hkv=2, N=16, d=64, scale=0.125,
+        causal=0):
+    return lib.fa_fwd(q, k, v, out, lse, B, H, Hkv, N, d, scale, causal, NULL)
+
+
+def test_fwd_host_validation(lib):
+    assert fwd(lib, q=NULL) == -1
+    assert fwd(lib, k=P_BAD) == -1           # not 16-byte aligned
+    assert fwd(lib, H=3, Hkv=2) == -1         # H % Hkv != 0
+    assert fwd(lib, causal=2) == -1
+    assert fwd(lib, scale=float("nan")) == -1
+    assert fwd(lib, scale=-1.0) == -1
+    assert fwd(lib, d=96) == -2
+    assert fwd(lib, d=256) == -2
+    assert fwd(lib, B=0) == 0                 # empty problem: no launch, success
+    assert fwd(lib, N=0) == 0
+
+
+def test_varlen_host_validation(lib):
+    f = lib.fa_fwd_varlen
+    assert f(P, P, P, P, NULL, NULL, 2, 10, 5, 2, 2, 64, 0.1, 0, NULL) == -1   # no cu_seqlens
+    assert f(P, P, P, P, NULL, P, -1, 10, 5, 2, 2, 64, 0.1, 0, NULL) == -1
+    assert f(P, P, P, P, NULL, P, 2, 10, 5, 2, 2, 80, 0.1, 0, NULL) == -2
+    assert f(P, P, P, P, NULL, P, 0, 10, 5, 2, 2, 64, 0.1, 0, NULL) == 0
+
+
+def test_decode_host_validation(lib):
+    f = lib.fa_decode_paged
+    base = dict(max_blocks=4, max_ctx=64, batch=2, H=8, Hkv=2, d=128, bs=16, nb=8)
+
+    def call(ws=P, ws_bytes=1 << 20, **kw):
+        a = dict(base, **kw)
+        return f(P, P, P, P, a["max_blocks"], P, a["max_ctx"], a["batch"], a["H"], a["Hkv"],
+                 a["d"], a["bs"], a["nb"], 0.1, P, NULL, ws, ws_bytes, NULL)
+    assert call(bs=32) == -2                  # only 16-token blocks are built
+    assert call(H=64, Hkv=2) == -2            # group of 32 query heads per KV head
+    assert call(max_ctx=65) == -1             # table cannot hold that many tokens
+    assert call(H=7) == -1
+    assert call(batch=0) == 0
+    assert call(ws=NULL) == -4
+    assert call(ws_bytes=16) == -4
+    assert call(ws=ctypes.c_void_p(0x10010)) == -4   # not 256-byte aligned
+
+
+def test_workspace_size(lib):
+    import exact_attention_33_gb300 as fa
+    n = fa.fa_decode_workspace_size(64, 32, 8, 128, 32768, 16)
+    assert n >= 64 * 32 * 128 * 4 and n % 256 == 0
+    assert fa.fa_decode_workspace_size(1, 32, 8, 128, 1024, 32) == 0
+    assert fa.fa_decode_workspace_size(1, 30, 8, 128, 1024, 16) == 0

@@ -1,0 +1,118 @@
+"""GPU parity of the dense prefill path (fa_fwd) against the fp64 oracle."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from exact_attention_33_gb300 import workloads as W
+from gpu_helpers import assert_device_clean, compare, dev_bf16, host_f64, torch_mod
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa():
+    from exact_attention_33_gb300.build import build
+    build()
+    import exact_attention_33_gb300 as fa_mod
+    fa_mod.fa_device_status(clear=True)
+    return fa_mod
+
+
+def run_dense(fa, inp, causal, scale=None):
+    torch = torch_mod()
+    q, k, v = dev_bf16(inp.q), dev_bf16(inp.k), dev_bf16(inp.v)
+    out, lse = fa.fa_fwd(q, k, v, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    return host_f64(out), lse.cpu().numpy().astype(np.float64)
+
+
+def f64(bits):
+    return W.bf16_bits_to_f64(bits)
+
+
+def test_pr1_reference_case(fa):
+    cfg = W.WORKLOADS["pr1"]
+    inp = W.dense_inputs(cfg["B"], cfg["N"], cfg["H"], cfg["Hkv"], cfg["d"], seed=0)
+    out, lse = run_dense(fa, inp, causal=False, scale=1 / 8)
+    o_ref, l_ref = oracle.attention_dense(f64(inp.q), f64(inp.k), f64(inp.v), scale=1 / 8)
+    compare(out, o_ref, lse, l_ref, "pr1")
+    assert_device_clean()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,N,H,Hkv", [(1, 1, 2, 2), (2, 77, 4, 2), (1, 128, 2, 1),
+                                       (2, 300, 4, 4), (1, 513, 2, 2), (1, 1000, 8, 1)])
+def test_dense_small(fa, d, causal, B, N, H, Hkv):
+    inp = W.dense_inputs(B, N, H, Hkv, d, seed=100 + N)
+    out, lse = run_dense(fa, inp, causal)
+    o_ref, l_ref = oracle.attention_dense(f64(inp.q), f64(inp.k), f64(inp.v), causal=causal)
+    compare(out, o_ref, lse, l_ref, f"dense B{B} N{N} H{H}/{Hkv} d{d} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dense_d64_config(fa, causal):
+    cfg = W.WORKLOADS["dense_d64"]
+    inp = W.dense_inputs(cfg["B"], cfg["N"], cfg["H"], cfg["Hkv"], cfg["d"], seed=0)
+    out, lse = run_dense(fa, inp, causal)
+    o_ref, l_ref = oracle.attention_dense(f64(inp.q), f64(inp.k), f64(inp.v), causal=causal)
+    compare(out, o_ref, lse, l_ref, f"dense_d64 causal={causal}")
+    assert_device_clean()
+
+
+@pytest.fixture(scope="module")
+def long_inputs():
+    cfg = W.WORKLOADS["long_causal_d128"]
+    return W.dense_inputs(cfg["B"], cfg["N"], cfg["H"], cfg["Hkv"], cfg["d"], seed=0,
+                          outlier_frac=cfg["outlier_frac"], outlier_scale=cfg["outlier_scale"])
+
+
+def test_long_causal_config_sampled(fa, long_inputs):
+    """Full-size launch; the oracle evaluates 4 seeded (batch, head) pairs."""
+    inp = long_inputs
+    out, lse = run_dense(fa, inp, causal=True)
+    rng = np.random.default_rng(5)
+    pairs = [(int(x) // inp.H, int(x) % inp.H) for x in rng.choice(inp.B * inp.H, 4, replace=False)]
+    for b, h in pairs:
+        g = h // (inp.H // inp.Hkv)
+        o_ref, l_ref = oracle.attention_one(f64(inp.q[b][:, h:h + 1]), f64(inp.k[b][:, g:g + 1]),
+                                            f64(inp.v[b][:, g:g + 1]), causal=True)
+        compare(out[b, :, h], o_ref[:, 0], lse[b, h], l_ref[0], f"long b{b} h{h}")
+    assert np.all(np.isfinite(out))
+    assert_device_clean()
+
+
+def test_deterministic(fa):
+    torch = torch_mod()
+    inp = W.dense_inputs(2, 700, 4, 2, 128, seed=7)
+    q, k, v = dev_bf16(inp.q), dev_bf16(inp.k), dev_bf16(inp.v)
+    o1, l1 = fa.fa_fwd(q, k, v, causal=True)
+    o2, l2 = fa.fa_fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_explicit_scale_and_no_lse(fa):
+    torch = torch_mod()
+    inp = W.dense_inputs(1, 200, 2, 2, 64, seed=8)
+    q, k, v = dev_bf16(inp.q), dev_bf16(inp.k), dev_bf16(inp.v)
+    out, lse = fa.fa_fwd(q, k, v, causal=False, scale=0.3, want_lse=False)
+    torch.cuda.synchronize()
+    assert lse is None
+    o_ref, _ = oracle.attention_dense(f64(inp.q), f64(inp.k), f64(inp.v), scale=0.3)
+    compare(host_f64(out), o_ref, what="scale 0.3")
+
+
+def test_rejects_bad_arguments(fa):
+    torch = torch_mod()
+    q = torch.zeros((1, 8, 2, 96), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fa.FaError) as e:
+        fa.fa_fwd(q, q, q)
+    assert e.value.status == -2
+    q = torch.zeros((1, 8, 3, 64), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((1, 8, 2, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fa.FaError) as e:
+        fa.fa_fwd(q, k, k)
+    assert e.value.status == -1
