@@ -201,56 +201,77 @@ def to_dev(bits, torch, device):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
 
 
-def build_step(torch, device):
-    """Create the three workloads on the device; returns a dict of legs."""
-    cfg_l = W.WORKLOADS["long_causal_d128"]
-    long_in = W.dense_inputs(cfg_l["B"], cfg_l["N"], cfg_l["H"], cfg_l["Hkv"], cfg_l["d"], seed=0,
-                             outlier_frac=cfg_l["outlier_frac"],
-                             outlier_scale=cfg_l["outlier_scale"])
-    cfg_v = W.WORKLOADS["varlen_gqa_d128"]
-    lengths = W.varlen_lengths(cfg_v["num_seqs"], cfg_v["len_lo"], cfg_v["len_hi"])
-    var_in = W.varlen_inputs(lengths, cfg_v["H"], cfg_v["Hkv"], cfg_v["d"], seed=0)
-    cfg_d = W.WORKLOADS["paged_decode_gqa_d128"]
-    ctx = W.decode_ctx_lens(cfg_d["batch"], cfg_d["ctx_lo"], cfg_d["ctx_hi"])
-    dec_in = W.decode_inputs(ctx, cfg_d["H"], cfg_d["Hkv"], cfg_d["d"], cfg_d["block_size"], seed=0)
-
+def build_step(torch, device, which=("long", "varlen", "decode"), decode_batch=None):
+    """Create the selected workloads on the device; returns a dict of legs."""
+    import exact_attention_33_gb300 as fa
     legs = {}
+    if "long" in which:
+        cfg_l = W.WORKLOADS["long_causal_d128"]
+        long_in = W.dense_inputs(cfg_l["B"], cfg_l["N"], cfg_l["H"], cfg_l["Hkv"], cfg_l["d"],
+                                 seed=0, outlier_frac=cfg_l["outlier_frac"],
+                                 outlier_scale=cfg_l["outlier_scale"])
+        _add_long(legs, long_in, cfg_l)
+    if "varlen" in which:
+        cfg_v = W.WORKLOADS["varlen_gqa_d128"]
+        lengths = W.varlen_lengths(cfg_v["num_seqs"], cfg_v["len_lo"], cfg_v["len_hi"])
+        var_in = W.varlen_inputs(lengths, cfg_v["H"], cfg_v["Hkv"], cfg_v["d"], seed=0)
+        _add_varlen(legs, var_in, lengths, cfg_v)
+    if "decode" in which:
+        cfg_d = W.WORKLOADS["paged_decode_gqa_d128"]
+        ctx = W.decode_ctx_lens(cfg_d["batch"], cfg_d["ctx_lo"], cfg_d["ctx_hi"])
+        if decode_batch is not None:
+            ctx = ctx[:decode_batch]
+        dec_in = W.decode_inputs(ctx, cfg_d["H"], cfg_d["Hkv"], cfg_d["d"], cfg_d["block_size"],
+                                 seed=0)
+        _add_decode(legs, dec_in, cfg_d)
+    for leg in legs.values():
+        leg["dev"] = {k: to_dev(v, torch, device) for k, v in leg["host"].items()}
+    if "long" in legs:
+        lq = legs["long"]["dev"]["q"]
+        B, N, H, Hkv, d = legs["long"]["shape"]
+        legs["long"]["out"] = torch.empty_like(lq)
+        legs["long"]["lse"] = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    if "varlen" in legs:
+        legs["varlen"]["cu_dev"] = torch.from_numpy(legs["varlen"]["cu"]).to(device)
+        vq = legs["varlen"]["dev"]["q"]
+        legs["varlen"]["out"] = torch.empty_like(vq)
+        legs["varlen"]["lse"] = torch.empty((vq.shape[1], vq.shape[0]), dtype=torch.float32,
+                                            device=device)
+    if "decode" in legs:
+        leg = legs["decode"]
+        leg["table_dev"] = torch.from_numpy(leg["table"]).to(device)
+        leg["ctx_dev"] = torch.from_numpy(leg["ctx"]).to(device)
+        dq = leg["dev"]["q"]
+        leg["out"] = torch.empty_like(dq)
+        leg["lse"] = torch.empty(dq.shape[:2], dtype=torch.float32, device=device)
+        ws = fa.fa_decode_workspace_size(dq.shape[0], dq.shape[1], leg["Hkv"], dq.shape[2],
+                                         leg["max_ctx"], 16)
+        leg["ws"] = torch.empty(ws, dtype=torch.uint8, device=device)
+    return legs
+
+
+def _add_long(legs, long_in, cfg_l):
     legs["long"] = dict(
         host={"q": long_in.q, "k": long_in.k, "v": long_in.v},
         flops=W.prefill_flops(cfg_l["B"], cfg_l["N"], cfg_l["H"], cfg_l["d"], True),
         shape=(cfg_l["B"], cfg_l["N"], cfg_l["H"], cfg_l["Hkv"], cfg_l["d"]))
+
+
+def _add_varlen(legs, var_in, lengths, cfg_v):
     legs["varlen"] = dict(
         host={"q": var_in.q, "k": var_in.k, "v": var_in.v},
         cu=var_in.cu_seqlens, max_seqlen=var_in.max_seqlen,
         flops=W.varlen_flops(lengths, cfg_v["H"], cfg_v["d"], True),
         total_tokens=var_in.total_tokens)
+
+
+def _add_decode(legs, dec_in, cfg_d):
     legs["decode"] = dict(
         host={"q": dec_in.q, "k_pool": dec_in.k_pool, "v_pool": dec_in.v_pool},
         table=dec_in.block_table, ctx=dec_in.ctx_lens, max_ctx=dec_in.max_ctx_len,
         bytes=W.decode_bytes(dec_in.ctx_lens, cfg_d["H"], cfg_d["Hkv"], cfg_d["d"],
-                             dec_in.block_table.shape[1], cfg_d["block_size"]))
-    for leg in legs.values():
-        leg["dev"] = {k: to_dev(v, torch, device) for k, v in leg["host"].items()}
-    legs["varlen"]["cu_dev"] = torch.from_numpy(legs["varlen"]["cu"]).to(device)
-    legs["decode"]["table_dev"] = torch.from_numpy(dec_in.block_table).to(device)
-    legs["decode"]["ctx_dev"] = torch.from_numpy(dec_in.ctx_lens).to(device)
-    # outputs and workspace, allocated once
-    import exact_attention_33_gb300 as fa
-    lq = legs["long"]["dev"]["q"]
-    B, N, H, Hkv, d = legs["long"]["shape"]
-    legs["long"]["out"] = torch.empty_like(lq)
-    legs["long"]["lse"] = torch.empty((B, H, N), dtype=torch.float32, device=device)
-    vq = legs["varlen"]["dev"]["q"]
-    legs["varlen"]["out"] = torch.empty_like(vq)
-    legs["varlen"]["lse"] = torch.empty((vq.shape[1], vq.shape[0]), dtype=torch.float32,
-                                        device=device)
-    dq = legs["decode"]["dev"]["q"]
-    legs["decode"]["out"] = torch.empty_like(dq)
-    legs["decode"]["lse"] = torch.empty(dq.shape[:2], dtype=torch.float32, device=device)
-    ws = fa.fa_decode_workspace_size(dq.shape[0], dq.shape[1], cfg_d["Hkv"], cfg_d["d"],
-                                     dec_in.max_ctx_len, cfg_d["block_size"])
-    legs["decode"]["ws"] = torch.empty(ws, dtype=torch.uint8, device=device)
-    return legs
+                             dec_in.block_table.shape[1], cfg_d["block_size"]),
+        Hkv=cfg_d["Hkv"])
 
 
 def run_leg(fa, name, leg, dev):
@@ -286,7 +307,6 @@ def oracle_sample_tflops(max_seconds=20.0, rows_per_pair=None, pairs=4, seed=5):
     # one (batch, head) slice at a time keeps host memory small
     for idx in rng.choice(cfg["B"] * H, pairs, replace=False):
         b, h = int(idx) // H, int(idx) % H
-        q = W.bf16_bits_to_f64(W.normal_bf16_bits((N, H, d), 0, 0)[:, h:h + 1]) if False else None
         inp = _long_slice(b, h)
         rows = None
         if rows_per_pair is not None:
@@ -380,11 +400,12 @@ def bench_ours(args, rank, world, local):
     init_dist(world, "nccl")
     fa.load_library()
     fa.fa_device_status(clear=True)
-    legs = build_step(torch, device)
+    order = [n for n in LEG_ORDER if n in args.legs]
+    legs = build_step(torch, device, order, args.decode_batch)
     stream = torch.cuda.current_stream()
 
     def step(ev=None):
-        for i, name in enumerate(LEG_ORDER):
+        for i, name in enumerate(order):
             if ev is not None:
                 ev[i][0].record(stream)
             run_leg(fa, name, legs[name], legs[name]["dev"])
@@ -395,7 +416,7 @@ def bench_ours(args, rank, world, local):
         step()
     torch.cuda.synchronize()
 
-    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in LEG_ORDER]
+    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in order]
               for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
@@ -412,7 +433,7 @@ def bench_ours(args, rank, world, local):
         time.sleep(0.2)
     total_ms = t_start.elapsed_time(t_end)
     leg_ms = {name: [events[it][i][0].elapsed_time(events[it][i][1]) for it in range(args.steps)]
-              for i, name in enumerate(LEG_ORDER)}
+              for i, name in enumerate(order)}
     status = fa.fa_device_status(clear=True)
     if status != 0:
         raise RuntimeError(f"device status word set during the bench: {status:#x}")
@@ -420,20 +441,20 @@ def bench_ours(args, rank, world, local):
     # ---- end to end: pinned host inputs in, results out, inside the timed region
     pinned = {name: {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16))
                      .view(torch.bfloat16).pin_memory()
-                     for k, v in legs[name]["host"].items()} for name in LEG_ORDER}
+                     for k, v in legs[name]["host"].items()} for name in order}
     host_out = {name: (torch.empty(legs[name]["out"].shape, dtype=torch.bfloat16).pin_memory(),
                        torch.empty(legs[name]["lse"].shape, dtype=torch.float32).pin_memory())
-                for name in LEG_ORDER}
-    h2d = sum(t.numel() * t.element_size() for n in LEG_ORDER for t in pinned[n].values())
+                for name in order}
+    h2d = sum(t.numel() * t.element_size() for n in order for t in pinned[n].values())
     d2h = sum(o.numel() * o.element_size() + l.numel() * l.element_size()
               for o, l in host_out.values())
     e2e_steps = max(1, min(args.steps, 10))
-    e2e_ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in LEG_ORDER]
+    e2e_ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in order]
               for _ in range(e2e_steps)]
     barrier(world)
     torch.cuda.synchronize()
     for it in range(e2e_steps):
-        for i, name in enumerate(LEG_ORDER):
+        for i, name in enumerate(order):
             leg = legs[name]
             e2e_ev[it][i][0].record(stream)
             for k, t in pinned[name].items():
@@ -445,37 +466,57 @@ def bench_ours(args, rank, world, local):
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = {name: [e2e_ev[it][i][0].elapsed_time(e2e_ev[it][i][1]) for it in range(e2e_steps)]
-              for i, name in enumerate(LEG_ORDER)}
+              for i, name in enumerate(order)}
 
-    # ---- numbers (max over ranks of the time)
-    dev_idx = device
-    t_long = max_over_ranks(sum(leg_ms["long"]) / 1e3, world, dev_idx)
-    t_var = max_over_ranks(sum(leg_ms["varlen"]) / 1e3, world, dev_idx)
-    t_dec = max_over_ranks(sum(leg_ms["decode"]) / 1e3, world, dev_idx)
-    t_total = max_over_ranks(total_ms / 1e3, world, dev_idx)
+    # ---- numbers (max over ranks of each time)
     K = args.steps
-    f_long, f_var = legs["long"]["flops"], legs["varlen"]["flops"]
-    dbytes = legs["decode"]["bytes"]
-    prefill_tflops = weak_scaling_value((f_long + f_var) * K, world, t_long + t_var) / 1e12
-    decode_gbs = weak_scaling_value(dbytes * K, world, t_dec) / 1e9
-    e2e_pre = max_over_ranks((sum(e2e_ms["long"]) + sum(e2e_ms["varlen"])) / 1e3, world, dev_idx)
-    e2e_dec = max_over_ranks(sum(e2e_ms["decode"]) / 1e3, world, dev_idx)
-    e2e_tflops = weak_scaling_value((f_long + f_var) * e2e_steps, world, e2e_pre) / 1e12
-    e2e_gbs = weak_scaling_value(dbytes * e2e_steps, world, e2e_dec) / 1e9
+    t = {n: max_over_ranks(sum(leg_ms[n]) / 1e3, world, device) for n in order}
+    te = {n: max_over_ranks(sum(e2e_ms[n]) / 1e3, world, device) for n in order}
+    t_total = max_over_ranks(total_ms / 1e3, world, device)
+    pre = [n for n in ("long", "varlen") if n in order]
+    f_pre = sum(legs[n]["flops"] for n in pre)
+    prefill_tflops = (weak_scaling_value(f_pre * K, world, sum(t[n] for n in pre)) / 1e12
+                      if pre else None)
+    e2e_tflops = (weak_scaling_value(f_pre * e2e_steps, world, sum(te[n] for n in pre)) / 1e12
+                  if pre else None)
+    dbytes = legs["decode"]["bytes"] if "decode" in order else None
+    decode_gbs = weak_scaling_value(dbytes * K, world, t["decode"]) / 1e9 if dbytes else None
+    e2e_gbs = weak_scaling_value(dbytes * e2e_steps, world, te["decode"]) / 1e9 if dbytes else None
 
     if rank != 0:
         return 0
     peaks = measured_peaks()
     clk = clocks.summary()
-    long_launch_s = statistics.mean(leg_ms["long"]) / 1e3
-    dec_launch_s = statistics.mean(leg_ms["decode"]) / 1e3
     timed_s = total_ms / 1e3
     tensor_peak = peaks["bf16_tflops_sustained"] if timed_s > 2.0 else peaks["bf16_tflops"]
-    ach_long = f_long / long_launch_s / 1e12
-    ach_dec = dbytes / dec_launch_s / 1e9
-    tr_p = profiled_traffic("prefill")
-    tr_d = profiled_traffic("decode")
-    cpu_tf, cpu_desc, _ = oracle_sample_tflops(max_seconds=args.cpu_seconds)
+    leg_info, roof, roof_dec = {}, None, None
+    if "long" in order:
+        f = legs["long"]["flops"]
+        leg_info["long_causal_prefill"] = {"ms": 1e3 * t["long"] / K,
+                                           "tflops": f * K / t["long"] / 1e12}
+        ach = f / (statistics.mean(leg_ms["long"]) / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": "prefill_kernel<128,causal> (long-context launch)",
+                "achieved": ach, "peak": tensor_peak, "unit": "TFLOP/s",
+                "frac": ach / tensor_peak, "traffic": profiled_traffic("prefill"),
+                "peak_source": peaks["source"] + (" sustained" if timed_s > 2.0 else " burst")}
+    if "varlen" in order:
+        f = legs["varlen"]["flops"]
+        leg_info["varlen_causal_prefill"] = {"ms": 1e3 * t["varlen"] / K,
+                                             "tflops": f * K / t["varlen"] / 1e12}
+    if "decode" in order:
+        leg_info["paged_decode"] = {"ms": 1e3 * t["decode"] / K,
+                                    "gbs": dbytes * K / t["decode"] / 1e9}
+        ach = dbytes / (statistics.mean(leg_ms["decode"]) / 1e3) / 1e9
+        roof_dec = {"bound": "hbm", "kernel": "decode_split_kernel + decode_combine_kernel",
+                    "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": ach / peaks["hbm_gbs"], "traffic": profiled_traffic("decode"),
+                    "peak_source": peaks["source"]}
+    if args.cpu_seconds > 0:
+        cpu_tf, cpu_desc, _ = oracle_sample_tflops(max_seconds=args.cpu_seconds)
+        cpu = {"value": cpu_tf, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": cpu_desc}
+    else:
+        cpu = None
     line = {
         "metric": METRIC,
         "value": prefill_tflops,
@@ -494,34 +535,26 @@ def bench_ours(args, rank, world, local):
                         "(1% x8 key outliers) + packed varlen causal prefill 32 seqs U[64,4096] "
                         "H16/Hkv4 d128 + paged GQA decode batch64 H32/Hkv8 d128 ctx U[512,32768] "
                         "block16",
-            "prefill_flops_per_step": f_long + f_var,
+            "legs": order,
+            "decode_batch": args.decode_batch or 64,
+            "prefill_flops_per_step": f_pre,
             "decode_bytes_per_step": dbytes,
             "l2": "every input is larger than L2 (no flush needed)",
             "parallelism": f"replicas x{world}",
         },
-        "decode": {"value": decode_gbs, "unit": "GB/s",
-                   "frac_of_8tbs": decode_gbs / world / NOMINAL_HBM_GBS,
-                   "frac_of_measured": decode_gbs / world / peaks["hbm_gbs"],
-                   "ms_per_step": 1e3 * t_dec / K},
-        "legs": {
-            "long_causal_prefill": {"ms": 1e3 * t_long / K, "tflops": f_long * K / t_long / 1e12},
-            "varlen_causal_prefill": {"ms": 1e3 * t_var / K, "tflops": f_var * K / t_var / 1e12},
-            "paged_decode": {"ms": 1e3 * t_dec / K, "gbs": dbytes * K / t_dec / 1e9},
-        },
-        "roofline": {"bound": "tensor", "kernel": "prefill_kernel<128,causal> (long-context launch)",
-                     "achieved": ach_long, "peak": tensor_peak, "unit": "TFLOP/s",
-                     "frac": ach_long / tensor_peak, "traffic": tr_p,
-                     "peak_source": peaks["source"] + (" sustained" if timed_s > 2.0 else " burst")},
-        "roofline_decode": {"bound": "hbm", "kernel": "decode_split_kernel + decode_combine_kernel",
-                            "achieved": ach_dec, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                            "frac": ach_dec / peaks["hbm_gbs"], "traffic": tr_d,
-                            "peak_source": peaks["source"]},
+        "decode": None if dbytes is None else {
+            "value": decode_gbs, "unit": "GB/s",
+            "frac_of_8tbs": decode_gbs / world / NOMINAL_HBM_GBS,
+            "frac_of_measured": decode_gbs / world / peaks["hbm_gbs"],
+            "ms_per_step": 1e3 * t["decode"] / K},
+        "legs": leg_info,
+        "roofline": roof,
+        "roofline_decode": roof_dec,
         "e2e": {"value": e2e_tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "decode_gbs": e2e_gbs, "steps": e2e_steps},
-        "gpu_launches": sum(LAUNCHES_PER_STEP.values()) * K,
+        "gpu_launches": sum(LAUNCHES_PER_STEP[n] for n in order) * K,
         "clocks": clk,
-        "cpu_baseline": {"value": cpu_tf, "unit": "TFLOP/s", "cores": blas_threads(),
-                         "kind": "oracle", "sample": cpu_desc},
+        "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -534,8 +567,13 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
-                    help="budget of the oracle CPU-baseline sample")
+                    help="budget of the oracle CPU-baseline sample (0: skip)")
+    ap.add_argument("--legs", default="long,varlen,decode",
+                    help="comma-separated subset of the step (for profiling runs)")
+    ap.add_argument("--decode-batch", type=int, default=None,
+                    help="use only the first B decode sequences (for profiling runs)")
     args = ap.parse_args(argv)
+    args.legs = [x for x in args.legs.split(",") if x]
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_env()
