@@ -20,7 +20,8 @@ import threading
 
 __all__ = [
     "FaError", "library_path", "load_library", "fa_fwd", "fa_fwd_varlen",
-    "fa_decode_paged", "fa_decode_workspace_size", "fa_status_string", "fa_device_status",
+    "fa_decode_paged", "fa_decode_paged_noalloc", "fa_decode_workspace_size",
+    "fa_status_string", "fa_device_status",
     "fa_version", "FA_DEV_TIMEOUT", "FA_DEV_BAD_BLOCK", "FA_DEV_BAD_CTX", "FA_DEV_BAD_SEQLEN",
 ]
 
@@ -69,6 +70,9 @@ def load_library() -> ctypes.CDLL:
         lib.fa_decode_paged.argtypes = [vp, vp, vp, vp, i, vp, i, i, i, i, i, i, i, f, vp, vp,
                                         vp, sz, vp]
         lib.fa_decode_paged.restype = i
+        lib.fa_decode_paged_noalloc.argtypes = [vp, vp, vp, vp, i, vp, i, i, i, i, i, i, i, f,
+                                                vp, vp, vp]
+        lib.fa_decode_paged_noalloc.restype = i
         lib.fa_status_string.argtypes = [i]
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i]
@@ -214,4 +218,27 @@ def fa_decode_paged(q, k_pool, v_pool, block_table, ctx_lens, max_ctx_len, scale
         _stream_handle(stream))
     if rc != FA_OK:
         raise FaError("fa_decode_paged", rc)
+    return out, lse
+
+
+FA_DECODE_NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def fa_decode_paged_noalloc(q, k_pool, v_pool, block_table, ctx_lens, max_ctx_len, *, out,
+                            lse=None, scale=None, stream=None):
+    """Paged decode that allocates nothing on the device, for callers that
+    cannot call cudaMalloc (a plugin whose host framework owns all device
+    memory, or a decode loop that must avoid the implicit synchronisation of
+    cudaMalloc/cudaFree).  The split partial states live in the library's
+    static scratch array of FA_DECODE_NOALLOC_SCRATCH_BYTES; larger requests
+    are rejected.  The caller passes ``out`` (and optionally ``lse``); calls
+    whose kernels overlap on the GPU race on the shared scratch."""
+    batch, H, d = q.shape
+    num_blocks, block_size, Hkv, _ = k_pool.shape
+    rc = load_library().fa_decode_paged_noalloc(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), block_table.shape[1],
+        _ptr(ctx_lens), int(max_ctx_len), batch, H, Hkv, d, block_size, num_blocks,
+        _scale(scale, d), _ptr(out), _ptr(lse), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError("fa_decode_paged_noalloc", rc)
     return out, lse

@@ -330,3 +330,56 @@ int fa_decode_paged(const void *q, const void *k_pool, const void *v_pool,
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------
+// Allocation-free paged decode: the split partial states go to a static
+// device array instead of a caller workspace.  For callers that cannot call
+// cudaMalloc (a plugin whose host framework owns all device memory, or a
+// decode loop that must avoid cudaMalloc/cudaFree and their implicit device
+// synchronisation).  Every call on a device shares this one array.
+namespace fa {
+namespace {
+
+static __device__ __align__(256) unsigned char g_decode_scratch[FA_DECODE_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_decode_scratch on the current device.  In host code the
+// symbol is only a host-side stand-in, so the address is looked up once per
+// device with cudaGetSymbolAddress while that device is current.
+unsigned char *noalloc_scratch() {
+  constexpr int kMaxDev = 64;
+  static unsigned char *ptrs[kMaxDev] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (ptrs[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    ptrs[dev] = static_cast<unsigned char *>(p);
+  }
+  return ptrs[dev];
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" int fa_decode_paged_noalloc(const void *q, const void *k_pool, const void *v_pool,
+                                       const int32_t *block_table, int max_blocks_per_seq,
+                                       const int32_t *ctx_lens, int max_ctx_len, int batch,
+                                       int H, int Hkv, int d, int block_size, int num_blocks,
+                                       float scale, void *out, float *lse, fa_stream_t stream) {
+  // Same argument rules as fa_decode_paged (checked there); only the size of
+  // the partial states must fit the static array.
+  if (batch < 0 || H < 1 || Hkv < 1 || H % Hkv != 0 || max_ctx_len < 0)
+    return FA_ERR_INVALID_ARG;
+  if ((d != 64 && d != 128) || block_size != kDecodeBlock) return FA_ERR_UNSUPPORTED;
+  if (batch == 0) return FA_OK;
+  const DecodeWs w = decode_ws(batch, H, Hkv, d, max_ctx_len);
+  const size_t need = w.o_bytes + w.ml_bytes;
+  if (need > FA_DECODE_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
+  unsigned char *scratch = noalloc_scratch();
+  if (scratch == nullptr) return FA_ERR_CUDA;
+  return fa_decode_paged(q, k_pool, v_pool, block_table, max_blocks_per_seq, ctx_lens,
+                         max_ctx_len, batch, H, Hkv, d, block_size, num_blocks, scale, out, lse,
+                         scratch, FA_DECODE_NOALLOC_SCRATCH_BYTES, stream);
+}

@@ -136,6 +136,36 @@ int fa_decode_paged(const void *q, const void *k_pool, const void *v_pool,
                     void *out, float *lse, void *workspace, size_t workspace_bytes,
                     fa_stream_t stream);
 
+/*
+ * Paged decode that allocates nothing and takes no workspace.
+ * The pages have no counterpart of this call; it exists for callers that
+ * cannot call cudaMalloc: for example a C plugin run by a host framework that
+ * owns every device allocation and hands the plugin only its input and output
+ * buffers, or a latency-critical decode loop that must not pay the implicit
+ * device synchronisation of cudaMalloc/cudaFree.
+ * Same arguments, layouts and results as fa_decode_paged, minus the
+ * workspace.  The split partial states live in a library-owned static device
+ * array of FA_DECODE_NOALLOC_SCRATCH_BYTES bytes, which every GPU that loads
+ * the library holds until the process exits.
+ *  - A request whose partial states would need more than that (compare
+ *    fa_decode_workspace_size() with FA_DECODE_NOALLOC_SCRATCH_BYTES) returns
+ *    FA_ERR_WORKSPACE and launches nothing.
+ *  - The first call on a device looks up the array's device address on that
+ *    device (with it current); make that first call before any stream
+ *    capture.
+ *  - Every call on a device shares the one array and it keeps the last call's
+ *    contents; nothing in it needs to start at zero, because each call writes
+ *    every partial state before its combine reads it.  Calls whose kernels
+ *    overlap on the GPU (other streams, other host threads) race on the array
+ *    and must be ordered by the caller.
+ */
+#define FA_DECODE_NOALLOC_SCRATCH_BYTES (32u << 20)
+int fa_decode_paged_noalloc(const void *q, const void *k_pool, const void *v_pool,
+                            const int32_t *block_table, int max_blocks_per_seq,
+                            const int32_t *ctx_lens, int max_ctx_len, int batch, int H,
+                            int Hkv, int d, int block_size, int num_blocks, float scale,
+                            void *out, float *lse, fa_stream_t stream);
+
 /* Human-readable text of an fa_status value (static storage). */
 const char *fa_status_string(int status);
 
