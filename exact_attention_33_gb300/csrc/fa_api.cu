@@ -129,6 +129,14 @@ int decode_split_tokens(int batch, int Hkv, int max_ctx_len) {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Heads per group of the prefill CTA order: the largest divisor of H that is
+// at most 8 (consecutive heads, so GQA heads sharing a KV head stay together).
+int prefill_head_group(int H) {
+  for (int g = 8; g > 1; --g)
+    if (H % g == 0) return g;
+  return 1;
+}
+
 struct DecodeWs {
   int split_tokens;
   int max_splits;
@@ -210,6 +218,7 @@ int fa_fwd(const void *q, const void *k, const void *v, void *out, float *lse, i
   p.H = H;
   p.Hkv = Hkv;
   p.group = H / Hkv;
+  p.head_group = prefill_head_group(H);
   p.N = N;
   p.max_pairs = static_cast<int>(pairs);
   p.total_tokens = 0;
@@ -255,6 +264,7 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float 
   p.H = H;
   p.Hkv = Hkv;
   p.group = H / Hkv;
+  p.head_group = prefill_head_group(H);
   p.N = total_tokens;
   p.max_pairs = static_cast<int>(pairs);
   p.total_tokens = total_tokens;

@@ -29,6 +29,7 @@ struct PrefillParams {
   const int32_t *cu_seqlens;  // varlen only
   int B;                  // dense: batch; varlen: number of sequences
   int H, Hkv, group;      // group = H / Hkv
+  int head_group;         // heads per CTA-ordering group (divides H)
   int N;                  // dense: sequence length; varlen: total tokens
   int max_pairs;          // number of 256-row query-tile pairs of the longest sequence
   int total_tokens;       // varlen: T

@@ -34,6 +34,10 @@
 
 namespace fa {
 
+// The reference maximum of the exponentials moves only when the row maximum
+// grows by more than this many powers of two.
+constexpr float kRescaleLog2 = 8.f;
+
 template <int D>
 struct PrefillLayout {
   static constexpr int kChunkBytes = 128 * 128;        // 128 rows x 64 bf16 (one swizzle span)
@@ -93,18 +97,24 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   constexpr int S = L::kStages;
 
   // ---------------------------------------------------------- work item
-  // One CTA per (sequence, 256-row query pair, head); heads vary fastest so
-  // that CTAs sharing a KV head run together.  For causal attention the
-  // pairs with the most key tiles are launched first.
+  // One CTA per (sequence, 256-row query pair, head).  CTAs are ordered in
+  // groups of p.head_group heads of one sequence: inside a group the pair
+  // index varies slowest and the head fastest, so the CTAs running at the
+  // same time share the K/V of a few heads in L2.  For causal attention the
+  // pairs with the most key tiles come first in every group.
   const int lin = blockIdx.x;
-  const int h = lin % p.H;
-  const int r = lin / p.H;
-  int b, pair, seq_start, len;
+  const int hgs = p.head_group;
+  const int h_in = lin % hgs;
+  const int t_lin = lin / hgs;
+  const int pair_rank = t_lin % p.max_pairs;
+  const int grp = t_lin / p.max_pairs;
+  const int h = (grp % (p.H / hgs)) * hgs + h_in;
+  const int unit = grp / (p.H / hgs);  // batch element or sequence
+  const int pair = CAUSAL ? (p.max_pairs - 1 - pair_rank) : pair_rank;
+  int b, seq_start, len;
   if (VARLEN) {
-    const int s = r % p.B;
-    pair = p.max_pairs - 1 - r / p.B;
-    seq_start = p.cu_seqlens[s];
-    const int seq_end = p.cu_seqlens[s + 1];
+    seq_start = p.cu_seqlens[unit];
+    const int seq_end = p.cu_seqlens[unit + 1];
     if (seq_start < 0 || seq_end < seq_start || seq_end > p.total_tokens) {
       if (pair == 0 && h == 0) raise_status(p.status, FA_DEV_BAD_SEQLEN);
       return;
@@ -114,8 +124,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       raise_status(p.status, FA_DEV_BAD_SEQLEN);  // longer than max_seqlen: tail not covered
     b = 0;
   } else {
-    b = r % p.B;
-    pair = CAUSAL ? (p.max_pairs - 1 - r / p.B) : (r / p.B);
+    b = unit;
     seq_start = 0;
     len = p.N;
   }
@@ -307,8 +316,16 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int qi = row0 + i * kPrefillBM + row;  // query row within the sequence
     const int my_end = kv_end[i];
     const float sl2 = p.scale_log2;
-    float m = -CUDART_INF_F;  // running max, log2 units
-    float l = 0.f;            // running sum relative to m
+    const float2 sl2x2 = make_float2(sl2, sl2);
+    // Reference maximum of the exponentials, log2 units.  It follows the row
+    // maximum, but moves only when the maximum grows by more than
+    // kRescaleLog2: until then every p stays below 2^kRescaleLog2, which the
+    // fp32 sum and the bf16 P operand hold as well as values below 1.  o and
+    // l always share the reference, so o / l is the same result; O in TMEM
+    // is rescaled only when the reference moves.
+    float m_ref = -CUDART_INF_F;
+    float l = 0.f;        // running sum of the bf16 P values, relative to m_ref
+    float l_exact = 0.f;  // running sum of the fp32 exponentials, relative to m_ref
     bool ok = true;
     const int limit = CAUSAL ? min(len, qi + 1) : len;  // keys [0, limit) are visible
 
@@ -318,71 +335,86 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       if (!ok) break;
       tc_fence_after();
 
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t rr[32];
-        tmem_ld32_wait(tS + c * 32, rr);
-#pragma unroll
-        for (int t = 0; t < 32; ++t) s[c * 32 + t] = __uint_as_float(rr[t]);
-      }
+      uint32_t sr[128];
+      tmem_ld128_wait(tS, sr);
       const int nvis = limit - j * kPrefillBN;
       if (__any_sync(0xffffffffu, nvis < kPrefillBN)) {
 #pragma unroll
         for (int c = 0; c < 128; ++c)
-          if (c >= nvis) s[c] = -CUDART_INF_F;
+          if (c >= nvis) sr[c] = 0xff800000u;  // -inf
       }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+      float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+      float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
 #pragma unroll
       for (int c = 4; c < 128; c += 4) {
-        mx0 = fmaxf(mx0, s[c]);
-        mx1 = fmaxf(mx1, s[c + 1]);
-        mx2 = fmaxf(mx2, s[c + 2]);
-        mx3 = fmaxf(mx3, s[c + 3]);
+        mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
+        mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
+        mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
+        mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
       }
-      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-      const float m_new = fmaxf(m, mx * sl2);
+      const float m_new = fmaxf(m_ref, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
+      // false while nothing visible has been seen (both -inf)
+      const bool grow = m_new > m_ref + kRescaleLog2;
+      float alpha = 1.f;
+      if (grow) {
+        alpha = ex2(m_ref - m_new);  // 0 on the first visible tile
+        m_ref = m_new;
+      }
       // NaN guard ("exp(-inf - -inf) is NaN"): a row that has seen no
-      // visible key yet keeps a finite reference of 0.
-      const float m_use = (m_new == -CUDART_INF_F) ? 0.f : m_new;
-      const float alpha = ex2(m - m_use);
-      const float neg = -m_use;
-      float rs0 = 0.f, rs1 = 0.f;
-      uint32_t pk[64];
+      // visible key yet uses the finite reference 0, so every p is 0.
+      const float m_use = (m_ref == -CUDART_INF_F) ? 0.f : m_ref;
+      const float2 negm = make_float2(-m_use, -m_use);
+      // Two row sums: l sums the bf16 values that the P V product multiplies,
+      // so o / l is a weighted mean with consistent weights; l_exact sums the
+      // fp32 exponentials and gives the log-sum-exp.
+      float2 rs0 = make_float2(0.f, 0.f), rs1 = make_float2(0.f, 0.f);
+      float2 re0 = make_float2(0.f, 0.f), re1 = make_float2(0.f, 0.f);
+      // P in two halves of 64 keys, each stored to TMEM as soon as it is packed
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float p0 = ex2(fmaf(s[2 * c], sl2, neg));
-        const float p1 = ex2(fmaf(s[2 * c + 1], sl2, neg));
-        rs0 += p0;
-        rs1 += p1;
-        pk[c] = pack_bf16x2(p0, p1);
-      }
-      l = l * alpha + (rs0 + rs1);
-      {
-        uint32_t lo[32], hi[32];
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          lo[c] = pk[c];
-          hi[c] = pk[32 + c];
+        for (int c = 0; c < 32; c += 2) {
+          const int e = half * 64 + 2 * c;
+          const float2 x0 = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                  sl2x2, negm);
+          const float2 x1 = ffma2(make_float2(__uint_as_float(sr[e + 2]),
+                                              __uint_as_float(sr[e + 3])), sl2x2, negm);
+          const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
+          const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+          pk[c] = pack_bf16x2(p0.x, p0.y);
+          pk[c + 1] = pack_bf16x2(p1.x, p1.y);
+          re0 = fadd2(re0, p0);
+          re1 = fadd2(re1, p1);
+          rs0 = fadd2(rs0, bf16x2_to_float2(pk[c]));
+          rs1 = fadd2(rs1, bf16x2_to_float2(pk[c + 1]));
         }
-        tmem_st32(tS, lo);
-        tmem_st32(tS + 32, hi);
+        tmem_st32(tS + half * 32, pk);
       }
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      const float2 rs = fadd2(rs0, rs1);
+      const float2 re = fadd2(re0, re1);
+      l = l * alpha + (rs.x + rs.y);
+      l_exact = l_exact * alpha + (re.x + re.y);
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+        const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32_wait(tO + c * 32, o);
 #pragma unroll
-          for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+          for (int t = 0; t < 32; t += 2) {
+            const float2 v = fmul2(make_float2(__uint_as_float(o[t]), __uint_as_float(o[t + 1])), a2);
+            o[t] = __float_as_uint(v.x);
+            o[t + 1] = __float_as_uint(v.y);
+          }
           tmem_st32(tO + c * 32, o);
         }
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&p_full[i]);
-      m = m_new;
     }
+    const float m = m_ref;
 
     // ---------------------------------------------------- epilogue
     if (ok && my_end > 0) {
@@ -420,8 +452,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           }
         }
         if (live && p.lse != nullptr) {
-          const float lse =
-              (l > 0.f) ? (m + __log2f(l)) * 0.69314718055994530942f : -CUDART_INF_F;
+          const float lse = (l_exact > 0.f)
+                                ? (m + __log2f(l_exact)) * 0.69314718055994530942f
+                                : -CUDART_INF_F;
           if (VARLEN)
             p.lse[static_cast<size_t>(h) * p.total_tokens + seq_start + qi] = lse;
           else
