@@ -43,13 +43,18 @@ struct PrefillLayout {
   static constexpr int kChunkBytes = 128 * 128;        // 128 rows x 64 bf16 (one swizzle span)
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
-  static constexpr int kStages = (D == 128) ? 2 : 4;
+  // K and V have rings of their own: a K stage is released as soon as both
+  // S MMAs have read it, a V stage after both P V MMAs, so K loads run about
+  // two key tiles ahead of their use.
+  static constexpr int kStagesK = (D == 128) ? 3 : 6;
+  static constexpr int kStagesV = (D == 128) ? 2 : 4;
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kPrefillQTiles * kTileBytes;
-  static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kBar = kV + kStages * kTileBytes;
-  // q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_done[2], drain
-  static constexpr int kNumBars = 1 + 3 * kStages + 7;
+  static constexpr int kV = kK + kStagesK * kTileBytes;
+  static constexpr int kBar = kV + kStagesV * kTileBytes;
+  // q_full, k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], s_full[2],
+  // p_full[2], o_done[2], drain
+  static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 7;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kSmemAlloc = kBytes + 1024;     // base is aligned up to 1024 in-kernel
@@ -94,7 +99,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                    const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   using L = PrefillLayout<D>;
-  constexpr int S = L::kStages;
+  constexpr int SK = L::kStagesK;
+  constexpr int SV = L::kStagesV;
 
   // ---------------------------------------------------------- work item
   // One CTA per (sequence, 256-row query pair, head).  CTAs are ordered in
@@ -151,9 +157,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBar);
   uint64_t *q_full = bars;
   uint64_t *k_full = bars + 1;
-  uint64_t *v_full = bars + 1 + S;
-  uint64_t *kv_empty = bars + 1 + 2 * S;
-  uint64_t *s_full = bars + 1 + 3 * S;
+  uint64_t *k_empty = k_full + SK;
+  uint64_t *v_full = k_empty + SK;
+  uint64_t *v_empty = v_full + SV;
+  uint64_t *s_full = v_empty + SV;
   uint64_t *p_full = s_full + 2;
   uint64_t *o_done = p_full + 2;
   uint64_t *drain = o_done + 2;
@@ -165,10 +172,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < SK; ++s) {
       mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < SV; ++s) {
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -209,34 +219,39 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           tma_load_4d(sQ + i * L::kTileBytes + c * L::kChunkBytes, &tm_q, q_full, c * 64, h,
                       qrow, b);
       }
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n_kv; ++j) {
-        const int st = j % S;
-        if (j >= S && !mbar_wait(&kv_empty[st], ((j / S) - 1) & 1, abort_flag, p.status)) break;
         const int krow = seq_start + j * kPrefillBN;
-        mbar_arrive_expect_tx(&k_full[st], L::kTileBytes);
+        const int sk = j % SK;
+        if (j >= SK && !mbar_wait(&k_empty[sk], ((j / SK) - 1) & 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&k_full[sk], L::kTileBytes);
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c)
-          tma_load_4d(sK + st * L::kTileBytes + c * L::kChunkBytes, &tm_k, &k_full[st], c * 64,
+          tma_load_4d(sK + sk * L::kTileBytes + c * L::kChunkBytes, &tm_k, &k_full[sk], c * 64,
                       kvh, krow, b);
-        mbar_arrive_expect_tx(&v_full[st], L::kTileBytes);
+        k_issued = j + 1;
+        const int sv = j % SV;
+        if (j >= SV && !mbar_wait(&v_empty[sv], ((j / SV) - 1) & 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&v_full[sv], L::kTileBytes);
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c)
-          tma_load_4d(sV + st * L::kTileBytes + c * L::kChunkBytes, &tm_v, &v_full[st], c * 64,
+          tma_load_4d(sV + sv * L::kTileBytes + c * L::kChunkBytes, &tm_v, &v_full[sv], c * 64,
                       kvh, krow, b);
-        issued = j + 1;
+        v_issued = j + 1;
       }
       // Never leave copies in flight into shared memory that is about to be
       // released: wait for the last load of every stage.
       mbar_drain(q_full, 0, p.status);
-      for (int j = max(0, issued - S); j < issued; ++j) {
-        mbar_drain(&k_full[j % S], (j / S) & 1, p.status);
-        mbar_drain(&v_full[j % S], (j / S) & 1, p.status);
-      }
+      for (int j = max(0, k_issued - SK); j < k_issued; ++j)
+        mbar_drain(&k_full[j % SK], (j / SK) & 1, p.status);
+      for (int j = max(0, v_issued - SV); j < v_issued; ++j)
+        mbar_drain(&v_full[j % SV], (j / SV) & 1, p.status);
     }
   } else if (warp == 8) {
     // ------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop converged; elect.sync picks the lane
+    // that issues each tcgen05 instruction.
+    {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kPrefillBM, kPrefillBN, false, false);
       constexpr uint32_t kIdescO = idesc_bf16_f32(kPrefillBM, D, false, true);
       const uint32_t q_base = smem_u32(sQ);
@@ -250,9 +265,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
           const uint64_t a = sdesc_sw128(q_base + i * L::kTileBytes + off, 16, 1024);
           const uint64_t bd = sdesc_sw128(k_base + st * L::kTileBytes + off, 16, 1024);
-          mma_ss(d_t, a, bd, kIdescS, kk > 0 ? 1u : 0u);
+          mma_ss_elect(d_t, a, bd, kIdescS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&s_full[i]);
+        mma_commit_elect(&s_full[i]);
       };
       auto issue_o = [&](int i, int st, int j) {
         const uint32_t d_t = tmem + L::kTmemO + i * D;
@@ -261,48 +276,60 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         for (int kk = 0; kk < kPrefillBN / 16; ++kk) {
           const uint64_t bd =
               sdesc_sw128(v_base + st * L::kTileBytes + kk * 2048, L::kChunkBytes, 1024);
-          mma_ts(d_t, p_t + kk * 8, bd, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts_elect(d_t, p_t + kk * 8, bd, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&o_done[i]);
+        mma_commit_elect(&o_done[i]);
       };
 
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.status) && mbar_wait(&k_full[0], 0, abort_flag, p.status);
+      // Issue order per key tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so
+      // that each softmax warpgroup works while the tensor pipe runs the
+      // other tile's products.  S_i(j+1) reuses the TMEM columns that PV_i(j),
+      // issued just before it by this thread, reads P_i(j) from; tcgen05 MMAs
+      // issued by one thread execute in order.
+      bool ok = mbar_wait_warp(q_full, 0, abort_flag, p.status) &&
+                mbar_wait_warp(&k_full[0], 0, abort_flag, p.status);
       if (ok) {
         tc_fence_after();
         for (int i = 0; i < 2; ++i)
           if (kv_end[i] > 0) issue_s(i, 0);
+        mma_commit_elect(&k_empty[0]);
       }
       for (int j = 0; ok && j < n_kv; ++j) {
-        const int st = j % S;
-        const int st1 = (j + 1) % S;
+        const int sv = j % SV;
+        const int sk1 = (j + 1) % SK;
         bool k_next = false;
-        if (!mbar_wait(&v_full[st], (j / S) & 1, abort_flag, p.status)) break;
+        auto wait_k_next = [&]() -> bool {
+          if (k_next) return true;
+          if (!mbar_wait_warp(&k_full[sk1], ((j + 1) / SK) & 1, abort_flag, p.status)) return false;
+          tc_fence_after();
+          k_next = true;
+          return true;
+        };
+        if (!mbar_wait_warp(&v_full[sv], (j / SV) & 1, abort_flag, p.status)) break;
         tc_fence_after();
-        for (int i = 0; i < 2 && ok; ++i) {
-          if (j < kv_end[i]) {
-            if (!mbar_wait(&p_full[i], j & 1, abort_flag, p.status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_o(i, st, j);
-          }
-          if (j + 1 < kv_end[i]) {
-            if (!k_next) {
-              if (!mbar_wait(&k_full[st1], ((j + 1) / S) & 1, abort_flag, p.status)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              k_next = true;
-            }
-            issue_s(i, st1);
-          }
+        if (j < kv_end[0]) {
+          if (!mbar_wait_warp(&p_full[0], j & 1, abort_flag, p.status)) break;
+          tc_fence_after();
+          issue_o(0, sv, j);
         }
-        mma_commit(&kv_empty[st]);
+        if (j + 1 < kv_end[0]) {
+          if (!wait_k_next()) break;
+          issue_s(0, sk1);
+        }
+        if (j < kv_end[1]) {
+          if (!mbar_wait_warp(&p_full[1], j & 1, abort_flag, p.status)) break;
+          tc_fence_after();
+          issue_o(1, sv, j);
+        }
+        mma_commit_elect(&v_empty[sv]);
+        if (j + 1 < kv_end[1]) {
+          if (!wait_k_next()) break;
+          issue_s(1, sk1);
+        }
+        if (j + 1 < n_kv) mma_commit_elect(&k_empty[sk1]);
       }
       // Everything this thread issued must finish before TMEM is released.
-      mma_commit(drain);
+      mma_commit_elect(drain);
       mbar_drain(drain, 0, p.status);
     }
   } else {
