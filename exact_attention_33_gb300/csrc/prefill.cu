@@ -44,10 +44,13 @@ struct PrefillLayout {
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
   // K and V have rings of their own: a K stage is released as soon as both
-  // S MMAs have read it, a V stage after both P V MMAs, so K loads run about
-  // two key tiles ahead of their use.
-  static constexpr int kStagesK = (D == 128) ? 3 : 6;
-  static constexpr int kStagesV = (D == 128) ? 2 : 4;
+  // S MMAs have read it, a V stage after both P V MMAs.
+#ifndef FA_PREFILL_STAGES_K128
+#define FA_PREFILL_STAGES_K128 3
+#define FA_PREFILL_STAGES_V128 2
+#endif
+  static constexpr int kStagesK = (D == 128) ? FA_PREFILL_STAGES_K128 : 5;
+  static constexpr int kStagesV = (D == 128) ? FA_PREFILL_STAGES_V128 : 5;
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kPrefillQTiles * kTileBytes;
   static constexpr int kV = kK + kStagesK * kTileBytes;
@@ -219,25 +222,38 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           tma_load_4d(sQ + i * L::kTileBytes + c * L::kChunkBytes, &tm_q, q_full, c * 64, h,
                       qrow, b);
       }
+      // Issue order K(0), then V(j), K(j+1) for every j: a V load never waits
+      // behind a K stage that frees later.
       int k_issued = 0, v_issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int krow = seq_start + j * kPrefillBN;
+      auto load_k = [&](int j) -> bool {
         const int sk = j % SK;
-        if (j >= SK && !mbar_wait(&k_empty[sk], ((j / SK) - 1) & 1, abort_flag, p.status)) break;
+        if (j >= SK && !mbar_wait(&k_empty[sk], ((j / SK) - 1) & 1, abort_flag, p.status))
+          return false;
         mbar_arrive_expect_tx(&k_full[sk], L::kTileBytes);
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c)
           tma_load_4d(sK + sk * L::kTileBytes + c * L::kChunkBytes, &tm_k, &k_full[sk], c * 64,
-                      kvh, krow, b);
+                      kvh, seq_start + j * kPrefillBN, b);
         k_issued = j + 1;
+        return true;
+      };
+      auto load_v = [&](int j) -> bool {
         const int sv = j % SV;
-        if (j >= SV && !mbar_wait(&v_empty[sv], ((j / SV) - 1) & 1, abort_flag, p.status)) break;
+        if (j >= SV && !mbar_wait(&v_empty[sv], ((j / SV) - 1) & 1, abort_flag, p.status))
+          return false;
         mbar_arrive_expect_tx(&v_full[sv], L::kTileBytes);
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c)
           tma_load_4d(sV + sv * L::kTileBytes + c * L::kChunkBytes, &tm_v, &v_full[sv], c * 64,
-                      kvh, krow, b);
+                      kvh, seq_start + j * kPrefillBN, b);
         v_issued = j + 1;
+        return true;
+      };
+      if (n_kv > 0 && load_k(0)) {
+        for (int j = 0; j < n_kv; ++j) {
+          if (!load_v(j)) break;
+          if (j + 1 < n_kv && !load_k(j + 1)) break;
+        }
       }
       // Never leave copies in flight into shared memory that is about to be
       // released: wait for the last load of every stage.
