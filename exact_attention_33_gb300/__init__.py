@@ -19,7 +19,7 @@ import os
 import threading
 
 __all__ = [
-    "FaError", "library_path", "load_library", "fa_fwd", "fa_fwd_varlen",
+    "FaError", "library_path", "load_library", "fa_fwd", "fa_fwd_varlen", "fa_fwd_paged",
     "fa_decode_paged", "fa_decode_paged_noalloc", "fa_decode_workspace_size",
     "fa_status_string", "fa_device_status",
     "fa_version", "FA_DEV_TIMEOUT", "FA_DEV_BAD_BLOCK", "FA_DEV_BAD_CTX", "FA_DEV_BAD_SEQLEN",
@@ -65,6 +65,9 @@ def load_library() -> ctypes.CDLL:
         lib.fa_fwd.restype = i
         lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
         lib.fa_fwd_varlen.restype = i
+        lib.fa_fwd_paged.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, i, i, i, i, f, i,
+                                     vp, vp, vp]
+        lib.fa_fwd_paged.restype = i
         lib.fa_decode_workspace_size.argtypes = [i, i, i, i, i, i]
         lib.fa_decode_workspace_size.restype = sz
         lib.fa_decode_paged.argtypes = [vp, vp, vp, vp, i, vp, i, i, i, i, i, i, i, f, vp, vp,
@@ -179,6 +182,39 @@ def fa_fwd_varlen(q, k, v, cu_seqlens, max_seqlen, causal=False, scale=None, out
                                       1 if causal else 0, _stream_handle(stream))
     if rc != FA_OK:
         raise FaError("fa_fwd_varlen", rc)
+    return out, lse
+
+
+def fa_fwd_paged(q, k_pool, v_pool, block_table, ctx_lens, cu_seqlens_q, max_seqlen_q,
+                 max_ctx_len, causal=True, scale=None, out=None, lse=None, want_lse=True,
+                 stream=None):
+    """Query chunks [Tq,H,d] against a paged KV cache (chunked prefill).
+
+    pools [num_blocks,16,Hkv,d] bf16; block_table int32 [batch,max_blocks];
+    ctx_lens int32 [batch]; cu_seqlens_q int32 [batch+1]; all on the device.
+    Returns (out [Tq,H,d] bf16, lse [H,Tq] fp32 or None).
+    """
+    torch = _torch()
+    _check_bf16_cuda("q", q, 3)
+    _check_bf16_cuda("k_pool", k_pool, 4)
+    _check_bf16_cuda("v_pool", v_pool, 4)
+    for name, t in (("block_table", block_table), ("ctx_lens", ctx_lens),
+                    ("cu_seqlens_q", cu_seqlens_q)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    Tq, H, d = q.shape
+    num_blocks, block_size, Hkv, _ = k_pool.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((H, Tq), dtype=torch.float32, device=q.device)
+    rc = load_library().fa_fwd_paged(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), block_table.shape[1],
+        _ptr(ctx_lens), _ptr(cu_seqlens_q), cu_seqlens_q.numel() - 1, Tq, int(max_seqlen_q),
+        int(max_ctx_len), H, Hkv, d, block_size, num_blocks, _scale(scale, d),
+        1 if causal else 0, _ptr(out), _ptr(lse), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError("fa_fwd_paged", rc)
     return out, lse
 
 

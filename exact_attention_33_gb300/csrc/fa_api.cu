@@ -22,8 +22,8 @@ namespace fa {
 __device__ unsigned int g_status = 0;
 
 cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                           const PrefillParams &p, int d, bool causal, bool varlen, int grid,
-                           cudaStream_t stream);
+                           const CUtensorMap &tv1, const PrefillParams &p, int d, bool causal,
+                           int kind, int grid, cudaStream_t stream);
 cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
                           int d, cudaStream_t stream);
 
@@ -67,15 +67,17 @@ int make_map(CUtensorMap *map, const void *base, int d, int heads, long long row
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
-// Paged pool [num_blocks * block_size tokens][Hkv][d] as a 3-D map.
-int make_pool_map(CUtensorMap *map, const void *base, int d, int heads, long long tokens) {
+// Paged pool [num_blocks * block_size tokens][Hkv][d] as a 3-D map; each copy
+// moves {64, 1, box_rows} (a whole 16-token block, or one token row).
+int make_pool_map(CUtensorMap *map, const void *base, int d, int heads, long long tokens,
+                  int box_rows = kDecodeBlock) {
   auto fn = encode_fn();
   if (fn == nullptr) return FA_ERR_CUDA;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
                               static_cast<cuuint64_t>(tokens)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                                  static_cast<cuuint64_t>(heads) * d * 2};
-  const cuuint32_t box[3] = {64, 1, kDecodeBlock};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -224,8 +226,8 @@ int fa_fwd(const void *q, const void *k, const void *v, void *out, float *lse, i
   p.total_tokens = 0;
   p.scale_log2 = scale * kLog2e;
   p.causal = causal;
-  cudaError_t e = launch_prefill(tq, tk, tv, p, d, causal != 0, false, static_cast<int>(grid),
-                                 reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_prefill(tq, tk, tv, tv, p, d, causal != 0, kKindDense,
+                                 static_cast<int>(grid), reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -270,8 +272,71 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float 
   p.total_tokens = total_tokens;
   p.scale_log2 = scale * kLog2e;
   p.causal = causal;
-  cudaError_t e = launch_prefill(tq, tk, tv, p, d, causal != 0, true, static_cast<int>(grid),
-                                 reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_prefill(tq, tk, tv, tv, p, d, causal != 0, kKindVarlen,
+                                 static_cast<int>(grid), reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_fwd_paged(const void *q, const void *k_pool, const void *v_pool,
+                 const int32_t *block_table, int max_blocks_per_seq, const int32_t *ctx_lens,
+                 const int32_t *cu_seqlens_q, int batch, int total_q, int max_seqlen_q,
+                 int max_ctx_len, int H, int Hkv, int d, int block_size, int num_blocks,
+                 float scale, int causal, void *out, float *lse, fa_stream_t stream) {
+  if (!q || !k_pool || !v_pool || !block_table || !ctx_lens || !cu_seqlens_q || !out)
+    return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16))
+    return FA_ERR_INVALID_ARG;
+  if (!aligned(block_table, 4) || !aligned(ctx_lens, 4) || !aligned(cu_seqlens_q, 4) ||
+      (lse && !aligned(lse, 4)))
+    return FA_ERR_INVALID_ARG;
+  if (batch < 0 || total_q < 0 || max_seqlen_q < 0 || max_ctx_len < 0 || H < 1 || Hkv < 1 ||
+      H % Hkv != 0 || num_blocks < 1 || max_blocks_per_seq < 1)
+    return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (block_size != kDecodeBlock) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(max_blocks_per_seq) * block_size < max_ctx_len)
+    return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (batch == 0 || total_q == 0 || max_seqlen_q == 0) return FA_OK;
+  if (max_seqlen_q > total_q) max_seqlen_q = total_q;
+  const long long pairs = (max_seqlen_q + kPrefillRowsPerCta - 1) / kPrefillRowsPerCta;
+  const long long grid = pairs * batch * H;
+  if (grid > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(total_q) * H * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
+
+  CUtensorMap tq, tk, tv, tv1;
+  const long long tokens = static_cast<long long>(num_blocks) * block_size;
+  int rc = make_map(&tq, q, d, H, total_q, 1, kPrefillBM);
+  if (rc == FA_OK) rc = make_pool_map(&tk, k_pool, d, Hkv, tokens);
+  if (rc == FA_OK) rc = make_pool_map(&tv, v_pool, d, Hkv, tokens);
+  if (rc == FA_OK) rc = make_pool_map(&tv1, v_pool, d, Hkv, tokens, 1);
+  if (rc != FA_OK) return rc;
+
+  PrefillParams p{};
+  p.status = status_ptr();
+  if (p.status == nullptr) return FA_ERR_CUDA;
+  p.out = out;
+  p.lse = lse;
+  p.cu_seqlens = cu_seqlens_q;
+  p.B = batch;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.group = H / Hkv;
+  p.head_group = prefill_head_group(H);
+  p.N = total_q;
+  p.max_pairs = static_cast<int>(pairs);
+  p.total_tokens = total_q;
+  p.scale_log2 = scale * kLog2e;
+  p.causal = causal;
+  p.block_table = block_table;
+  p.ctx_lens = ctx_lens;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.max_ctx_len = max_ctx_len;
+  p.num_blocks = num_blocks;
+  cudaError_t e = launch_prefill(tq, tk, tv, tv1, p, d, causal != 0, kKindPaged,
+                                 static_cast<int>(grid), reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -22,6 +22,11 @@ constexpr int kPrefillQTiles = 2;
 constexpr int kPrefillRowsPerCta = kPrefillBM * kPrefillQTiles;
 constexpr int kPrefillThreads = 320;  // 8 softmax warps + 1 MMA warp + 1 TMA warp
 
+// Work layouts of the prefill kernel.
+constexpr int kKindDense = 0;   // [B, N, H, d] batch
+constexpr int kKindVarlen = 1;  // packed sequences, cu_seqlens
+constexpr int kKindPaged = 2;   // packed query chunks over a paged KV cache
+
 struct PrefillParams {
   unsigned int *status;   // per-device sticky FA_DEV_* word
   void *out;              // bf16 [rows, H, d] (dense rows = B*N, varlen rows = T)
@@ -35,6 +40,12 @@ struct PrefillParams {
   int total_tokens;       // varlen: T
   float scale_log2;       // scale * log2(e)
   int causal;
+  // paged kind only
+  const int32_t *block_table;  // [num_seqs, max_blocks_per_seq]
+  const int32_t *ctx_lens;     // keys per sequence
+  int max_blocks_per_seq;
+  int max_ctx_len;
+  int num_blocks;
 };
 
 // ------------------------------------------------------------------- decode

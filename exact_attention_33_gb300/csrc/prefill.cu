@@ -96,11 +96,14 @@ __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]
       : "memory");
 }
 
-template <int D, bool CAUSAL, bool VARLEN>
+// KIND: dense batch, packed varlen batch, or packed queries over a paged KV
+// cache (chunked prefill).
+template <int D, bool CAUSAL, int KIND>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+                   const __grid_constant__ CUtensorMap tm_v,
+                   const __grid_constant__ CUtensorMap tm_v1, const PrefillParams p) {
   using L = PrefillLayout<D>;
   constexpr int SK = L::kStagesK;
   constexpr int SV = L::kStagesV;
@@ -120,8 +123,17 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   const int h = (grp % (p.H / hgs)) * hgs + h_in;
   const int unit = grp / (p.H / hgs);  // batch element or sequence
   const int pair = CAUSAL ? (p.max_pairs - 1 - pair_rank) : pair_rank;
-  int b, seq_start, len;
-  if (VARLEN) {
+  // len: query rows of the unit; kv_len: its keys; offset = kv_len - len
+  // aligns causal masking to the bottom right (query i sees keys
+  // j <= i + offset).
+  int b, seq_start, len, kv_len, offset;
+  if (KIND == kKindDense) {
+    b = unit;
+    seq_start = 0;
+    len = p.N;
+    kv_len = len;
+    offset = 0;
+  } else {
     seq_start = p.cu_seqlens[unit];
     const int seq_end = p.cu_seqlens[unit + 1];
     if (seq_start < 0 || seq_end < seq_start || seq_end > p.total_tokens) {
@@ -132,15 +144,23 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     if (len > p.max_pairs * kPrefillRowsPerCta && pair == 0 && h == 0)
       raise_status(p.status, FA_DEV_BAD_SEQLEN);  // longer than max_seqlen: tail not covered
     b = 0;
-  } else {
-    b = unit;
-    seq_start = 0;
-    len = p.N;
+    if (KIND == kKindVarlen) {
+      kv_len = len;
+      offset = 0;
+    } else {
+      kv_len = p.ctx_lens[unit];
+      if (kv_len < 0 || kv_len > p.max_ctx_len ||
+          kv_len > p.max_blocks_per_seq * kDecodeBlock) {
+        if (pair == 0 && h == 0) raise_status(p.status, FA_DEV_BAD_CTX);
+        return;
+      }
+      offset = kv_len - len;
+    }
   }
   const int row0 = pair * kPrefillRowsPerCta;
   if (row0 >= len) return;  // no padding work: the whole CTA leaves before any set-up
 
-  const int n_kv_all = (len + kPrefillBN - 1) / kPrefillBN;
+  const int n_kv_all = (kv_len + kPrefillBN - 1) / kPrefillBN;
   int kv_end[kPrefillQTiles];
 #pragma unroll
   for (int i = 0; i < kPrefillQTiles; ++i) {
@@ -148,7 +168,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     if (t0 >= len) {
       kv_end[i] = 0;
     } else {
-      kv_end[i] = CAUSAL ? min(n_kv_all, t0 / kPrefillBN + 1) : n_kv_all;
+      int e = n_kv_all;
+      if (CAUSAL) {
+        const int last_key = min(t0 + kPrefillBM - 1, len - 1) + offset;
+        e = (last_key < 0) ? 0 : min(n_kv_all, last_key / kPrefillBN + 1);
+      }
+      // a live tile runs at least one key tile (possibly fully masked), so
+      // that rows which see no key are still written (O = 0, LSE = -inf)
+      kv_end[i] = max(e, 1);
     }
   }
   const int n_kv = max(kv_end[0], kv_end[1]);
@@ -197,6 +224,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     tmem_alloc(tmem_slot, L::kTmemCols);
     tmem_relinquish();
   }
+  if (KIND == kKindPaged) {
+    // Rows of a V stage that no load fills (keys past the context in the last
+    // key tile) must hold finite values: P is 0 there, but 0 * NaN is NaN.
+    uint4 *z = reinterpret_cast<uint4 *>(smem + L::kV);
+    for (int t = threadIdx.x; t < SV * L::kTileBytes / 16; t += kPrefillThreads)
+      z[t] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -207,7 +242,114 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   uint8_t *sV = smem + L::kV;
   const int kvh = h / p.group;
 
-  if (warp == 9) {
+  if (warp == 9 && KIND == kKindPaged) {
+    // ------------------------------------------------------ TMA producer, paged
+    // The warp runs converged: lanes 0..7 look up the 8 physical blocks of a
+    // 128-key tile in the block table, lane 0 issues the copies.  A block
+    // whose id is outside the pool is not loaded (its keys hold stale data,
+    // the status word records the error).  In the last block only the slots
+    // inside the context are copied (one-row boxes for V), so stale slots of
+    // the pool never reach shared memory.
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_v1);
+      const int nq = (kv_end[1] > 0) ? 2 : 1;
+      mbar_arrive_expect_tx(q_full, nq * L::kTileBytes);
+      for (int i = 0; i < nq; ++i) {
+        const int qrow = seq_start + row0 + i * kPrefillBM;
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_4d(sQ + i * L::kTileBytes + c * L::kChunkBytes, &tm_q, q_full, c * 64, h,
+                      qrow, b);
+      }
+    }
+    __syncwarp();
+    const int32_t *trow = p.block_table + static_cast<size_t>(unit) * p.max_blocks_per_seq;
+    constexpr int kBlkPerTile = kPrefillBN / kDecodeBlock;
+    constexpr uint32_t kRowBytes = 128 * L::kChunks;  // one key row, all chunks
+    const int total_blk = (kv_len + kDecodeBlock - 1) / kDecodeBlock;
+    int k_issued = 0, v_issued = 0;
+    // physical block of slot `lane` of tile j (or -1), and its valid rows
+    auto lookup = [&](int j, int &rows) -> int {
+      const int blk = j * kBlkPerTile + lane;
+      rows = 0;
+      if (lane >= kBlkPerTile || blk >= total_blk) return -1;
+      const int phys = trow[blk];
+      if (phys < 0 || phys >= p.num_blocks) {
+        raise_status(p.status, FA_DEV_BAD_BLOCK);
+        return -1;
+      }
+      rows = min(kDecodeBlock, kv_len - blk * kDecodeBlock);
+      return phys;
+    };
+    auto load_k = [&](int j) -> bool {
+      const int sk = j % SK;
+      if (j >= SK && !mbar_wait_warp(&k_empty[sk], ((j / SK) - 1) & 1, abort_flag, p.status))
+        return false;
+      int rows;
+      const int phys = lookup(j, rows);
+      const uint32_t bytes =
+          __reduce_add_sync(0xffffffffu, phys >= 0 ? kDecodeBlock * kRowBytes : 0u);
+      if (lane == 0) mbar_arrive_expect_tx(&k_full[sk], bytes);
+      for (int t = 0; t < kBlkPerTile; ++t) {
+        const int pb = __shfl_sync(0xffffffffu, phys, t);
+        if (lane == 0 && pb >= 0) {
+#pragma unroll
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_3d(sK + sk * L::kTileBytes + c * L::kChunkBytes + t * kDecodeBlock * 128,
+                        &tm_k, &k_full[sk], c * 64, kvh, pb * kDecodeBlock);
+        }
+      }
+      k_issued = j + 1;
+      return true;
+    };
+    auto load_v = [&](int j) -> bool {
+      const int sv = j % SV;
+      if (j >= SV && !mbar_wait_warp(&v_empty[sv], ((j / SV) - 1) & 1, abort_flag, p.status))
+        return false;
+      int rows;
+      const int phys = lookup(j, rows);
+      const uint32_t bytes =
+          __reduce_add_sync(0xffffffffu, phys >= 0 ? static_cast<uint32_t>(rows) * kRowBytes : 0u);
+      if (lane == 0) mbar_arrive_expect_tx(&v_full[sv], bytes);
+      for (int t = 0; t < kBlkPerTile; ++t) {
+        const int pb = __shfl_sync(0xffffffffu, phys, t);
+        const int nr = __shfl_sync(0xffffffffu, rows, t);
+        if (lane == 0 && pb >= 0) {
+          uint8_t *dst = sV + sv * L::kTileBytes + t * kDecodeBlock * 128;
+          if (nr == kDecodeBlock) {
+#pragma unroll
+            for (int c = 0; c < L::kChunks; ++c)
+              tma_load_3d(dst + c * L::kChunkBytes, &tm_v, &v_full[sv], c * 64, kvh,
+                          pb * kDecodeBlock);
+          } else {
+            for (int r = 0; r < nr; ++r)
+#pragma unroll
+              for (int c = 0; c < L::kChunks; ++c)
+                tma_load_3d(dst + c * L::kChunkBytes + r * 128, &tm_v1, &v_full[sv], c * 64, kvh,
+                            pb * kDecodeBlock + r);
+          }
+        }
+      }
+      v_issued = j + 1;
+      return true;
+    };
+    if (n_kv > 0 && load_k(0)) {
+      for (int j = 0; j < n_kv; ++j) {
+        if (!load_v(j)) break;
+        if (j + 1 < n_kv && !load_k(j + 1)) break;
+      }
+    }
+    if (lane == 0) {
+      mbar_drain(q_full, 0, p.status);
+      for (int j = max(0, k_issued - SK); j < k_issued; ++j)
+        mbar_drain(&k_full[j % SK], (j / SK) & 1, p.status);
+      for (int j = max(0, v_issued - SV); j < v_issued; ++j)
+        mbar_drain(&v_full[j % SV], (j / SV) & 1, p.status);
+    }
+  } else if (warp == 9) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -370,7 +512,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     float l = 0.f;        // running sum of the bf16 P values, relative to m_ref
     float l_exact = 0.f;  // running sum of the fp32 exponentials, relative to m_ref
     bool ok = true;
-    const int limit = CAUSAL ? min(len, qi + 1) : len;  // keys [0, limit) are visible
+    // keys [0, limit) are visible to this row (bottom-right causal alignment)
+    const int limit = CAUSAL ? min(kv_len, qi + 1 + offset) : kv_len;
 
     for (int j = 0; j < my_end; ++j) {
       ok = mbar_wait(&s_full[i], j & 1, abort_flag, p.status);
@@ -468,7 +611,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const bool live = qi < len;
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
         size_t out_row;
-        if (VARLEN)
+        if (KIND != kKindDense)
           out_row = static_cast<size_t>(seq_start + qi);
         else
           out_row = static_cast<size_t>(b) * p.N + qi;
@@ -498,7 +641,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           const float lse = (l_exact > 0.f)
                                 ? (m + __log2f(l_exact)) * 0.69314718055994530942f
                                 : -CUDART_INF_F;
-          if (VARLEN)
+          if (KIND != kKindDense)
             p.lse[static_cast<size_t>(h) * p.total_tokens + seq_start + qi] = lse;
           else
             p.lse[(static_cast<size_t>(b) * p.H + h) * p.N + qi] = lse;
@@ -518,34 +661,43 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
 // ------------------------------------------------------------------ launch
 
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, int KIND>
 static cudaError_t launch_prefill_t(const CUtensorMap &tq, const CUtensorMap &tk,
-                                    const CUtensorMap &tv, const PrefillParams &p, int grid,
-                                    cudaStream_t stream) {
+                                    const CUtensorMap &tv, const CUtensorMap &tv1,
+                                    const PrefillParams &p, int grid, cudaStream_t stream) {
   using L = PrefillLayout<D>;
-  auto kern = prefill_kernel<D, CAUSAL, VARLEN>;
+  auto kern = prefill_kernel<D, CAUSAL, KIND>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kPrefillThreads, L::kSmemAlloc, stream>>>(tq, tk, tv, p);
+  kern<<<grid, kPrefillThreads, L::kSmemAlloc, stream>>>(tq, tk, tv, tv1, p);
   return cudaGetLastError();
 }
 
+template <int D, int KIND>
+static cudaError_t launch_prefill_k(const CUtensorMap &tq, const CUtensorMap &tk,
+                                    const CUtensorMap &tv, const CUtensorMap &tv1,
+                                    const PrefillParams &p, bool causal, int grid,
+                                    cudaStream_t stream) {
+  return causal ? launch_prefill_t<D, true, KIND>(tq, tk, tv, tv1, p, grid, stream)
+                : launch_prefill_t<D, false, KIND>(tq, tk, tv, tv1, p, grid, stream);
+}
+
 cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                           const PrefillParams &p, int d, bool causal, bool varlen, int grid,
-                           cudaStream_t stream) {
+                           const CUtensorMap &tv1, const PrefillParams &p, int d, bool causal,
+                           int kind, int grid, cudaStream_t stream) {
   if (d == 64) {
-    if (varlen)
-      return causal ? launch_prefill_t<64, true, true>(tq, tk, tv, p, grid, stream)
-                    : launch_prefill_t<64, false, true>(tq, tk, tv, p, grid, stream);
-    return causal ? launch_prefill_t<64, true, false>(tq, tk, tv, p, grid, stream)
-                  : launch_prefill_t<64, false, false>(tq, tk, tv, p, grid, stream);
+    if (kind == kKindDense)
+      return launch_prefill_k<64, kKindDense>(tq, tk, tv, tv1, p, causal, grid, stream);
+    if (kind == kKindVarlen)
+      return launch_prefill_k<64, kKindVarlen>(tq, tk, tv, tv1, p, causal, grid, stream);
+    return launch_prefill_k<64, kKindPaged>(tq, tk, tv, tv1, p, causal, grid, stream);
   }
-  if (varlen)
-    return causal ? launch_prefill_t<128, true, true>(tq, tk, tv, p, grid, stream)
-                  : launch_prefill_t<128, false, true>(tq, tk, tv, p, grid, stream);
-  return causal ? launch_prefill_t<128, true, false>(tq, tk, tv, p, grid, stream)
-                : launch_prefill_t<128, false, false>(tq, tk, tv, p, grid, stream);
+  if (kind == kKindDense)
+    return launch_prefill_k<128, kKindDense>(tq, tk, tv, tv1, p, causal, grid, stream);
+  if (kind == kKindVarlen)
+    return launch_prefill_k<128, kKindVarlen>(tq, tk, tv, tv1, p, causal, grid, stream);
+  return launch_prefill_k<128, kKindPaged>(tq, tk, tv, tv1, p, causal, grid, stream);
 }
 
 }  // namespace fa

@@ -43,6 +43,10 @@ WORKLOADS = {
                             d=128, causal=True),
     "paged_decode_gqa_d128": dict(kind="decode", batch=64, H=32, Hkv=8, d=128, block_size=16,
                                   ctx_lo=512, ctx_hi=32768),
+    # chunked prefill over a paged cache: each sequence has a cached prefix of
+    # U[1024, 16384] tokens (seed 6) and appends a chunk of 1024 new tokens
+    "paged_prefill_gqa_d128": dict(kind="paged_prefill", batch=8, H=32, Hkv=8, d=128,
+                                   block_size=16, prefix_lo=1024, prefix_hi=16384, chunk=1024),
 }
 
 
@@ -216,6 +220,38 @@ def decode_inputs(ctx_lens, H, Hkv, d, block_size=16, seed=0, table_seed=4,
                         normal_bf16_bits((nb_total, block_size, Hkv, d), seed, 2))
 
 
+@dataclass
+class PagedPrefillInputs:
+    pool: DecodeInputs           # pool, block table and ctx_lens (= prefix + chunk)
+    q_lens: np.ndarray           # int32 [batch]
+    cu_seqlens_q: np.ndarray     # int32 [batch + 1]
+    q: np.ndarray                # bf16 bits [total_q, H, d]
+
+    @property
+    def total_q(self) -> int:
+        return int(self.cu_seqlens_q[-1])
+
+    @property
+    def max_seqlen_q(self) -> int:
+        return int(self.q_lens.max()) if len(self.q_lens) else 0
+
+
+def paged_prefill_inputs(ctx_lens, q_lens, H, Hkv, d, block_size=16, seed=0, table_seed=4,
+                         extra_blocks=0) -> PagedPrefillInputs:
+    """Query chunks over a paged pool: the pool and table follow the decode
+    recipe; the packed queries use seed ``seed`` stream 3."""
+    pool = decode_inputs(ctx_lens, H, Hkv, d, block_size, seed, table_seed, extra_blocks)
+    q_lens = np.asarray(q_lens, dtype=np.int32)
+    cu = cu_seqlens_from(q_lens)
+    return PagedPrefillInputs(pool, q_lens, cu, normal_bf16_bits((int(cu[-1]), H, d), seed, 3))
+
+
+def paged_prefill_lengths(batch=8, prefix_lo=1024, prefix_hi=16384, chunk=1024, seed=6):
+    prefix = np.random.default_rng(seed).integers(prefix_lo, prefix_hi + 1, size=batch)
+    q_lens = np.full(batch, chunk, dtype=np.int32)
+    return (prefix + chunk).astype(np.int32), q_lens
+
+
 # ---------------------------------------------------------------- counters
 
 def prefill_flops(B, N, H, d, causal) -> float:
@@ -226,6 +262,20 @@ def prefill_flops(B, N, H, d, causal) -> float:
 
 def varlen_flops(lengths, H, d, causal) -> float:
     return float(sum(prefill_flops(1, int(L), H, d, causal) for L in lengths))
+
+
+def paged_prefill_flops(ctx_lens, q_lens, H, d, causal=True) -> float:
+    """4*d*H per visible (query, key) pair; bottom-right causal alignment."""
+    total = 0.0
+    for ctx, nq in zip(ctx_lens, q_lens):
+        ctx, nq = int(ctx), int(nq)
+        if causal:
+            i = np.arange(nq)
+            vis = np.clip(i + 1 + (ctx - nq), 0, ctx)
+            total += float(vis.sum())
+        else:
+            total += float(ctx) * nq
+    return 4.0 * d * H * total
 
 
 def decode_bytes(ctx_lens, H, Hkv, d, max_blocks_per_seq, block_size=16) -> int:

@@ -100,6 +100,33 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float 
                   fa_stream_t stream);
 
 /*
+ * Prefill of query chunks against a paged KV cache (chunked prefill / cached
+ * prefix): "S12 FlashAttention", "Implementation" - the paged variant is the
+ * same tiled recurrence with the block table in front of the key access.
+ * Each sequence b brings cu_seqlens_q[b+1] - cu_seqlens_q[b] query tokens
+ * (packed as in fa_fwd_varlen) and reads its ctx_lens[b] keys, the cached
+ * prefix plus the chunk itself, which the caller has already written to the
+ * pool.
+ *   q, out       : [total_q, H, d] bf16
+ *   k_pool,
+ *   v_pool       : [num_blocks, block_size, Hkv, d] bf16, block_size == 16
+ *   block_table  : int32 [batch, max_blocks_per_seq]
+ *   ctx_lens     : int32 [batch], 0 <= ctx_lens[b] <= max_ctx_len
+ *   cu_seqlens_q : int32 DEVICE array [batch + 1] (rules as cu_seqlens)
+ *   lse          : [H, total_q] fp32, may be NULL
+ *   causal       : bottom-right aligned: query i of a chunk of Nq queries
+ *                  sees key j iff j <= i + (ctx_len - Nq).  A query that sees
+ *                  no key gets out = 0 and lse = -inf.
+ * Slots of the last block past ctx_len are never copied on chip.  Device-side
+ * checks: FA_DEV_BAD_CTX, FA_DEV_BAD_BLOCK, FA_DEV_BAD_SEQLEN.
+ */
+int fa_fwd_paged(const void *q, const void *k_pool, const void *v_pool,
+                 const int32_t *block_table, int max_blocks_per_seq, const int32_t *ctx_lens,
+                 const int32_t *cu_seqlens_q, int batch, int total_q, int max_seqlen_q,
+                 int max_ctx_len, int H, int Hkv, int d, int block_size, int num_blocks,
+                 float scale, int causal, void *out, float *lse, fa_stream_t stream);
+
+/*
  * Bytes of caller-owned workspace that fa_decode_paged needs for the split
  * partial states (m, l, o) of every (sequence, query head, key split).
  * Returns 0 for invalid arguments.  The split size depends only on these

@@ -56,6 +56,7 @@ __all__ = [
     "attention_dense",
     "attention_varlen",
     "paged_decode",
+    "paged_prefill",
     "tile_state",
     "merge_states",
     "gather_paged",
@@ -204,6 +205,38 @@ def paged_decode(q, k_pool, v_pool, block_table, ctx_lens, block_size, scale=Non
             for h in heads:
                 o[b, h] = o_b[0, h]
                 lse[b, h] = lse_b[h, 0]
+    return o, lse
+
+
+def paged_prefill(q, k_pool, v_pool, block_table, ctx_lens, cu_seqlens_q, block_size,
+                  scale=None, causal=True, seqs=None, heads=None):
+    """Several query tokens per sequence against a paged KV cache (chunked
+    prefill over cached keys).
+
+    "S12 FlashAttention", Implementation: the paged variant is the same loop
+    with the block table in front of the key access; here each sequence b
+    brings ``cu_seqlens_q[b+1] - cu_seqlens_q[b]`` query tokens (packed like
+    the varlen layout) and reads its ``ctx_lens[b]`` cached keys through the
+    block table.  Causal masking is bottom-right aligned: query i of a chunk
+    of Nq queries sees key j iff j <= i + (ctx - Nq), so the chunk's queries
+    are the last Nq positions of the sequence.
+    q: [Tq, H, d]; pools [num_blocks, block_size, Hkv, d]; returns
+    (o [Tq, H, d], lse [H, Tq]).
+    """
+    q = np.asarray(q)
+    cu = np.asarray(cu_seqlens_q, dtype=np.int64)
+    t_q, h_q, _ = q.shape
+    o = np.zeros((t_q, h_q, np.asarray(v_pool).shape[3]), dtype=np.float64)
+    lse = np.full((h_q, t_q), -np.inf, dtype=np.float64)
+    for b in (range(len(cu) - 1) if seqs is None else seqs):
+        a, e = int(cu[b]), int(cu[b + 1])
+        if e <= a:
+            continue
+        kc = gather_paged(k_pool, block_table[b], ctx_lens[b], block_size)
+        vc = gather_paged(v_pool, block_table[b], ctx_lens[b], block_size)
+        o_b, lse_b = attention_one(q[a:e], kc, vc, scale=scale, causal=causal, heads=heads)
+        o[a:e] = o_b
+        lse[:, a:e] = lse_b
     return o, lse
 
 

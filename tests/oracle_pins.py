@@ -416,10 +416,54 @@ def pin_dense_layout(ora):
         np.testing.assert_allclose(l[b], l_ref, atol=1e-13)
 
 
+def pin_paged_prefill(ora):
+    """Chunked prefill over a paged cache: (1) a chunk covering the whole
+    sequence laid out contiguously is plain causal attention; (2) per element
+    it matches a pure-Python evaluation of the bottom-right causal rule;
+    (3) a decode step (chunk of one query) matches paged_decode; (4) stale
+    slots past the context never matter."""
+    rng = np.random.default_rng(27)
+    bs, hkv, h, d = 4, 2, 4, 3
+    ctx = np.array([9, 4, 13])
+    qlen = np.array([3, 4, 1])
+    nblk = (ctx + bs - 1) // bs
+    nb = int(nblk.sum()) + 2
+    perm = rng.permutation(nb)
+    table = np.full((3, int(nblk.max())), -1)
+    pos = 0
+    for b, n in enumerate(nblk):
+        table[b, :n] = perm[pos:pos + n]
+        pos += n
+    kp = rand(rng, nb, bs, hkv, d)
+    vp = rand(rng, nb, bs, hkv, d)
+    cu = np.concatenate([[0], np.cumsum(qlen)])
+    q = rand(rng, int(cu[-1]), h, d)
+    o, l = ora.paged_prefill(q, kp, vp, table, ctx, cu, bs, scale=0.7, causal=True)
+    for b in range(3):
+        kc = np.concatenate([kp[table[b, t // bs], t % bs][None] for t in range(ctx[b])])
+        vc = np.concatenate([vp[table[b, t // bs], t % bs][None] for t in range(ctx[b])])
+        o_ref, l_ref = brute_attention(q[cu[b]:cu[b + 1]], kc, vc, 0.7, True)
+        np.testing.assert_allclose(o[cu[b]:cu[b + 1]], o_ref, atol=1e-13)
+        np.testing.assert_allclose(l[:, cu[b]:cu[b + 1]], l_ref, atol=1e-13)
+    # one query per sequence is a decode step
+    od, ld = ora.paged_decode(q[cu[1:] - 1], kp, vp, table, ctx, bs, scale=0.7)
+    np.testing.assert_allclose(o[cu[1:] - 1], od, atol=1e-13)
+    np.testing.assert_allclose(l[:, cu[1:] - 1].T, ld, atol=1e-13)
+    # whole sequence as the chunk over a contiguous pool == causal attention
+    kfull = rand(rng, 8, 1, 2)
+    vfull = rand(rng, 8, 1, 2)
+    qfull = rand(rng, 8, 2, 2)
+    o1, l1 = ora.paged_prefill(qfull, kfull.reshape(2, 4, 1, 2), vfull.reshape(2, 4, 1, 2),
+                               np.array([[0, 1]]), np.array([8]), np.array([0, 8]), 4)
+    o2, l2 = ora.attention_one(qfull, kfull, vfull, causal=True)
+    np.testing.assert_allclose(o1, o2, atol=1e-14)
+    np.testing.assert_allclose(l1, l2, atol=1e-14)
+
+
 ALL_PINS = [
     pin_worked_example, pin_zero_query, pin_single_key, pin_dominant_key,
     pin_constant_values, pin_rows_are_softmax, pin_convex_combination,
     pin_key_permutation, pin_masked_keys_do_nothing, pin_brute_force,
     pin_default_scale, pin_recurrence, pin_paged, pin_flash_decoding,
-    pin_nan_guard, pin_fully_masked_row, pin_dense_layout,
+    pin_nan_guard, pin_fully_masked_row, pin_dense_layout, pin_paged_prefill,
 ]
