@@ -286,6 +286,47 @@ def run_leg(fa, name, leg, dev):
                            workspace=leg["ws"])
 
 
+def measure_paged_prefill(torch, device, fa, steps, warmup, peak):
+    """Chunked prefill over a paged cache (8 sequences, cached prefixes
+    U[1024, 16384] plus 1024 new tokens, GQA 32/8, d = 128, causal), timed
+    with CUDA events on its own after the main step."""
+    cfg = W.WORKLOADS["paged_prefill_gqa_d128"]
+    ctx, ql = W.paged_prefill_lengths(cfg["batch"], cfg["prefix_lo"], cfg["prefix_hi"],
+                                      cfg["chunk"])
+    inp = W.paged_prefill_inputs(ctx, ql, cfg["H"], cfg["Hkv"], cfg["d"], seed=0)
+    pl = inp.pool
+    q = to_dev(inp.q, torch, device)
+    kp = to_dev(pl.k_pool, torch, device)
+    vp = to_dev(pl.v_pool, torch, device)
+    table = torch.from_numpy(pl.block_table).to(device)
+    ctx_d = torch.from_numpy(pl.ctx_lens).to(device)
+    cu = torch.from_numpy(inp.cu_seqlens_q).to(device)
+    out = torch.empty_like(q)
+    lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=device)
+    flops = W.paged_prefill_flops(pl.ctx_lens, inp.q_lens, cfg["H"], cfg["d"], True)
+
+    def run():
+        fa.fa_fwd_paged(q, kp, vp, table, ctx_d, cu, inp.max_seqlen_q, pl.max_ctx_len,
+                        causal=True, out=out, lse=lse)
+
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    tf = flops / (ms / 1e3) / 1e12
+    return {"workload": "chunked prefill over a paged KV cache: 8 sequences, cached prefix "
+                        "U[1024,16384] + 1024-token chunk, H32/Hkv8, d128, causal, block16",
+            "ms": ms, "tflops": tf, "frac_of_peak": tf / peak, "flops": flops,
+            "launches_per_call": 1}
+
+
 LEG_ORDER = ("long", "varlen", "decode")
 LAUNCHES_PER_STEP = {"long": 1, "varlen": 1, "decode": 2}
 
@@ -468,6 +509,14 @@ def bench_ours(args, rank, world, local):
     e2e_ms = {name: [e2e_ev[it][i][0].elapsed_time(e2e_ev[it][i][1]) for it in range(e2e_steps)]
               for i, name in enumerate(order)}
 
+    nxt = {}
+    if args.next_legs and "long" in order:
+        peaks0 = measured_peaks()
+        nxt["paged_prefill"] = measure_paged_prefill(torch, device, fa, min(args.steps, 50),
+                                                     args.warmup, peaks0["bf16_tflops"])
+        if fa.fa_device_status(clear=True) != 0:
+            raise RuntimeError("device status word set during the paged-prefill leg")
+
     # ---- numbers (max over ranks of each time)
     K = args.steps
     t = {n: max_over_ranks(sum(leg_ms[n]) / 1e3, world, device) for n in order}
@@ -552,6 +601,7 @@ def bench_ours(args, rank, world, local):
         "roofline_decode": roof_dec,
         "e2e": {"value": e2e_tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "decode_gbs": e2e_gbs, "steps": e2e_steps},
+        "next": nxt or None,
         "gpu_launches": sum(LAUNCHES_PER_STEP[n] for n in order) * K,
         "clocks": clk,
         "cpu_baseline": cpu,
@@ -570,6 +620,8 @@ def main(argv=None):
                     help="budget of the oracle CPU-baseline sample (0: skip)")
     ap.add_argument("--legs", default="long,varlen,decode",
                     help="comma-separated subset of the step (for profiling runs)")
+    ap.add_argument("--no-next", dest="next_legs", action="store_false",
+                    help="skip the separately timed paged-prefill leg")
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="use only the first B decode sequences (for profiling runs)")
     args = ap.parse_args(argv)

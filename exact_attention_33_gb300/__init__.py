@@ -20,6 +20,7 @@ import threading
 
 __all__ = [
     "FaError", "library_path", "load_library", "fa_fwd", "fa_fwd_varlen", "fa_fwd_paged",
+    "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size",
     "fa_decode_paged", "fa_decode_paged_noalloc", "fa_decode_workspace_size",
     "fa_status_string", "fa_device_status",
     "fa_version", "FA_DEV_TIMEOUT", "FA_DEV_BAD_BLOCK", "FA_DEV_BAD_CTX", "FA_DEV_BAD_SEQLEN",
@@ -65,6 +66,10 @@ def load_library() -> ctypes.CDLL:
         lib.fa_fwd.restype = i
         lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
         lib.fa_fwd_varlen.restype = i
+        lib.fa_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i]
+        lib.fa_fwd_splitkv_workspace_size.restype = sz
+        lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
+        lib.fa_fwd_splitkv.restype = i
         lib.fa_fwd_paged.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, i, i, i, i, f, i,
                                      vp, vp, vp]
         lib.fa_fwd_paged.restype = i
@@ -156,6 +161,37 @@ def fa_fwd(q, k, v, causal=False, scale=None, out=None, lse=None, want_lse=True,
                                _scale(scale, d), 1 if causal else 0, _stream_handle(stream))
     if rc != FA_OK:
         raise FaError("fa_fwd", rc)
+    return out, lse
+
+
+def fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits=0) -> int:
+    return int(load_library().fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits))
+
+
+def fa_fwd_splitkv(q, k, v, causal=False, scale=None, num_splits=0, out=None, lse=None,
+                   workspace=None, want_lse=True, stream=None):
+    """Dense prefill with split-KV partial states and a combine (for small
+    B * H).  Same layouts as :func:`fa_fwd`."""
+    torch = _torch()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_bf16_cuda(name, t, 4)
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    if k.shape != (B, N, Hkv, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, N, Hkv, d] matching q")
+    need = fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    rc = load_library().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H,
+                                       Hkv, N, d, _scale(scale, d), 1 if causal else 0,
+                                       int(num_splits), _ptr(workspace), workspace.numel(),
+                                       _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError("fa_fwd_splitkv", rc)
     return out, lse
 
 

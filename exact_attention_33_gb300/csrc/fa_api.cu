@@ -24,6 +24,7 @@ __device__ unsigned int g_status = 0;
 cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                            const CUtensorMap &tv1, const PrefillParams &p, int d, bool causal,
                            int kind, int grid, cudaStream_t stream);
+cudaError_t launch_prefill_split_combine(const PrefillParams &p, int d, cudaStream_t stream);
 cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
                           int d, cudaStream_t stream);
 
@@ -137,6 +138,35 @@ int prefill_head_group(int H) {
   for (int g = 8; g > 1; --g)
     if (H % g == 0) return g;
   return 1;
+}
+
+// Splits of the split-KV prefill: enough CTAs for about two per SM, at most
+// 16 splits and at most one split per key tile.
+int prefill_num_splits(int B, int H, int N, int requested) {
+  const long long pairs = (N + kPrefillRowsPerCta - 1) / kPrefillRowsPerCta;
+  const int tiles = (N + kPrefillBN - 1) / kPrefillBN;
+  int s = requested;
+  if (s <= 0) {
+    int sms = sm_count();
+    if (sms <= 0) sms = 148;
+    const long long base = std::max(1LL, pairs * B * H);
+    s = static_cast<int>((2LL * sms + base - 1) / base);
+  }
+  return std::max(1, std::min({s, 16, std::max(1, tiles)}));
+}
+
+struct SplitWs {
+  int splits;
+  size_t o_bytes, ml_bytes;
+};
+
+SplitWs split_ws(int B, int H, int N, int d, int requested) {
+  SplitWs w;
+  w.splits = prefill_num_splits(B, H, N, requested);
+  const size_t rows = static_cast<size_t>(w.splits) * B * N * H;
+  w.o_bytes = round_up(rows * d * sizeof(float), 256);
+  w.ml_bytes = round_up(rows * 4 * sizeof(float), 256);
+  return w;
 }
 
 struct DecodeWs {
@@ -274,6 +304,63 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float 
   p.causal = causal;
   cudaError_t e = launch_prefill(tq, tk, tv, tv, p, d, causal != 0, kKindVarlen,
                                  static_cast<int>(grid), reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits) {
+  if (B < 0 || H < 1 || N < 0 || num_splits < 0 || (d != 64 && d != 128)) return 0;
+  const SplitWs w = split_ws(B, H, N, d, num_splits);
+  return w.o_bytes + w.ml_bytes;
+}
+
+int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                   int H, int Hkv, int N, int d, float scale, int causal, int num_splits,
+                   void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+  if (!q || !k || !v || !out) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+    return FA_ERR_INVALID_ARG;
+  if (lse && !aligned(lse, 4)) return FA_ERR_INVALID_ARG;
+  if (B < 0 || N < 0 || H < 1 || Hkv < 1 || H % Hkv != 0 || num_splits < 0)
+    return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (B == 0 || N == 0) return FA_OK;
+  const SplitWs w = split_ws(B, H, N, d, num_splits);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.o_bytes + w.ml_bytes)
+    return FA_ERR_WORKSPACE;
+  const long long pairs = (N + kPrefillRowsPerCta - 1) / kPrefillRowsPerCta;
+  const long long grid = pairs * B * H * w.splits;
+  if (grid > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(N) * H * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
+
+  CUtensorMap tq, tk, tv;
+  int rc = make_map(&tq, q, d, H, N, B, kPrefillBM);
+  if (rc == FA_OK) rc = make_map(&tk, k, d, Hkv, N, B, kPrefillBN);
+  if (rc == FA_OK) rc = make_map(&tv, v, d, Hkv, N, B, kPrefillBN);
+  if (rc != FA_OK) return rc;
+
+  PrefillParams p{};
+  p.status = status_ptr();
+  if (p.status == nullptr) return FA_ERR_CUDA;
+  p.out = out;
+  p.lse = lse;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.group = H / Hkv;
+  p.head_group = prefill_head_group(H);
+  p.N = N;
+  p.max_pairs = static_cast<int>(pairs);
+  p.scale_log2 = scale * kLog2e;
+  p.causal = causal;
+  p.num_splits = w.splits;
+  p.o_part = static_cast<float *>(workspace);
+  p.ml_part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + w.o_bytes);
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_prefill(tq, tk, tv, tv, p, d, causal != 0, kKindDenseSplit,
+                                 static_cast<int>(grid), st);
+  if (e == cudaSuccess) e = launch_prefill_split_combine(p, d, st);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

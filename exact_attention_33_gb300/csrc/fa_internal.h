@@ -26,6 +26,7 @@ constexpr int kPrefillThreads = 320;  // 8 softmax warps + 1 MMA warp + 1 TMA wa
 constexpr int kKindDense = 0;   // [B, N, H, d] batch
 constexpr int kKindVarlen = 1;  // packed sequences, cu_seqlens
 constexpr int kKindPaged = 2;   // packed query chunks over a paged KV cache
+constexpr int kKindDenseSplit = 3;  // dense batch, key tiles split over CTAs
 
 struct PrefillParams {
   unsigned int *status;   // per-device sticky FA_DEV_* word
@@ -40,6 +41,10 @@ struct PrefillParams {
   int total_tokens;       // varlen: T
   float scale_log2;       // scale * log2(e)
   int causal;
+  // split kind only: partial states
+  int num_splits;
+  float *o_part;   // fp32 [splits, B, N, H, d]
+  float *ml_part;  // fp32x4 [splits, B, N, H]: m (log2 units), l, l_exact, 0
   // paged kind only
   const int32_t *block_table;  // [num_seqs, max_blocks_per_seq]
   const int32_t *ctx_lens;     // keys per sequence

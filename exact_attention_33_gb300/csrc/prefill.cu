@@ -114,7 +114,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   // index varies slowest and the head fastest, so the CTAs running at the
   // same time share the K/V of a few heads in L2.  For causal attention the
   // pairs with the most key tiles come first in every group.
-  const int lin = blockIdx.x;
+  // Split-KV layout: the split index varies fastest; each split owns a
+  // contiguous slice of the key tiles and writes partial (m, l, o) states.
+  const int split = (KIND == kKindDenseSplit) ? static_cast<int>(blockIdx.x % p.num_splits) : 0;
+  const int lin = (KIND == kKindDenseSplit) ? static_cast<int>(blockIdx.x / p.num_splits)
+                                            : static_cast<int>(blockIdx.x);
   const int hgs = p.head_group;
   const int h_in = lin % hgs;
   const int t_lin = lin / hgs;
@@ -127,7 +131,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   // aligns causal masking to the bottom right (query i sees keys
   // j <= i + offset).
   int b, seq_start, len, kv_len, offset;
-  if (KIND == kKindDense) {
+  if (KIND == kKindDense || KIND == kKindDenseSplit) {
     b = unit;
     seq_start = 0;
     len = p.N;
@@ -178,7 +182,19 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       kv_end[i] = max(e, 1);
     }
   }
+  // This CTA's key tiles are [kv0, kv0 + n_kv); from here on kv_end[i] counts
+  // the tiles of query tile i inside that range.
+  int kv0 = 0;
+  if (KIND == kKindDenseSplit) {
+    const int total = max(kv_end[0], kv_end[1]);
+    const int per = (total + p.num_splits - 1) / p.num_splits;
+    kv0 = split * per;
+    const int stop = min(total, kv0 + per);
+#pragma unroll
+    for (int i = 0; i < kPrefillQTiles; ++i) kv_end[i] = max(0, min(kv_end[i], stop) - kv0);
+  }
   const int n_kv = max(kv_end[0], kv_end[1]);
+  const bool live1 = row0 + kPrefillBM < len;  // the second query tile has rows
 
   // ---------------------------------------------------------- shared memory
   extern __shared__ uint8_t smem_raw[];
@@ -255,7 +271,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_v1);
-      const int nq = (kv_end[1] > 0) ? 2 : 1;
+      const int nq = live1 ? 2 : 1;
       mbar_arrive_expect_tx(q_full, nq * L::kTileBytes);
       for (int i = 0; i < nq; ++i) {
         const int qrow = seq_start + row0 + i * kPrefillBM;
@@ -273,7 +289,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     int k_issued = 0, v_issued = 0;
     // physical block of slot `lane` of tile j (or -1), and its valid rows
     auto lookup = [&](int j, int &rows) -> int {
-      const int blk = j * kBlkPerTile + lane;
+      const int blk = (kv0 + j) * kBlkPerTile + lane;
       rows = 0;
       if (lane >= kBlkPerTile || blk >= total_blk) return -1;
       const int phys = trow[blk];
@@ -355,7 +371,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      const int nq = (kv_end[1] > 0) ? 2 : 1;
+      const int nq = live1 ? 2 : 1;
       mbar_arrive_expect_tx(q_full, nq * L::kTileBytes);
       for (int i = 0; i < nq; ++i) {
         const int qrow = seq_start + row0 + i * kPrefillBM;
@@ -375,7 +391,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c)
           tma_load_4d(sK + sk * L::kTileBytes + c * L::kChunkBytes, &tm_k, &k_full[sk], c * 64,
-                      kvh, seq_start + j * kPrefillBN, b);
+                      kvh, seq_start + (kv0 + j) * kPrefillBN, b);
         k_issued = j + 1;
         return true;
       };
@@ -387,7 +403,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c)
           tma_load_4d(sV + sv * L::kTileBytes + c * L::kChunkBytes, &tm_v, &v_full[sv], c * 64,
-                      kvh, seq_start + j * kPrefillBN, b);
+                      kvh, seq_start + (kv0 + j) * kPrefillBN, b);
         v_issued = j + 1;
         return true;
       };
@@ -444,7 +460,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       // other tile's products.  S_i(j+1) reuses the TMEM columns that PV_i(j),
       // issued just before it by this thread, reads P_i(j) from; tcgen05 MMAs
       // issued by one thread execute in order.
-      bool ok = mbar_wait_warp(q_full, 0, abort_flag, p.status) &&
+      // (a split that owns no key tile issues nothing)
+      bool ok = n_kv > 0 && mbar_wait_warp(q_full, 0, abort_flag, p.status) &&
                 mbar_wait_warp(&k_full[0], 0, abort_flag, p.status);
       if (ok) {
         tc_fence_after();
@@ -523,7 +540,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
       uint32_t sr[128];
       tmem_ld128_wait(tS, sr);
-      const int nvis = limit - j * kPrefillBN;
+      const int nvis = limit - (kv0 + j) * kPrefillBN;
       if (__any_sync(0xffffffffu, nvis < kPrefillBN)) {
 #pragma unroll
         for (int c = 0; c < 128; ++c)
@@ -603,7 +620,39 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const float m = m_ref;
 
     // ---------------------------------------------------- epilogue
-    if (ok && my_end > 0) {
+    if (KIND == kKindDenseSplit) {
+      // Partial state of this split: o unnormalised (fp32), m (log2 units),
+      // l over the bf16 weights and l over the fp32 exponentials.  A row of
+      // a live tile that got no key tile stores the neutral state.
+      const bool tile_live = row0 + i * kPrefillBM < len;
+      bool have = ok && my_end > 0;
+      if (have) {
+        have = mbar_wait(&o_done[i], (my_end - 1) & 1, abort_flag, p.status);
+        have = __all_sync(0xffffffffu, have);
+      }
+      if (tile_live && (have || my_end == 0)) {
+        if (have) tc_fence_after();
+        const bool live = qi < len;
+        const size_t prow = (static_cast<size_t>(split) * p.B + b) * p.N + qi;
+        float *orow = p.o_part + (prow * p.H + h) * D;
+        if (have) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32_wait(tO + c * 32, o);
+            if (live) {
+#pragma unroll
+              for (int v4 = 0; v4 < 8; ++v4)
+                reinterpret_cast<uint4 *>(orow)[c * 8 + v4] =
+                    make_uint4(o[v4 * 4], o[v4 * 4 + 1], o[v4 * 4 + 2], o[v4 * 4 + 3]);
+            }
+          }
+        }
+        if (live)
+          reinterpret_cast<float4 *>(p.ml_part)[prow * p.H + h] =
+              have ? make_float4(m, l, l_exact, 0.f) : make_float4(-CUDART_INF_F, 0.f, 0.f, 0.f);
+      }
+    } else if (ok && my_end > 0) {
       ok = mbar_wait(&o_done[i], (my_end - 1) & 1, abort_flag, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
@@ -659,6 +708,63 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------ split combine
+// One warp per (batch, row, head) merges the partial states of the splits
+// with the rescaling of the explainer page's "Show the maths":
+// M = max m_s, o = sum 2^(m_s - M) o_s / sum 2^(m_s - M) l_s,
+// lse = (M + log2 sum 2^(m_s - M) l_exact_s) ln 2.
+template <int D>
+__global__ void __launch_bounds__(128) prefill_split_combine_kernel(const PrefillParams p) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const size_t rows = static_cast<size_t>(p.B) * p.N * p.H;
+  const size_t gw = static_cast<size_t>(blockIdx.x) * 4 + warp;
+  if (gw >= rows) return;
+  const size_t bn = gw / p.H;  // b * N + n
+  const int h = static_cast<int>(gw % p.H);
+  const size_t stride = static_cast<size_t>(p.B) * p.N * p.H;  // between splits
+  const float4 *ml = reinterpret_cast<const float4 *>(p.ml_part) + gw;
+  float M = -CUDART_INF_F;
+  for (int s = 0; s < p.num_splits; ++s) M = fmaxf(M, ml[s * stride].x);
+  constexpr int E = D / 32;
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float Ls = 0.f, Le = 0.f;
+  if (M != -CUDART_INF_F) {
+    for (int s = 0; s < p.num_splits; ++s) {
+      const float4 st = ml[s * stride];
+      if (st.x == -CUDART_INF_F) continue;  // a split without keys for this row
+      const float w = ex2(st.x - M);
+      Ls += w * st.y;
+      Le += w * st.z;
+      const float *orow = p.o_part + (s * stride + gw) * D + lane * E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] += w * orow[e];
+    }
+  }
+  const float inv = (Ls > 0.f) ? 1.f / Ls : 0.f;
+  uint16_t *dst = static_cast<uint16_t *>(p.out) + gw * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; e += 2)
+    *reinterpret_cast<uint32_t *>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+  if (lane == 0 && p.lse != nullptr) {
+    const size_t b = bn / p.N, n = bn % p.N;
+    p.lse[(b * p.H + h) * p.N + n] =
+        (Le > 0.f) ? (M + __log2f(Le)) * 0.69314718055994530942f : -CUDART_INF_F;
+  }
+}
+
+cudaError_t launch_prefill_split_combine(const PrefillParams &p, int d, cudaStream_t stream) {
+  const size_t rows = static_cast<size_t>(p.B) * p.N * p.H;
+  const unsigned grid = static_cast<unsigned>((rows + 3) / 4);
+  if (d == 64)
+    prefill_split_combine_kernel<64><<<grid, 128, 0, stream>>>(p);
+  else
+    prefill_split_combine_kernel<128><<<grid, 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ launch
 
 template <int D, bool CAUSAL, int KIND>
@@ -691,12 +797,16 @@ cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const C
       return launch_prefill_k<64, kKindDense>(tq, tk, tv, tv1, p, causal, grid, stream);
     if (kind == kKindVarlen)
       return launch_prefill_k<64, kKindVarlen>(tq, tk, tv, tv1, p, causal, grid, stream);
+    if (kind == kKindDenseSplit)
+      return launch_prefill_k<64, kKindDenseSplit>(tq, tk, tv, tv1, p, causal, grid, stream);
     return launch_prefill_k<64, kKindPaged>(tq, tk, tv, tv1, p, causal, grid, stream);
   }
   if (kind == kKindDense)
     return launch_prefill_k<128, kKindDense>(tq, tk, tv, tv1, p, causal, grid, stream);
   if (kind == kKindVarlen)
     return launch_prefill_k<128, kKindVarlen>(tq, tk, tv, tv1, p, causal, grid, stream);
+  if (kind == kKindDenseSplit)
+    return launch_prefill_k<128, kKindDenseSplit>(tq, tk, tv, tv1, p, causal, grid, stream);
   return launch_prefill_k<128, kKindPaged>(tq, tk, tv, tv1, p, causal, grid, stream);
 }
 

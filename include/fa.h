@@ -100,6 +100,25 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float 
                   fa_stream_t stream);
 
 /*
+ * Dense prefill with the key tiles of every query tile split over several
+ * CTAs, for batches whose B * H * ceil(N / 256) work items cannot fill the
+ * GPU (long single sequences).  "S12 FlashAttention", "What this unlocks
+ * beyond speed": the same recurrence applied across processors - each split
+ * produces a partial (m, l, o) state and a second kernel merges them with the
+ * rescaling of the explainer page's "Show the maths".
+ * Arguments and results as fa_fwd, plus:
+ *   num_splits : 1..16, or 0 to let the library choose (about two CTAs per
+ *                SM); values above the number of 128-key tiles are clamped.
+ *   workspace  : >= fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits)
+ *                bytes, 256-byte aligned, owned by the caller.
+ * Two kernels run in stream order: the split prefill and the combine.
+ */
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits);
+int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                   int H, int Hkv, int N, int d, float scale, int causal, int num_splits,
+                   void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * Prefill of query chunks against a paged KV cache (chunked prefill / cached
  * prefix): "S12 FlashAttention", "Implementation" - the paged variant is the
  * same tiled recurrence with the block table in front of the key access.
