@@ -50,6 +50,10 @@ if ROOT not in sys.path:
 from exact_attention_33_gb300 import workloads as W  # noqa: E402
 
 METRIC = "prefill TFLOP/s & % bf16 tensor peak; paged-decode HBM GB/s & % of 8 TB/s"
+WORKLOAD_TEXT = ("exact-attention hot path: long-context causal prefill B2 H32 N8192 d128 "
+                 "(1% x8 key outliers) + packed varlen causal prefill 32 seqs U[64,4096] "
+                 "H16/Hkv4 d128 + paged GQA decode batch64 H32/Hkv8 d128 ctx U[512,32768] "
+                 "block16")
 NOMINAL_HBM_GBS = 8000.0
 PROFILES = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = {
@@ -421,8 +425,10 @@ def bench_reference(args, rank, world):
         "steps": steps, "warmup": warmup, "ms_per_step": 1e3 * total_t / steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "long-context causal prefill B2 H32 N8192 d128 (oracle sample)",
-                   "sample": "per step: one seeded (batch, head) pair, 1024 seeded query rows"},
+        "config": {"workload": WORKLOAD_TEXT,
+                   "sample": "per step: the oracle on one seeded (batch, head) pair of the "
+                             "long-context causal prefill, 1024 seeded query rows",
+                   "parallelism": "host cores, rank 0 only"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(),
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -580,10 +586,7 @@ def bench_ours(args, rank, world, local):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {
-            "workload": "exact-attention hot path: long-context causal prefill B2 H32 N8192 d128 "
-                        "(1% x8 key outliers) + packed varlen causal prefill 32 seqs U[64,4096] "
-                        "H16/Hkv4 d128 + paged GQA decode batch64 H32/Hkv8 d128 ctx U[512,32768] "
-                        "block16",
+            "workload": WORKLOAD_TEXT,
             "legs": order,
             "decode_batch": args.decode_batch or 64,
             "prefill_flops_per_step": f_pre,
