@@ -85,6 +85,8 @@ def load_library() -> ctypes.CDLL:
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i]
         lib.fa_device_status.restype = i
+        lib.fa_selftest_wait_timeout.argtypes = [vp, vp]
+        lib.fa_selftest_wait_timeout.restype = i
         lib.fa_version.argtypes = []
         lib.fa_version.restype = i
         _lib = lib
@@ -97,6 +99,18 @@ def fa_status_string(status: int) -> str:
 
 def fa_version() -> int:
     return int(load_library().fa_version())
+
+
+def fa_selftest_wait_timeout(stream=None) -> int:
+    """Run the bounded-wait self-test; returns the wait's result (0 = it gave
+    up, as intended).  FA_DEV_TIMEOUT is set in the status word afterwards."""
+    torch = _torch()
+    res = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    rc = load_library().fa_selftest_wait_timeout(_ptr(res), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError("fa_selftest_wait_timeout", rc)
+    torch.cuda.synchronize()
+    return int(res.item())
 
 
 def fa_device_status(clear: bool = True) -> int:

@@ -16,6 +16,7 @@
 
 #include "../../include/fa.h"
 #include "fa_internal.h"
+#include "ptx.cuh"
 
 namespace fa {
 
@@ -186,6 +187,22 @@ DecodeWs decode_ws(int batch, int H, int Hkv, int d, int max_ctx_len) {
   return w;
 }
 
+// Waits, through the same bounded mbar_wait that every pipeline uses, on an
+// mbarrier that nothing arrives at; the wait gives up after kWaitLimitNs and
+// raises FA_DEV_TIMEOUT.  Lets the failure path be tested without faulting.
+__global__ void wait_timeout_selftest_kernel(unsigned int *status, int *result) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const bool ok = mbar_wait(&bar, 0, &abort_flag, status);
+  if (threadIdx.x == 0) *result = ok ? 1 : 0;
+}
+
 }  // namespace
 }  // namespace fa
 
@@ -216,6 +233,15 @@ int fa_device_status(unsigned int *status, int clear) {
     if (cudaMemcpyToSymbol(g_status, &z, sizeof(z)) != cudaSuccess) return FA_ERR_CUDA;
   }
   return FA_OK;
+}
+
+int fa_selftest_wait_timeout(int *wait_result, fa_stream_t stream) {
+  if (wait_result == nullptr) return FA_ERR_INVALID_ARG;
+  unsigned int *st = status_ptr();
+  if (st == nullptr) return FA_ERR_CUDA;
+  wait_timeout_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(st,
+                                                                                   wait_result);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,

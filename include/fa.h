@@ -222,6 +222,15 @@ const char *fa_status_string(int status);
  */
 int fa_device_status(unsigned int *status, int clear);
 
+/*
+ * Self-test of the failure path: launches one warp that waits, through the
+ * library's bounded pipeline wait, on a barrier that nothing completes.  The
+ * wait gives up after about one second, sets FA_DEV_TIMEOUT in the status
+ * word and writes 0 to *wait_result (a DEVICE int; 1 would mean the wait
+ * succeeded).  The context stays usable.  Asynchronous on `stream`.
+ */
+int fa_selftest_wait_timeout(int *wait_result, fa_stream_t stream);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int fa_version(void);
 
