@@ -331,6 +331,42 @@ def measure_paged_prefill(torch, device, fa, steps, warmup, peak):
             "launches_per_call": 1}
 
 
+def measure_fp8_prefill(torch, device, fa, steps, warmup, peak_bf16):
+    """FP8 (e4m3) dense causal prefill at the long-context shape (B=2, H=32,
+    N=8192, d=128), timed with CUDA events on its own after the main step.
+    Its peak is the measured bf16 figure times the nominal fp8 / bf16 tensor
+    ratio (4.5 / 2.25 PFLOP/s)."""
+    cfg = W.WORKLOADS["long_causal_fp8_d128"]
+    inp = W.fp8_inputs(cfg["B"], cfg["N"], cfg["H"], cfg["Hkv"], cfg["d"], seed=0)
+    q, k, v = (torch.from_numpy(getattr(inp, n)).to(device) for n in ("q", "k", "v"))
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=device)
+    lse = torch.empty((cfg["B"], cfg["H"], cfg["N"]), dtype=torch.float32, device=device)
+    flops = W.prefill_flops(cfg["B"], cfg["N"], cfg["H"], cfg["d"], True)
+
+    def run():
+        fa.fa_fwd_fp8(q, k, v, inp.q_descale, inp.k_descale, inp.v_descale, causal=True,
+                      out=out, lse=lse)
+
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    tf = flops / (ms / 1e3) / 1e12
+    peak = 2.0 * peak_bf16
+    return {"workload": "FP8 e4m3 dense causal prefill, B2 H32 N8192 d128, per-tensor descales "
+                        "(N(0,1) quantised)",
+            "ms": ms, "tflops": tf, "frac_of_peak": tf / peak, "peak_tflops": peak,
+            "peak_source": "measured bf16 burst x 2 (nominal fp8/bf16 ratio)", "flops": flops,
+            "launches_per_call": 1}
+
+
 LEG_ORDER = ("long", "varlen", "decode")
 LAUNCHES_PER_STEP = {"long": 1, "varlen": 1, "decode": 2}
 
@@ -522,6 +558,10 @@ def bench_ours(args, rank, world, local):
                                                      args.warmup, peaks0["bf16_tflops"])
         if fa.fa_device_status(clear=True) != 0:
             raise RuntimeError("device status word set during the paged-prefill leg")
+        nxt["fp8_prefill"] = measure_fp8_prefill(torch, device, fa, min(args.steps, 50),
+                                                 args.warmup, peaks0["bf16_tflops"])
+        if fa.fa_device_status(clear=True) != 0:
+            raise RuntimeError("device status word set during the fp8 prefill leg")
 
     # ---- numbers (max over ranks of each time)
     K = args.steps

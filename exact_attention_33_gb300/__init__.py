@@ -20,7 +20,7 @@ import threading
 
 __all__ = [
     "FaError", "library_path", "load_library", "fa_fwd", "fa_fwd_varlen", "fa_fwd_paged",
-    "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size",
+    "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_fwd_fp8",
     "fa_decode_paged", "fa_decode_paged_noalloc", "fa_decode_workspace_size",
     "fa_status_string", "fa_device_status",
     "fa_version", "FA_DEV_TIMEOUT", "FA_DEV_BAD_BLOCK", "FA_DEV_BAD_CTX", "FA_DEV_BAD_SEQLEN",
@@ -66,6 +66,8 @@ def load_library() -> ctypes.CDLL:
         lib.fa_fwd.restype = i
         lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
         lib.fa_fwd_varlen.restype = i
+        lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, f, f, f, i, vp]
+        lib.fa_fwd_fp8.restype = i
         lib.fa_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i]
         lib.fa_fwd_splitkv_workspace_size.restype = sz
         lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
@@ -175,6 +177,29 @@ def fa_fwd(q, k, v, causal=False, scale=None, out=None, lse=None, want_lse=True,
                                _scale(scale, d), 1 if causal else 0, _stream_handle(stream))
     if rc != FA_OK:
         raise FaError("fa_fwd", rc)
+    return out, lse
+
+
+def fa_fwd_fp8(q, k, v, q_descale, k_descale, v_descale, causal=False, scale=None, out=None,
+               lse=None, want_lse=True, stream=None):
+    """Dense prefill on e4m3 codes.  q [B,N,H,d], k/v [B,N,Hkv,d] uint8 CUDA
+    tensors holding e4m3 bits; per-tensor descales.  Returns (out bf16, lse)."""
+    torch = _torch()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or t.dtype not in (torch.uint8, torch.float8_e4m3fn) or t.dim() != 4 \
+                or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D uint8/e4m3 CUDA tensor")
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    if out is None:
+        out = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    rc = load_library().fa_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv,
+                                   N, d, _scale(scale, d), float(q_descale), float(k_descale),
+                                   float(v_descale), 1 if causal else 0, _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError("fa_fwd_fp8", rc)
     return out, lse
 
 

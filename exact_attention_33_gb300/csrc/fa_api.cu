@@ -26,6 +26,9 @@ cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const C
                            const CUtensorMap &tv1, const PrefillParams &p, int d, bool causal,
                            int kind, int grid, cudaStream_t stream);
 cudaError_t launch_prefill_split_combine(const PrefillParams &p, int d, cudaStream_t stream);
+cudaError_t launch_prefill_fp8(const CUtensorMap &tq, const CUtensorMap &tk,
+                               const CUtensorMap &tv, const PrefillParams &p, bool causal,
+                               int grid, cudaStream_t stream);
 cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
                           int d, cudaStream_t stream);
 
@@ -53,17 +56,22 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // dims {d, heads, rows, outer}; each copy moves a box of {64, 1, box_rows, 1}
 // with 128-byte swizzle.  Out-of-range rows read as zero.
 int make_map(CUtensorMap *map, const void *base, int d, int heads, long long rows,
-             long long outer, int box_rows) {
+             long long outer, int box_rows, int elem_bytes = 2) {
   auto fn = encode_fn();
   if (fn == nullptr) return FA_ERR_CUDA;
+  const cuuint64_t eb = static_cast<cuuint64_t>(elem_bytes);
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
                               static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(outer)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2,
-                                 static_cast<cuuint64_t>(heads) * d * 2,
-                                 static_cast<cuuint64_t>(rows) * heads * d * 2};
-  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * eb,
+                                 static_cast<cuuint64_t>(heads) * d * eb,
+                                 static_cast<cuuint64_t>(rows) * heads * d * eb};
+  // one 128-byte swizzle row per copy: 64 bf16 or 128 one-byte values
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / elem_bytes), 1,
+                             static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+  const CUtensorMapDataType dt =
+      elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = fn(map, dt, 4, const_cast<void *>(base), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
@@ -281,6 +289,7 @@ int fa_fwd(const void *q, const void *k, const void *v, void *out, float *lse, i
   p.max_pairs = static_cast<int>(pairs);
   p.total_tokens = 0;
   p.scale_log2 = scale * kLog2e;
+  p.v_descale = 1.f;
   p.causal = causal;
   cudaError_t e = launch_prefill(tq, tk, tv, tv, p, d, causal != 0, kKindDense,
                                  static_cast<int>(grid), reinterpret_cast<cudaStream_t>(stream));
@@ -327,9 +336,53 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float 
   p.max_pairs = static_cast<int>(pairs);
   p.total_tokens = total_tokens;
   p.scale_log2 = scale * kLog2e;
+  p.v_descale = 1.f;
   p.causal = causal;
   cudaError_t e = launch_prefill(tq, tk, tv, tv, p, d, causal != 0, kKindVarlen,
                                  static_cast<int>(grid), reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_fwd_fp8(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
+               int Hkv, int N, int d, float scale, float q_descale, float k_descale,
+               float v_descale, int causal, fa_stream_t stream) {
+  if (!q || !k || !v || !out) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+    return FA_ERR_INVALID_ARG;
+  if (lse && !aligned(lse, 4)) return FA_ERR_INVALID_ARG;
+  if (B < 0 || N < 0 || H < 1 || Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!scale_ok(scale) || !scale_ok(q_descale) || !scale_ok(k_descale) ||
+      !scale_ok(v_descale))
+    return FA_ERR_INVALID_ARG;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (B == 0 || N == 0) return FA_OK;
+  const long long pairs = (N + kPrefillRowsPerCta - 1) / kPrefillRowsPerCta;
+  const long long grid = pairs * B * H;
+  if (grid > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(N) * H * d >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
+  CUtensorMap tq, tk, tv;
+  int rc = make_map(&tq, q, d, H, N, B, kPrefillBM, 1);
+  if (rc == FA_OK) rc = make_map(&tk, k, d, Hkv, N, B, kPrefillBN, 1);
+  if (rc == FA_OK) rc = make_map(&tv, v, d, Hkv, N, B, kPrefillBN, 1);
+  if (rc != FA_OK) return rc;
+  PrefillParams p{};
+  p.status = status_ptr();
+  if (p.status == nullptr) return FA_ERR_CUDA;
+  p.out = out;
+  p.lse = lse;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.group = H / Hkv;
+  p.head_group = prefill_head_group(H);
+  p.N = N;
+  p.max_pairs = static_cast<int>(pairs);
+  p.scale_log2 = scale * q_descale * k_descale * kLog2e;
+  p.v_descale = v_descale;
+  p.causal = causal;
+  cudaError_t e = launch_prefill_fp8(tq, tk, tv, p, causal != 0, static_cast<int>(grid),
+                                     reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -379,6 +432,7 @@ int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *out, float
   p.N = N;
   p.max_pairs = static_cast<int>(pairs);
   p.scale_log2 = scale * kLog2e;
+  p.v_descale = 1.f;
   p.causal = causal;
   p.num_splits = w.splits;
   p.o_part = static_cast<float *>(workspace);
@@ -442,6 +496,7 @@ int fa_fwd_paged(const void *q, const void *k_pool, const void *v_pool,
   p.max_pairs = static_cast<int>(pairs);
   p.total_tokens = total_q;
   p.scale_log2 = scale * kLog2e;
+  p.v_descale = 1.f;
   p.causal = causal;
   p.block_table = block_table;
   p.ctx_lens = ctx_lens;

@@ -39,7 +39,8 @@ struct PrefillParams {
   int N;                  // dense: sequence length; varlen: total tokens
   int max_pairs;          // number of 256-row query-tile pairs of the longest sequence
   int total_tokens;       // varlen: T
-  float scale_log2;       // scale * log2(e)
+  float scale_log2;       // scale * log2(e) (times the q and k descales for fp8)
+  float v_descale;        // multiplies the output (1 for bf16)
   int causal;
   // split kind only: partial states
   int num_splits;

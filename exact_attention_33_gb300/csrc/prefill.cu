@@ -38,10 +38,12 @@ namespace fa {
 // grows by more than this many powers of two.
 constexpr float kRescaleLog2 = 8.f;
 
-template <int D>
+template <int D, bool FP8 = false>
 struct PrefillLayout {
-  static constexpr int kChunkBytes = 128 * 128;        // 128 rows x 64 bf16 (one swizzle span)
-  static constexpr int kChunks = D / 64;
+  static constexpr int kElemBytes = FP8 ? 1 : 2;
+  static constexpr int kChunkElems = 128 / kElemBytes;   // elements per 128-byte swizzle row
+  static constexpr int kChunkBytes = 128 * 128;          // 128 rows x 128 bytes
+  static constexpr int kChunks = D * kElemBytes / 128;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
   // K and V have rings of their own: a K stage is released as soon as both
   // S MMAs have read it, a V stage after both P V MMAs.
@@ -49,8 +51,8 @@ struct PrefillLayout {
 #define FA_PREFILL_STAGES_K128 3
 #define FA_PREFILL_STAGES_V128 2
 #endif
-  static constexpr int kStagesK = (D == 128) ? FA_PREFILL_STAGES_K128 : 5;
-  static constexpr int kStagesV = (D == 128) ? FA_PREFILL_STAGES_V128 : 5;
+  static constexpr int kStagesK = (kTileBytes == 32768) ? FA_PREFILL_STAGES_K128 : 5;
+  static constexpr int kStagesV = (kTileBytes == 32768) ? FA_PREFILL_STAGES_V128 : 5;
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kPrefillQTiles * kTileBytes;
   static constexpr int kV = kK + kStagesK * kTileBytes;
@@ -98,13 +100,13 @@ __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]
 
 // KIND: dense batch, packed varlen batch, or packed queries over a paged KV
 // cache (chunked prefill).
-template <int D, bool CAUSAL, int KIND>
+template <int D, bool CAUSAL, int KIND, bool FP8 = false>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v,
                    const __grid_constant__ CUtensorMap tm_v1, const PrefillParams p) {
-  using L = PrefillLayout<D>;
+  using L = PrefillLayout<D, FP8>;
   constexpr int SK = L::kStagesK;
   constexpr int SV = L::kStagesV;
 
@@ -277,7 +279,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const int qrow = seq_start + row0 + i * kPrefillBM;
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c)
-          tma_load_4d(sQ + i * L::kTileBytes + c * L::kChunkBytes, &tm_q, q_full, c * 64, h,
+          tma_load_4d(sQ + i * L::kTileBytes + c * L::kChunkBytes, &tm_q, q_full, c * L::kChunkElems, h,
                       qrow, b);
       }
     }
@@ -315,7 +317,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
           for (int c = 0; c < L::kChunks; ++c)
             tma_load_3d(sK + sk * L::kTileBytes + c * L::kChunkBytes + t * kDecodeBlock * 128,
-                        &tm_k, &k_full[sk], c * 64, kvh, pb * kDecodeBlock);
+                        &tm_k, &k_full[sk], c * L::kChunkElems, kvh, pb * kDecodeBlock);
         }
       }
       k_issued = j + 1;
@@ -338,13 +340,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           if (nr == kDecodeBlock) {
 #pragma unroll
             for (int c = 0; c < L::kChunks; ++c)
-              tma_load_3d(dst + c * L::kChunkBytes, &tm_v, &v_full[sv], c * 64, kvh,
+              tma_load_3d(dst + c * L::kChunkBytes, &tm_v, &v_full[sv], c * L::kChunkElems, kvh,
                           pb * kDecodeBlock);
           } else {
             for (int r = 0; r < nr; ++r)
 #pragma unroll
               for (int c = 0; c < L::kChunks; ++c)
-                tma_load_3d(dst + c * L::kChunkBytes + r * 128, &tm_v1, &v_full[sv], c * 64, kvh,
+                tma_load_3d(dst + c * L::kChunkBytes + r * 128, &tm_v1, &v_full[sv], c * L::kChunkElems, kvh,
                             pb * kDecodeBlock + r);
           }
         }
@@ -377,7 +379,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const int qrow = seq_start + row0 + i * kPrefillBM;
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c)
-          tma_load_4d(sQ + i * L::kTileBytes + c * L::kChunkBytes, &tm_q, q_full, c * 64, h,
+          tma_load_4d(sQ + i * L::kTileBytes + c * L::kChunkBytes, &tm_q, q_full, c * L::kChunkElems, h,
                       qrow, b);
       }
       // Issue order K(0), then V(j), K(j+1) for every j: a V load never waits
@@ -390,7 +392,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         mbar_arrive_expect_tx(&k_full[sk], L::kTileBytes);
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c)
-          tma_load_4d(sK + sk * L::kTileBytes + c * L::kChunkBytes, &tm_k, &k_full[sk], c * 64,
+          tma_load_4d(sK + sk * L::kTileBytes + c * L::kChunkBytes, &tm_k, &k_full[sk], c * L::kChunkElems,
                       kvh, seq_start + (kv0 + j) * kPrefillBN, b);
         k_issued = j + 1;
         return true;
@@ -402,7 +404,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         mbar_arrive_expect_tx(&v_full[sv], L::kTileBytes);
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c)
-          tma_load_4d(sV + sv * L::kTileBytes + c * L::kChunkBytes, &tm_v, &v_full[sv], c * 64,
+          tma_load_4d(sV + sv * L::kTileBytes + c * L::kChunkBytes, &tm_v, &v_full[sv], c * L::kChunkElems,
                       kvh, seq_start + (kv0 + j) * kPrefillBN, b);
         v_issued = j + 1;
         return true;
@@ -426,8 +428,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     // The whole warp runs this loop converged; elect.sync picks the lane
     // that issues each tcgen05 instruction.
     {
-      constexpr uint32_t kIdescS = idesc_bf16_f32(kPrefillBM, kPrefillBN, false, false);
-      constexpr uint32_t kIdescO = idesc_bf16_f32(kPrefillBM, D, false, true);
+      // one MMA consumes 32 bytes of the contraction: 16 bf16 or 32 e4m3 values
+      constexpr int kKStep = 32 / L::kElemBytes;
+      constexpr uint32_t kIdescS = FP8 ? idesc_e4m3_f32(kPrefillBM, kPrefillBN, false, false)
+                                       : idesc_bf16_f32(kPrefillBM, kPrefillBN, false, false);
+      constexpr uint32_t kIdescO = FP8 ? idesc_e4m3_f32(kPrefillBM, D, false, true)
+                                       : idesc_bf16_f32(kPrefillBM, D, false, true);
       const uint32_t q_base = smem_u32(sQ);
       const uint32_t k_base = smem_u32(sK);
       const uint32_t v_base = smem_u32(sV);
@@ -435,11 +441,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       auto issue_s = [&](int i, int st) {
         const uint32_t d_t = tmem + i * 128;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < D / kKStep; ++kk) {
           const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
           const uint64_t a = sdesc_sw128(q_base + i * L::kTileBytes + off, 16, 1024);
           const uint64_t bd = sdesc_sw128(k_base + st * L::kTileBytes + off, 16, 1024);
-          mma_ss_elect(d_t, a, bd, kIdescS, kk > 0 ? 1u : 0u);
+          if (FP8)
+            mma_ss_f8_elect(d_t, a, bd, kIdescS, kk > 0 ? 1u : 0u);
+          else
+            mma_ss_elect(d_t, a, bd, kIdescS, kk > 0 ? 1u : 0u);
         }
         mma_commit_elect(&s_full[i]);
       };
@@ -447,10 +456,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const uint32_t d_t = tmem + L::kTmemO + i * D;
         const uint32_t p_t = tmem + i * 128;
 #pragma unroll
-        for (int kk = 0; kk < kPrefillBN / 16; ++kk) {
-          const uint64_t bd =
-              sdesc_sw128(v_base + st * L::kTileBytes + kk * 2048, L::kChunkBytes, 1024);
-          mma_ts_elect(d_t, p_t + kk * 8, bd, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kPrefillBN / kKStep; ++kk) {
+          // kKStep keys of 128-byte rows; P holds kKStep keys in 8 TMEM columns
+          const uint64_t bd = sdesc_sw128(v_base + st * L::kTileBytes + kk * kKStep * 128,
+                                          L::kChunkBytes, 1024);
+          if (FP8)
+            mma_ts_f8_elect(d_t, p_t + kk * 8, bd, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+          else
+            mma_ts_elect(d_t, p_t + kk * 8, bd, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit_elect(&o_done[i]);
       };
@@ -573,26 +586,51 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       float2 rs0 = make_float2(0.f, 0.f), rs1 = make_float2(0.f, 0.f);
       float2 re0 = make_float2(0.f, 0.f), re1 = make_float2(0.f, 0.f);
       // P in two halves of 64 keys, each stored to TMEM as soon as it is packed
+      if (!FP8) {
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const int e = half * 64 + 2 * c;
-          const float2 x0 = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
-                                  sl2x2, negm);
-          const float2 x1 = ffma2(make_float2(__uint_as_float(sr[e + 2]),
-                                              __uint_as_float(sr[e + 3])), sl2x2, negm);
-          const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
-          const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
-          pk[c] = pack_bf16x2(p0.x, p0.y);
-          pk[c + 1] = pack_bf16x2(p1.x, p1.y);
-          re0 = fadd2(re0, p0);
-          re1 = fadd2(re1, p1);
-          rs0 = fadd2(rs0, bf16x2_to_float2(pk[c]));
-          rs1 = fadd2(rs1, bf16x2_to_float2(pk[c + 1]));
+          for (int c = 0; c < 32; c += 2) {
+            const int e = half * 64 + 2 * c;
+            const float2 x0 = ffma2(
+                make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2x2, negm);
+            const float2 x1 = ffma2(
+                make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), sl2x2, negm);
+            const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
+            const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+            pk[c] = pack_bf16x2(p0.x, p0.y);
+            pk[c + 1] = pack_bf16x2(p1.x, p1.y);
+            re0 = fadd2(re0, p0);
+            re1 = fadd2(re1, p1);
+            rs0 = fadd2(rs0, bf16x2_to_float2(pk[c]));
+            rs1 = fadd2(rs1, bf16x2_to_float2(pk[c + 1]));
+          }
+          tmem_st32(tS + half * 32, pk);
         }
-        tmem_st32(tS + half * 32, pk);
+      } else {
+        // e4m3 P, four keys per TMEM column.  Its 3-bit mantissa leaves the
+        // weights as they are rounded; both sums use the fp32 exponentials.
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int e = half * 64 + 4 * c;
+            const float2 x0 = ffma2(
+                make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2x2, negm);
+            const float2 x1 = ffma2(
+                make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), sl2x2, negm);
+            const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
+            const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+            pk[c] = pack_e4m3x4(p0.x, p0.y, p1.x, p1.y);
+            re0 = fadd2(re0, p0);
+            re1 = fadd2(re1, p1);
+          }
+          tmem_st16(tS + half * 16, pk);
+        }
+        rs0 = re0;
+        rs1 = re1;
       }
       const float2 rs = fadd2(rs0, rs1);
       const float2 re = fadd2(re0, re1);
@@ -658,7 +696,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       if (ok) {
         tc_fence_after();
         const bool live = qi < len;
-        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        const float inv_l = (l > 0.f) ? p.v_descale / l : 0.f;
         size_t out_row;
         if (KIND != kKindDense)
           out_row = static_cast<size_t>(seq_start + qi);
@@ -767,12 +805,12 @@ cudaError_t launch_prefill_split_combine(const PrefillParams &p, int d, cudaStre
 
 // ------------------------------------------------------------------ launch
 
-template <int D, bool CAUSAL, int KIND>
+template <int D, bool CAUSAL, int KIND, bool FP8 = false>
 static cudaError_t launch_prefill_t(const CUtensorMap &tq, const CUtensorMap &tk,
                                     const CUtensorMap &tv, const CUtensorMap &tv1,
                                     const PrefillParams &p, int grid, cudaStream_t stream) {
-  using L = PrefillLayout<D>;
-  auto kern = prefill_kernel<D, CAUSAL, KIND>;
+  using L = PrefillLayout<D, FP8>;
+  auto kern = prefill_kernel<D, CAUSAL, KIND, FP8>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
   if (e != cudaSuccess) return e;
@@ -787,6 +825,13 @@ static cudaError_t launch_prefill_k(const CUtensorMap &tq, const CUtensorMap &tk
                                     cudaStream_t stream) {
   return causal ? launch_prefill_t<D, true, KIND>(tq, tk, tv, tv1, p, grid, stream)
                 : launch_prefill_t<D, false, KIND>(tq, tk, tv, tv1, p, grid, stream);
+}
+
+cudaError_t launch_prefill_fp8(const CUtensorMap &tq, const CUtensorMap &tk,
+                               const CUtensorMap &tv, const PrefillParams &p, bool causal,
+                               int grid, cudaStream_t stream) {
+  return causal ? launch_prefill_t<128, true, kKindDense, true>(tq, tk, tv, tv, p, grid, stream)
+                : launch_prefill_t<128, false, kKindDense, true>(tq, tk, tv, tv, p, grid, stream);
 }
 
 cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,

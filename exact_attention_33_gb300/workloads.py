@@ -45,6 +45,8 @@ WORKLOADS = {
                                   ctx_lo=512, ctx_hi=32768),
     # chunked prefill over a paged cache: each sequence has a cached prefix of
     # U[1024, 16384] tokens (seed 6) and appends a chunk of 1024 new tokens
+    "long_causal_fp8_d128": dict(kind="dense_fp8", B=2, H=32, Hkv=32, N=8192, d=128,
+                                 causal=True),
     "paged_prefill_gqa_d128": dict(kind="paged_prefill", batch=8, H=32, Hkv=8, d=128,
                                    block_size=16, prefix_lo=1024, prefix_hi=16384, chunk=1024),
 }
@@ -126,6 +128,100 @@ def dense_inputs(B, N, H, Hkv, d, seed=0, outlier_frac=0.0, outlier_scale=8.0,
                 rows[(b, g)] = idx
                 k[b, idx, g, :] = scale_bf16_bits_pow2(k[b, idx, g, :], outlier_scale)
     return DenseInputs(B, N, H, Hkv, d, q, k, v, rows)
+
+
+# ---------------------------------------------------------------- e4m3 inputs
+# OCP FP8 E4M3 ("fn" variant): 1 sign, 4 exponent (bias 7), 3 mantissa bits;
+# no infinities, codes 0x7f / 0xff are NaN, largest finite 448.
+E4M3_MAX = 448.0
+
+
+def e4m3_values() -> np.ndarray:
+    """The real value of each of the 256 codes (float64; NaN for 0x7f, 0xff)."""
+    c = np.arange(256)
+    e = (c >> 3) & 15
+    m = (c & 7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    val = np.where(c >= 128, -mag, mag)
+    val[(c & 0x7f) == 0x7f] = np.nan
+    return val
+
+
+def e4m3_encode(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest e4m3 code (ties to the even code, the sign kept
+    on zero), saturating at +-448.  The input is taken as float32.  Normal
+    range (|x| >= 2^-6): the float32 mantissa is rounded to 3 bits (ties to
+    even) and the exponent rebiased from 127 to 7; below it the value is a
+    multiple of the subnormal step 2^-9."""
+    xf = np.asarray(x, dtype=np.float32)
+    a = np.minimum(np.abs(xf), np.float32(E4M3_MAX))
+    bits = a.view(np.uint32)
+    r = (bits + np.uint32(0x7FFFF) + ((bits >> np.uint32(20)) & np.uint32(1))) >> np.uint32(20)
+    # r = 8 * biased float32 exponent + 3 mantissa bits; rebias 127 -> 7
+    code = np.where(a >= np.float32(2.0 ** -6), r - np.uint32(120 << 3),
+                    np.rint(a * np.float32(512.0)).astype(np.uint32)).astype(np.uint8)
+    return np.where(np.signbit(xf), code | np.uint8(0x80), code)
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    return e4m3_values()[np.asarray(codes, dtype=np.int64)]
+
+
+@dataclass
+class Fp8Inputs:
+    B: int
+    N: int
+    H: int
+    Hkv: int
+    d: int
+    q: np.ndarray   # uint8 e4m3 codes [B, N, H, d]
+    k: np.ndarray   # [B, N, Hkv, d]
+    v: np.ndarray   # [B, N, Hkv, d]
+    q_descale: float
+    k_descale: float
+    v_descale: float
+    scale: float | None = None   # softmax scale; None means 1/sqrt(d)
+
+    def real(self, name: str) -> np.ndarray:
+        """Dequantised float64 values code * descale of q, k or v."""
+        return e4m3_decode(getattr(self, name)) * getattr(self, name + "_descale")
+
+
+def fp8_inputs(B, N, H, Hkv, d, seed=0) -> Fp8Inputs:
+    """N(0, 1) draws (the bf16 recipe's streams 0, 1, 2) quantised per tensor:
+    descale = amax / 448 rounded up to a power of two, code = e4m3(x / descale)."""
+    out = {}
+    for name, shape, stream in (("q", (B, N, H, d), 0), ("k", (B, N, Hkv, d), 1),
+                                ("v", (B, N, Hkv, d), 2)):
+        x = bf16_bits_to_f32(normal_bf16_bits(shape, seed, stream)).reshape(-1)
+        amax = float(np.abs(x).max()) if x.size else 1.0
+        ds = 2.0 ** math.ceil(math.log2(max(amax, 1e-30) / E4M3_MAX))
+        inv = np.float32(1.0 / ds)    # a power of two: x * inv is exact
+        codes = np.empty(x.shape, dtype=np.uint8)
+        for c0 in range(0, x.size, CHUNK):
+            codes[c0:c0 + CHUNK] = e4m3_encode(x[c0:c0 + CHUNK] * inv)
+        out[name] = (codes.reshape(shape), ds)
+    return Fp8Inputs(B, N, H, Hkv, d, out["q"][0], out["k"][0], out["v"][0],
+                     out["q"][1], out["k"][1], out["v"][1])
+
+
+def fp8_exact_p_inputs(B, N, H, Hkv, d, seed=0, q_nnz=4) -> Fp8Inputs:
+    """Inputs whose softmax weights are powers of two, exact in e4m3: each
+    query row has ``q_nnz`` entries of +-1 (descale 1/2), keys are -1, 0, +1
+    (descale 2) and the softmax scale is ln 2, so every base-2 score
+    q.k * scale * log2(e) is an integer in [-q_nnz, q_nnz].  Values are
+    integers in [-8, 8] (exact in e4m3) with descale 1/4."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 7]))
+    one, m_one = 0x38, 0xB8
+    q = np.zeros((B, N, H, d), dtype=np.uint8)
+    if B * N * H:
+        pos = np.argsort(rng.random((B, N, H, d)), axis=-1)[..., :q_nnz]
+        sign = rng.integers(0, 2, size=pos.shape)
+        np.put_along_axis(q, pos, np.where(sign == 1, one, m_one).astype(np.uint8), axis=-1)
+    kc = rng.integers(-1, 2, size=(B, N, Hkv, d))
+    k = np.select([kc == 1, kc == -1], [one, m_one], 0).astype(np.uint8)
+    v = e4m3_encode(rng.integers(-8, 9, size=(B, N, Hkv, d)).astype(np.float64))
+    return Fp8Inputs(B, N, H, Hkv, d, q, k, v, 0.5, 2.0, 0.25, scale=math.log(2.0))
 
 
 def varlen_lengths(num_seqs=32, lo=64, hi=4096, seed=2) -> np.ndarray:

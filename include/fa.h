@@ -100,6 +100,21 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float 
                   fa_stream_t stream);
 
 /*
+ * Dense prefill with FP8 (e4m3) inputs on the kind::f8f6f4 tensor-core path
+ * ("S12 FlashAttention", Production notes: the Hopper generation of the
+ * method adds FP8 support).  q, k, v hold e4m3 codes (one byte each) in the
+ * layouts of fa_fwd; the real values are code * q_descale, code * k_descale,
+ * code * v_descale (per-tensor, finite, > 0).  The softmax weights P are
+ * rounded to e4m3 for the P V product, so the output error is bounded by
+ * about 2^-4 times the attention-weighted mean of |v| (see the tests).
+ *   out : [B, N, H, d] bf16;  lse : [B, H, N] fp32, may be NULL
+ * Supported: d == 128.
+ */
+int fa_fwd_fp8(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
+               int Hkv, int N, int d, float scale, float q_descale, float k_descale,
+               float v_descale, int causal, fa_stream_t stream);
+
+/*
  * Dense prefill with the key tiles of every query tile split over several
  * CTAs, for batches whose B * H * ceil(N / 256) work items cannot fill the
  * GPU (long single sequences).  "S12 FlashAttention", "What this unlocks

@@ -62,3 +62,38 @@ def test_counters():
     assert W.varlen_flops([10, 20], 2, 64, False) == 4.0 * (100 + 400) * 64 * 2
     ctx = np.array([16, 17])
     assert W.decode_bytes(ctx, 4, 2, 128, 2) == 33 * 2 * 128 * 4 + 2 * 4 * 128 * 4 + 2 * 4 * 4 + 8 + 3 * 4
+
+
+def test_e4m3_table_matches_format():
+    """OCP E4M3: 1.0 is 0x38, the largest finite value 448 (0x7e), the
+    smallest subnormal 2^-9 (0x01), 0x7f / 0xff NaN, sign in bit 7."""
+    t = W.e4m3_values()
+    assert t[0x38] == 1.0 and t[0xB8] == -1.0
+    assert t[0x7e] == 448.0 and np.nanmax(t) == 448.0
+    assert t[0x01] == 2.0 ** -9 and t[0x08] == 2.0 ** -6
+    assert np.isnan(t[0x7f]) and np.isnan(t[0xff])
+    assert np.all(np.diff(t[:0x7f]) > 0)
+    assert np.array_equal(t[0x80:0xff], -t[:0x7f])
+
+
+def test_e4m3_encode_matches_torch():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("no float8_e4m3fn in this torch")
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal(100000) * np.exp2(rng.uniform(-12, 8.7, 100000))
+    x = x[np.abs(x) <= 448.0].astype(np.float32)   # torch does not saturate
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(W.e4m3_encode(x), ref)
+    # ties go to the even code: 1 + 1/16 lies halfway between 1 and 1.125
+    assert W.e4m3_encode(np.array([1.0625, 1.1875]))[0] == 0x38
+    assert W.e4m3_encode(np.array([1.1875]))[0] == 0x3A
+    assert W.e4m3_encode(np.array([1e6, -1e6])).tolist() == [0x7e, 0xfe]
+
+
+def test_fp8_exact_inputs_give_integer_scores():
+    inp = W.fp8_exact_p_inputs(1, 64, 2, 1, 128, seed=1)
+    q, k = inp.real("q")[0], inp.real("k")[0]
+    s2 = np.einsum("nhd,mhd->hnm", q, np.repeat(k, 2, axis=1)) * inp.scale / np.log(2.0)
+    assert np.allclose(s2, np.round(s2), atol=1e-12) and np.abs(s2).max() <= 4
+    assert inp.v_descale == 0.25 and np.all(np.abs(W.e4m3_decode(inp.v)) <= 8)
