@@ -559,16 +559,19 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         for (int c = 0; c < 128; ++c)
           if (c >= nvis) sr[c] = 0xff800000u;  // -inf
       }
-      float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
-      float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+      // four independent three-input max chains over the 128 scores
+      auto f = [&](int c) { return __uint_as_float(sr[c]); };
+      float mx0 = f(0), mx1 = f(1), mx2 = f(2), mx3 = f(3);
 #pragma unroll
-      for (int c = 4; c < 128; c += 4) {
-        mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
-        mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
-        mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
-        mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
+      for (int c = 4; c < 124; c += 8) {
+        mx0 = fmax3(mx0, f(c), f(c + 1));
+        mx1 = fmax3(mx1, f(c + 2), f(c + 3));
+        mx2 = fmax3(mx2, f(c + 4), f(c + 5));
+        mx3 = fmax3(mx3, f(c + 6), f(c + 7));
       }
-      const float m_new = fmaxf(m_ref, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
+      mx0 = fmax3(mx0, f(124), f(125));
+      mx1 = fmax3(mx1, f(126), f(127));
+      const float m_new = fmaxf(m_ref, fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2);
       // false while nothing visible has been seen (both -inf)
       const bool grow = m_new > m_ref + kRescaleLog2;
       float alpha = 1.f;
@@ -603,8 +606,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             pk[c + 1] = pack_bf16x2(p1.x, p1.y);
             re0 = fadd2(re0, p0);
             re1 = fadd2(re1, p1);
-            rs0 = fadd2(rs0, bf16x2_to_float2(pk[c]));
-            rs1 = fadd2(rs1, bf16x2_to_float2(pk[c + 1]));
+            add_bf16x2_to(rs0, pk[c]);
+            add_bf16x2_to(rs1, pk[c + 1]);
           }
           tmem_st32(tS + half * 32, pk);
         }

@@ -421,6 +421,24 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   return r;
 }
 
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 onwards).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// acc.x += low bf16 of v, acc.y += high bf16 of v, each widened exactly and
+// added in fp32 (mixed-precision add.f32.bf16, sm_100 onwards).
+__device__ __forceinline__ void add_bf16x2_to(float2 &acc, uint32_t v) {
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\t"
+      "add.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(acc.x), "+f"(acc.y)
+      : "r"(v));
+}
+
 // Exact widening of a bf16x2 pair (low half first).
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t v) {
   return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
