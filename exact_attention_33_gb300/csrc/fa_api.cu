@@ -23,8 +23,8 @@ namespace fa {
 __device__ unsigned int g_status = 0;
 
 cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                           const CUtensorMap &tv1, const PrefillParams &p, int d, bool causal,
-                           int kind, int grid, cudaStream_t stream);
+                           const CUtensorMap &tv1, const CUtensorMap &to, const PrefillParams &p,
+                           int d, bool causal, int kind, int grid, cudaStream_t stream);
 cudaError_t launch_prefill_split_combine(const PrefillParams &p, int d, cudaStream_t stream);
 cudaError_t launch_prefill_fp8(const CUtensorMap &tq, const CUtensorMap &tk,
                                const CUtensorMap &tv, const PrefillParams &p, bool causal,
@@ -268,10 +268,11 @@ int fa_fwd(const void *q, const void *k, const void *v, void *out, float *lse, i
   if (grid > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(N) * H * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
 
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   int rc = make_map(&tq, q, d, H, N, B, kPrefillBM);
   if (rc == FA_OK) rc = make_map(&tk, k, d, Hkv, N, B, kPrefillBN);
   if (rc == FA_OK) rc = make_map(&tv, v, d, Hkv, N, B, kPrefillBN);
+  if (rc == FA_OK) rc = make_map(&to, out, d, H, N, B, kPrefillBM);
   if (rc != FA_OK) return rc;
 
   PrefillParams p{};
@@ -291,7 +292,7 @@ int fa_fwd(const void *q, const void *k, const void *v, void *out, float *lse, i
   p.scale_log2 = scale * kLog2e;
   p.v_descale = 1.f;
   p.causal = causal;
-  cudaError_t e = launch_prefill(tq, tk, tv, tv, p, d, causal != 0, kKindDense,
+  cudaError_t e = launch_prefill(tq, tk, tv, tv, to, p, d, causal != 0, kKindDense,
                                  static_cast<int>(grid), reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -315,10 +316,11 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float 
   if (grid > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(total_tokens) * H * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
 
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   int rc = make_map(&tq, q, d, H, total_tokens, 1, kPrefillBM);
   if (rc == FA_OK) rc = make_map(&tk, k, d, Hkv, total_tokens, 1, kPrefillBN);
   if (rc == FA_OK) rc = make_map(&tv, v, d, Hkv, total_tokens, 1, kPrefillBN);
+  if (rc == FA_OK) rc = make_map(&to, out, d, H, total_tokens, 1, kPrefillBM);
   if (rc != FA_OK) return rc;
 
   PrefillParams p{};
@@ -338,7 +340,7 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float 
   p.scale_log2 = scale * kLog2e;
   p.v_descale = 1.f;
   p.causal = causal;
-  cudaError_t e = launch_prefill(tq, tk, tv, tv, p, d, causal != 0, kKindVarlen,
+  cudaError_t e = launch_prefill(tq, tk, tv, tv, to, p, d, causal != 0, kKindVarlen,
                                  static_cast<int>(grid), reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -413,10 +415,11 @@ int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *out, float
   if (grid > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(N) * H * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
 
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   int rc = make_map(&tq, q, d, H, N, B, kPrefillBM);
   if (rc == FA_OK) rc = make_map(&tk, k, d, Hkv, N, B, kPrefillBN);
   if (rc == FA_OK) rc = make_map(&tv, v, d, Hkv, N, B, kPrefillBN);
+  if (rc == FA_OK) rc = make_map(&to, out, d, H, N, B, kPrefillBM);
   if (rc != FA_OK) return rc;
 
   PrefillParams p{};
@@ -438,7 +441,7 @@ int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *out, float
   p.o_part = static_cast<float *>(workspace);
   p.ml_part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + w.o_bytes);
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_prefill(tq, tk, tv, tv, p, d, causal != 0, kKindDenseSplit,
+  cudaError_t e = launch_prefill(tq, tk, tv, tv, to, p, d, causal != 0, kKindDenseSplit,
                                  static_cast<int>(grid), st);
   if (e == cudaSuccess) e = launch_prefill_split_combine(p, d, st);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -473,9 +476,10 @@ int fa_fwd_paged(const void *q, const void *k_pool, const void *v_pool,
   if (grid > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(total_q) * H * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
 
-  CUtensorMap tq, tk, tv, tv1;
+  CUtensorMap tq, tk, tv, tv1, to;
   const long long tokens = static_cast<long long>(num_blocks) * block_size;
   int rc = make_map(&tq, q, d, H, total_q, 1, kPrefillBM);
+  if (rc == FA_OK) rc = make_map(&to, out, d, H, total_q, 1, kPrefillBM);
   if (rc == FA_OK) rc = make_pool_map(&tk, k_pool, d, Hkv, tokens);
   if (rc == FA_OK) rc = make_pool_map(&tv, v_pool, d, Hkv, tokens);
   if (rc == FA_OK) rc = make_pool_map(&tv1, v_pool, d, Hkv, tokens, 1);
@@ -503,7 +507,7 @@ int fa_fwd_paged(const void *q, const void *k_pool, const void *v_pool,
   p.max_blocks_per_seq = max_blocks_per_seq;
   p.max_ctx_len = max_ctx_len;
   p.num_blocks = num_blocks;
-  cudaError_t e = launch_prefill(tq, tk, tv, tv1, p, d, causal != 0, kKindPaged,
+  cudaError_t e = launch_prefill(tq, tk, tv, tv1, to, p, d, causal != 0, kKindPaged,
                                  static_cast<int>(grid), reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

@@ -105,7 +105,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v,
-                   const __grid_constant__ CUtensorMap tm_v1, const PrefillParams p) {
+                   const __grid_constant__ CUtensorMap tm_v1,
+                   const __grid_constant__ CUtensorMap tm_o, const PrefillParams p) {
   using L = PrefillLayout<D, FP8>;
   constexpr int SK = L::kStagesK;
   constexpr int SV = L::kStagesV;
@@ -700,6 +701,48 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         tc_fence_after();
         const bool live = qi < len;
         const float inv_l = (l > 0.f) ? p.v_descale / l : 0.f;
+        // A whole bf16 tile goes out through shared memory and one TMA store
+        // per 64-column chunk (rows past the end of a dense sequence are
+        // clipped by the tensor bounds).  The warpgroup's Q tile is free: its
+        // last S MMA completed before the last S tile was handed over.  A
+        // partial tile of a packed layout, whose tail rows belong to the next
+        // sequence, is written row by row instead.
+        const bool tma_out =
+            !FP8 && (KIND == kKindDense || row0 + (i + 1) * kPrefillBM <= len);
+        if (tma_out) {
+          uint8_t *stile = sQ + i * L::kTileBytes;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32_wait(tO + c * 32, o);
+            uint8_t *srow = stile + (c >> 1) * L::kChunkBytes + row * 128;
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(o[v4 * 8 + 0]) * inv_l,
+                                __uint_as_float(o[v4 * 8 + 1]) * inv_l);
+              w.y = pack_bf16x2(__uint_as_float(o[v4 * 8 + 2]) * inv_l,
+                                __uint_as_float(o[v4 * 8 + 3]) * inv_l);
+              w.z = pack_bf16x2(__uint_as_float(o[v4 * 8 + 4]) * inv_l,
+                                __uint_as_float(o[v4 * 8 + 5]) * inv_l);
+              w.w = pack_bf16x2(__uint_as_float(o[v4 * 8 + 6]) * inv_l,
+                                __uint_as_float(o[v4 * 8 + 7]) * inv_l);
+              // 128-byte swizzle: 16-byte unit u of row r sits at u ^ (r % 8)
+              const int u = ((c & 1) * 4 + v4) ^ (row & 7);
+              *reinterpret_cast<uint4 *>(srow + u * 16) = w;
+            }
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1 + i, 128);
+          if (row == 0) {
+            const int orow = (KIND == kKindDense ? 0 : seq_start) + row0 + i * kPrefillBM;
+#pragma unroll
+            for (int c = 0; c < L::kChunks; ++c)
+              tma_store_4d(&tm_o, stile + c * L::kChunkBytes, c * L::kChunkElems, h, orow, b);
+            tma_store_commit();
+            tma_store_wait_read();
+          }
+        }
         size_t out_row;
         if (KIND != kKindDense)
           out_row = static_cast<size_t>(seq_start + qi);
@@ -708,7 +751,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) +
                                                ((out_row * p.H + h) * D) * 2);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; !tma_out && c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32_wait(tO + c * 32, o);
           if (live) {
@@ -811,51 +854,53 @@ cudaError_t launch_prefill_split_combine(const PrefillParams &p, int d, cudaStre
 template <int D, bool CAUSAL, int KIND, bool FP8 = false>
 static cudaError_t launch_prefill_t(const CUtensorMap &tq, const CUtensorMap &tk,
                                     const CUtensorMap &tv, const CUtensorMap &tv1,
-                                    const PrefillParams &p, int grid, cudaStream_t stream) {
+                                    const CUtensorMap &to, const PrefillParams &p, int grid,
+                                    cudaStream_t stream) {
   using L = PrefillLayout<D, FP8>;
   auto kern = prefill_kernel<D, CAUSAL, KIND, FP8>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kPrefillThreads, L::kSmemAlloc, stream>>>(tq, tk, tv, tv1, p);
+  kern<<<grid, kPrefillThreads, L::kSmemAlloc, stream>>>(tq, tk, tv, tv1, to, p);
   return cudaGetLastError();
 }
 
 template <int D, int KIND>
 static cudaError_t launch_prefill_k(const CUtensorMap &tq, const CUtensorMap &tk,
                                     const CUtensorMap &tv, const CUtensorMap &tv1,
-                                    const PrefillParams &p, bool causal, int grid,
-                                    cudaStream_t stream) {
-  return causal ? launch_prefill_t<D, true, KIND>(tq, tk, tv, tv1, p, grid, stream)
-                : launch_prefill_t<D, false, KIND>(tq, tk, tv, tv1, p, grid, stream);
+                                    const CUtensorMap &to, const PrefillParams &p, bool causal,
+                                    int grid, cudaStream_t stream) {
+  return causal ? launch_prefill_t<D, true, KIND>(tq, tk, tv, tv1, to, p, grid, stream)
+                : launch_prefill_t<D, false, KIND>(tq, tk, tv, tv1, to, p, grid, stream);
 }
 
 cudaError_t launch_prefill_fp8(const CUtensorMap &tq, const CUtensorMap &tk,
                                const CUtensorMap &tv, const PrefillParams &p, bool causal,
                                int grid, cudaStream_t stream) {
-  return causal ? launch_prefill_t<128, true, kKindDense, true>(tq, tk, tv, tv, p, grid, stream)
-                : launch_prefill_t<128, false, kKindDense, true>(tq, tk, tv, tv, p, grid, stream);
+  return causal
+             ? launch_prefill_t<128, true, kKindDense, true>(tq, tk, tv, tv, tq, p, grid, stream)
+             : launch_prefill_t<128, false, kKindDense, true>(tq, tk, tv, tv, tq, p, grid, stream);
 }
 
 cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                           const CUtensorMap &tv1, const PrefillParams &p, int d, bool causal,
-                           int kind, int grid, cudaStream_t stream) {
+                           const CUtensorMap &tv1, const CUtensorMap &to, const PrefillParams &p,
+                           int d, bool causal, int kind, int grid, cudaStream_t stream) {
   if (d == 64) {
     if (kind == kKindDense)
-      return launch_prefill_k<64, kKindDense>(tq, tk, tv, tv1, p, causal, grid, stream);
+      return launch_prefill_k<64, kKindDense>(tq, tk, tv, tv1, to, p, causal, grid, stream);
     if (kind == kKindVarlen)
-      return launch_prefill_k<64, kKindVarlen>(tq, tk, tv, tv1, p, causal, grid, stream);
+      return launch_prefill_k<64, kKindVarlen>(tq, tk, tv, tv1, to, p, causal, grid, stream);
     if (kind == kKindDenseSplit)
-      return launch_prefill_k<64, kKindDenseSplit>(tq, tk, tv, tv1, p, causal, grid, stream);
-    return launch_prefill_k<64, kKindPaged>(tq, tk, tv, tv1, p, causal, grid, stream);
+      return launch_prefill_k<64, kKindDenseSplit>(tq, tk, tv, tv1, to, p, causal, grid, stream);
+    return launch_prefill_k<64, kKindPaged>(tq, tk, tv, tv1, to, p, causal, grid, stream);
   }
   if (kind == kKindDense)
-    return launch_prefill_k<128, kKindDense>(tq, tk, tv, tv1, p, causal, grid, stream);
+    return launch_prefill_k<128, kKindDense>(tq, tk, tv, tv1, to, p, causal, grid, stream);
   if (kind == kKindVarlen)
-    return launch_prefill_k<128, kKindVarlen>(tq, tk, tv, tv1, p, causal, grid, stream);
+    return launch_prefill_k<128, kKindVarlen>(tq, tk, tv, tv1, to, p, causal, grid, stream);
   if (kind == kKindDenseSplit)
-    return launch_prefill_k<128, kKindDenseSplit>(tq, tk, tv, tv1, p, causal, grid, stream);
-  return launch_prefill_k<128, kKindPaged>(tq, tk, tv, tv1, p, causal, grid, stream);
+    return launch_prefill_k<128, kKindDenseSplit>(tq, tk, tv, tv1, to, p, causal, grid, stream);
+  return launch_prefill_k<128, kKindPaged>(tq, tk, tv, tv1, to, p, causal, grid, stream);
 }
 
 }  // namespace fa
