@@ -219,7 +219,16 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  if (threadIdx.x == 0) {
+  uint8_t *sQ = smem + L::kQ;
+  uint8_t *sK = smem + L::kK;
+  uint8_t *sV = smem + L::kV;
+  const int kvh = h / p.group;
+  // Dense kinds: K(0) is copied with Q, before the block-wide set-up ends.
+  const bool k0_early = (KIND != kKindPaged) && n_kv > 0;
+
+  if (warp == 9 && lane == 0) {
+    // The producer thread initialises the barriers and starts the Q copies
+    // (and K(0)) right away; the other warps wait for it at __syncthreads.
     mbar_init(q_full, 1);
     for (int s = 0; s < SK; ++s) {
       mbar_init(&k_full[s], 1);
@@ -238,6 +247,26 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    if (KIND == kKindPaged) tma_prefetch_desc(&tm_v1);
+    const int nq = live1 ? 2 : 1;
+    mbar_arrive_expect_tx(q_full, nq * L::kTileBytes);
+    for (int i = 0; i < nq; ++i) {
+      const int qrow = seq_start + row0 + i * kPrefillBM;
+#pragma unroll
+      for (int c = 0; c < L::kChunks; ++c)
+        tma_load_4d(sQ + i * L::kTileBytes + c * L::kChunkBytes, &tm_q, q_full,
+                    c * L::kChunkElems, h, qrow, b);
+    }
+    if (k0_early) {
+      mbar_arrive_expect_tx(&k_full[0], L::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < L::kChunks; ++c)
+        tma_load_4d(sK + c * L::kChunkBytes, &tm_k, &k_full[0], c * L::kChunkElems, kvh,
+                    seq_start + kv0 * kPrefillBN, b);
+    }
   }
   if (warp == 8) {
     tmem_alloc(tmem_slot, L::kTmemCols);
@@ -256,11 +285,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  uint8_t *sQ = smem + L::kQ;
-  uint8_t *sK = smem + L::kK;
-  uint8_t *sV = smem + L::kV;
-  const int kvh = h / p.group;
-
   if (warp == 9 && KIND == kKindPaged) {
     // ------------------------------------------------------ TMA producer, paged
     // The warp runs converged: lanes 0..7 look up the 8 physical blocks of a
@@ -269,40 +293,47 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     // the status word records the error).  In the last block only the slots
     // inside the context are copied (one-row boxes for V), so stale slots of
     // the pool never reach shared memory.
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      tma_prefetch_desc(&tm_v1);
-      const int nq = live1 ? 2 : 1;
-      mbar_arrive_expect_tx(q_full, nq * L::kTileBytes);
-      for (int i = 0; i < nq; ++i) {
-        const int qrow = seq_start + row0 + i * kPrefillBM;
-#pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_4d(sQ + i * L::kTileBytes + c * L::kChunkBytes, &tm_q, q_full, c * L::kChunkElems, h,
-                      qrow, b);
-      }
-    }
-    __syncwarp();
     const int32_t *trow = p.block_table + static_cast<size_t>(unit) * p.max_blocks_per_seq;
     constexpr int kBlkPerTile = kPrefillBN / kDecodeBlock;
     constexpr uint32_t kRowBytes = 128 * L::kChunks;  // one key row, all chunks
     const int total_blk = (kv_len + kDecodeBlock - 1) / kDecodeBlock;
     int k_issued = 0, v_issued = 0;
-    // physical block of slot `lane` of tile j (or -1), and its valid rows
-    auto lookup = [&](int j, int &rows) -> int {
-      const int blk = (kv0 + j) * kBlkPerTile + lane;
-      rows = 0;
-      if (lane >= kBlkPerTile || blk >= total_blk) return -1;
+    // The block table is read ahead: one coalesced load brings the 32 block
+    // ids of 4 consecutive key tiles (lane = 8 * tile + slot), fetched 4
+    // tiles before they are needed, so no copy waits on a table lookup.
+    // Ids of tiles outside this CTA's range, or past the context, are -1;
+    // an id outside the pool is reported and not loaded.
+    auto fetch = [&](int w) -> int {
+      const int blk = (kv0 + w) * kBlkPerTile + lane;
+      if (w + lane / kBlkPerTile >= n_kv || blk >= total_blk) return -1;
       const int phys = trow[blk];
       if (phys < 0 || phys >= p.num_blocks) {
         raise_status(p.status, FA_DEV_BAD_BLOCK);
         return -1;
       }
+      return phys;
+    };
+    constexpr int kWin = 32 / kBlkPerTile;
+    int win_cur = fetch(0), win_nxt = fetch(kWin), win_base = 0;
+    // physical block of slot `lane` of tile j (or -1), and its valid rows;
+    // tiles are looked up in increasing order
+    auto lookup = [&](int j, int &rows) -> int {
+      if (j >= win_base + kWin) {
+        win_base += kWin;
+        win_cur = win_nxt;
+        win_nxt = fetch(win_base + kWin);
+      }
+      const int phys = __shfl_sync(0xffffffffu, win_cur, ((j - win_base) * kBlkPerTile + lane) & 31);
+      const int blk = (kv0 + j) * kBlkPerTile + lane;
+      rows = 0;
+      if (lane >= kBlkPerTile || phys < 0) return -1;
       rows = min(kDecodeBlock, kv_len - blk * kDecodeBlock);
       return phys;
     };
+    // One copy per (block, 64-column chunk); the lanes issue them together
+    // (lane = slot * kChunks + chunk), after lane 0 has posted the byte count.
+    constexpr int kCopyLanes = kBlkPerTile * L::kChunks;
+    const int my_t = lane / L::kChunks, my_c = lane % L::kChunks;
     auto load_k = [&](int j) -> bool {
       const int sk = j % SK;
       if (j >= SK && !mbar_wait_warp(&k_empty[sk], ((j / SK) - 1) & 1, abort_flag, p.status))
@@ -312,15 +343,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       const uint32_t bytes =
           __reduce_add_sync(0xffffffffu, phys >= 0 ? kDecodeBlock * kRowBytes : 0u);
       if (lane == 0) mbar_arrive_expect_tx(&k_full[sk], bytes);
-      for (int t = 0; t < kBlkPerTile; ++t) {
-        const int pb = __shfl_sync(0xffffffffu, phys, t);
-        if (lane == 0 && pb >= 0) {
-#pragma unroll
-          for (int c = 0; c < L::kChunks; ++c)
-            tma_load_3d(sK + sk * L::kTileBytes + c * L::kChunkBytes + t * kDecodeBlock * 128,
-                        &tm_k, &k_full[sk], c * L::kChunkElems, kvh, pb * kDecodeBlock);
-        }
-      }
+      __syncwarp();
+      const int pb = __shfl_sync(0xffffffffu, phys, my_t & 7);
+      if (lane < kCopyLanes && pb >= 0)
+        tma_load_3d(sK + sk * L::kTileBytes + my_c * L::kChunkBytes + my_t * kDecodeBlock * 128,
+                    &tm_k, &k_full[sk], my_c * L::kChunkElems, kvh, pb * kDecodeBlock);
       k_issued = j + 1;
       return true;
     };
@@ -333,24 +360,26 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       const uint32_t bytes =
           __reduce_add_sync(0xffffffffu, phys >= 0 ? static_cast<uint32_t>(rows) * kRowBytes : 0u);
       if (lane == 0) mbar_arrive_expect_tx(&v_full[sv], bytes);
-      for (int t = 0; t < kBlkPerTile; ++t) {
-        const int pb = __shfl_sync(0xffffffffu, phys, t);
-        const int nr = __shfl_sync(0xffffffffu, rows, t);
-        if (lane == 0 && pb >= 0) {
-          uint8_t *dst = sV + sv * L::kTileBytes + t * kDecodeBlock * 128;
-          if (nr == kDecodeBlock) {
-#pragma unroll
-            for (int c = 0; c < L::kChunks; ++c)
-              tma_load_3d(dst + c * L::kChunkBytes, &tm_v, &v_full[sv], c * L::kChunkElems, kvh,
-                          pb * kDecodeBlock);
-          } else {
-            for (int r = 0; r < nr; ++r)
-#pragma unroll
-              for (int c = 0; c < L::kChunks; ++c)
-                tma_load_3d(dst + c * L::kChunkBytes + r * 128, &tm_v1, &v_full[sv], c * L::kChunkElems, kvh,
-                            pb * kDecodeBlock + r);
-          }
-        }
+      __syncwarp();
+      uint8_t *stage = sV + sv * L::kTileBytes;
+      // whole blocks
+      const int pb = __shfl_sync(0xffffffffu, phys, my_t & 7);
+      const int nr = __shfl_sync(0xffffffffu, rows, my_t & 7);
+      if (lane < kCopyLanes && pb >= 0 && nr == kDecodeBlock)
+        tma_load_3d(stage + my_c * L::kChunkBytes + my_t * kDecodeBlock * 128, &tm_v, &v_full[sv],
+                    my_c * L::kChunkElems, kvh, pb * kDecodeBlock);
+      // the block holding the end of the context: only its rows inside the
+      // context, one row per copy (lane = row * kChunks + chunk)
+      const unsigned part =
+          __ballot_sync(0xffffffffu, lane < kBlkPerTile && phys >= 0 && rows < kDecodeBlock);
+      if (part != 0u) {
+        const int tp = __ffs(part) - 1;
+        const int pbp = __shfl_sync(0xffffffffu, phys, tp);
+        const int nrp = __shfl_sync(0xffffffffu, rows, tp);
+        const int rr = lane / L::kChunks;
+        if (rr < nrp)
+          tma_load_3d(stage + my_c * L::kChunkBytes + (tp * kDecodeBlock + rr) * 128, &tm_v1,
+                      &v_full[sv], my_c * L::kChunkElems, kvh, pbp * kDecodeBlock + rr);
       }
       v_issued = j + 1;
       return true;
@@ -371,21 +400,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      const int nq = live1 ? 2 : 1;
-      mbar_arrive_expect_tx(q_full, nq * L::kTileBytes);
-      for (int i = 0; i < nq; ++i) {
-        const int qrow = seq_start + row0 + i * kPrefillBM;
-#pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_4d(sQ + i * L::kTileBytes + c * L::kChunkBytes, &tm_q, q_full, c * L::kChunkElems, h,
-                      qrow, b);
-      }
-      // Issue order K(0), then V(j), K(j+1) for every j: a V load never waits
-      // behind a K stage that frees later.
-      int k_issued = 0, v_issued = 0;
+      // Issue order K(0) (already issued with Q), then V(j), K(j+1) for
+      // every j: a V load never waits behind a K stage that frees later.
+      int k_issued = k0_early ? 1 : 0, v_issued = 0;
       auto load_k = [&](int j) -> bool {
         const int sk = j % SK;
         if (j >= SK && !mbar_wait(&k_empty[sk], ((j / SK) - 1) & 1, abort_flag, p.status))
@@ -410,7 +427,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         v_issued = j + 1;
         return true;
       };
-      if (n_kv > 0 && load_k(0)) {
+      if (n_kv > 0 && (k0_early || load_k(0))) {
         for (int j = 0; j < n_kv; ++j) {
           if (!load_v(j)) break;
           if (j + 1 < n_kv && !load_k(j + 1)) break;
