@@ -467,3 +467,77 @@ ALL_PINS = [
     pin_default_scale, pin_recurrence, pin_paged, pin_flash_decoding,
     pin_nan_guard, pin_fully_masked_row, pin_dense_layout, pin_paged_prefill,
 ]
+
+
+# ------------------------------------------------------------ backward pass
+# Pins for ``oracle.attention_grad``.  Each takes the forward oracle (for
+# attention_one) and the gradient oracle (for attention_backward_one); the
+# finite differences use only the forward definition.
+
+def _loss(fwd, q, k, v, do, scale, causal):
+    o, _ = fwd.attention_one(q, k, v, scale=scale, causal=causal)
+    return float((o * do).sum())
+
+
+def pin_backward_finite_differences(fwd, bwd):
+    """Central differences of <O, dO> w.r.t. every input element agree with
+    the analytic gradient (GQA, causal with Nq < Nk, and non-causal)."""
+    rng = np.random.default_rng(41)
+    eps = 1e-6
+    for nq, nk, h, hkv, causal in ((5, 5, 2, 1, True), (3, 6, 2, 2, True), (4, 4, 3, 1, False)):
+        q, k, v = rand(rng, nq, h, 3), rand(rng, nk, hkv, 3), rand(rng, nk, hkv, 3)
+        do = rand(rng, nq, h, 3)
+        scale = 0.7
+        dq, dk, dv = bwd.attention_backward_one(q, k, v, do, scale=scale, causal=causal)
+        for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+            num = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += eps
+                xm[idx] -= eps
+                args = {"q": q, "k": k, "v": v}
+                args[name] = xp
+                lp = _loss(fwd, args["q"], args["k"], args["v"], do, scale, causal)
+                args[name] = xm
+                lm = _loss(fwd, args["q"], args["k"], args["v"], do, scale, causal)
+                num[idx] = (lp - lm) / (2 * eps)
+            np.testing.assert_allclose(g, num, rtol=1e-6, atol=1e-8, err_msg=f"d{name}")
+
+
+def pin_backward_invariants(fwd, bwd):
+    """Rows of P sum to 1, so the value gradients of a KV head add up to the
+    upstream gradients of its query heads; without a mask, moving every key
+    by one vector leaves the softmax unchanged, so the key gradients sum to
+    zero.  The gradient is linear in dO."""
+    rng = np.random.default_rng(43)
+    q, k, v = rand(rng, 7, 4, 5), rand(rng, 9, 2, 5), rand(rng, 9, 2, 5)
+    do = rand(rng, 7, 4, 5)
+    for causal in (False, True):
+        dq, dk, dv = bwd.attention_backward_one(q, k, v, do, causal=causal)
+        for g in range(2):
+            np.testing.assert_allclose(dv[:, g].sum(axis=0), do[:, 2 * g:2 * g + 2].sum(axis=(0, 1)),
+                                       atol=1e-12)
+        if not causal:
+            np.testing.assert_allclose(dk.sum(axis=0), 0.0, atol=1e-12)
+        dq2, dk2, dv2 = bwd.attention_backward_one(q, k, v, 3.0 * do, causal=causal)
+        np.testing.assert_allclose(dq2, 3.0 * dq, atol=1e-12)
+        np.testing.assert_allclose(dk2, 3.0 * dk, atol=1e-12)
+    # a single visible key: O = v_0, so dV_0 = dO and dQ = dK = 0
+    dq, dk, dv = bwd.attention_backward_one(q[:1], k[:1], v[:1], do[:1], causal=True)
+    np.testing.assert_allclose(dv[0], do[0].reshape(2, 2, 5).sum(axis=1), atol=1e-12)
+    np.testing.assert_allclose(dq, 0.0, atol=1e-12)
+    np.testing.assert_allclose(dk, 0.0, atol=1e-12)
+
+
+def pin_backward_dense_layout(fwd, bwd):
+    rng = np.random.default_rng(47)
+    q, k, v, do = rand(rng, 2, 6, 2, 3), rand(rng, 2, 6, 1, 3), rand(rng, 2, 6, 1, 3), rand(rng, 2, 6, 2, 3)
+    dq, dk, dv = bwd.attention_backward_dense(q, k, v, do, causal=True)
+    for b in range(2):
+        r = bwd.attention_backward_one(q[b], k[b], v[b], do[b], causal=True)
+        for x, y in zip((dq[b], dk[b], dv[b]), r):
+            np.testing.assert_allclose(x, y, atol=0)
+
+
+BACKWARD_PINS = [pin_backward_finite_differences, pin_backward_invariants,
+                 pin_backward_dense_layout]

@@ -114,3 +114,60 @@ def test_helper_mistake_is_caught(monkeypatch, name, fn):
 def test_unmutated_oracle_passes_all_pins():
     for pin in ALL_PINS:
         pin(ora_mod)
+
+
+# ------------------------------------------------------------ backward pass
+import oracle.attention_grad as grad_mod  # noqa: E402
+from oracle_pins import BACKWARD_PINS  # noqa: E402
+
+
+def mutant_backward_one(mistake):
+    def attention_backward_one(q, k, v, do, scale=None, causal=False):
+        q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
+        nq, h_q, d = q.shape
+        nk, h_kv, _ = k.shape
+        if scale is None:
+            scale = 1.0 / math.sqrt(d)
+        group = h_q // h_kv
+        dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+        if causal:
+            visible = np.arange(nk)[None, :] <= np.arange(nq)[:, None] + (nk - nq)
+        else:
+            visible = np.ones((nq, nk), dtype=bool)
+        for h in range(h_q):
+            g = h // group
+            s = np.where(visible, scale * (q[:, h] @ k[:, g].T), -np.inf)
+            m = s.max(axis=1)
+            e = np.exp(s - m[:, None])
+            p = e / e.sum(axis=1)[:, None]
+            o = p @ v[:, g]
+            if mistake == "dv_no_transpose":
+                dv[:, g] += (p @ do[:, h])[:nk] if nq >= nk else np.pad(p @ do[:, h], ((0, nk - nq), (0, 0)))
+            else:
+                dv[:, g] += p.T @ do[:, h]
+            dp = do[:, h] @ v[:, g].T
+            d_row = 0.0 if mistake == "no_d_term" else (do[:, h] * o).sum(axis=1)[:, None]
+            ds = p * (dp - d_row)
+            sc = 1.0 if mistake == "dq_no_scale" else scale
+            dq[:, h] = sc * (ds @ k[:, g])
+            if mistake == "dk_overwrite_group":
+                dk[:, g] = scale * (ds.T @ q[:, h])
+            elif mistake == "dk_sign":
+                dk[:, g] -= scale * (ds.T @ q[:, h])
+            else:
+                dk[:, g] += scale * (ds.T @ q[:, h])
+        return dq, dk, dv
+    return attention_backward_one
+
+
+@pytest.mark.parametrize("mistake", ["dv_no_transpose", "no_d_term", "dq_no_scale",
+                                     "dk_overwrite_group", "dk_sign"])
+def test_backward_mistake_is_caught(monkeypatch, mistake):
+    monkeypatch.setattr(grad_mod, "attention_backward_one", mutant_backward_one(mistake))
+    failures = 0
+    for pin in BACKWARD_PINS:
+        try:
+            pin(ora_mod, grad_mod)
+        except (AssertionError, ValueError, IndexError):
+            failures += 1
+    assert failures > 0
