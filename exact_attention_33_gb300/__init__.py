@@ -21,6 +21,7 @@ import threading
 __all__ = [
     "FaError", "library_path", "load_library", "fa_fwd", "fa_fwd_varlen", "fa_fwd_paged",
     "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_fwd_fp8",
+    "fa_bwd", "fa_bwd_workspace_size",
     "fa_decode_paged", "fa_decode_paged_noalloc", "fa_decode_workspace_size",
     "fa_status_string", "fa_device_status",
     "fa_version", "FA_DEV_TIMEOUT", "FA_DEV_BAD_BLOCK", "FA_DEV_BAD_CTX", "FA_DEV_BAD_SEQLEN",
@@ -68,6 +69,10 @@ def load_library() -> ctypes.CDLL:
         lib.fa_fwd_varlen.restype = i
         lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, f, f, f, i, vp]
         lib.fa_fwd_fp8.restype = i
+        lib.fa_bwd_workspace_size.argtypes = [i, i, i]
+        lib.fa_bwd_workspace_size.restype = sz
+        lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
+        lib.fa_bwd.restype = i
         lib.fa_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i]
         lib.fa_fwd_splitkv_workspace_size.restype = sz
         lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
@@ -178,6 +183,39 @@ def fa_fwd(q, k, v, causal=False, scale=None, out=None, lse=None, want_lse=True,
     if rc != FA_OK:
         raise FaError("fa_fwd", rc)
     return out, lse
+
+
+def fa_bwd_workspace_size(B, H, N) -> int:
+    return int(load_library().fa_bwd_workspace_size(B, H, N))
+
+
+def fa_bwd(q, k, v, out, lse, dout, causal=False, scale=None, dq=None, dk=None, dv=None,
+           workspace=None, stream=None):
+    """Gradient of dense attention.  q, out, dout [B,N,H,d]; k, v [B,N,Hkv,d]
+    bf16 CUDA tensors; lse [B,H,N] fp32 from fa_fwd.  Returns (dq, dk, dv)."""
+    torch = _torch()
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
+        _check_bf16_cuda(name, t, 4)
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    if k.shape != (B, N, Hkv, d) or v.shape != k.shape or out.shape != q.shape \
+            or dout.shape != q.shape:
+        raise ValueError("shapes must be q/out/dout [B,N,H,d], k/v [B,N,Hkv,d]")
+    if not lse.is_cuda or lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be a [B,H,N] fp32 CUDA tensor")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = fa_bwd_workspace_size(B, H, N)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    rc = load_library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                               _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, N, d, _scale(scale, d),
+                               1 if causal else 0, _ptr(workspace), workspace.numel(),
+                               _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError("fa_bwd", rc)
+    return dq, dk, dv
 
 
 def fa_fwd_fp8(q, k, v, q_descale, k_descale, v_descale, causal=False, scale=None, out=None,

@@ -18,7 +18,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfa.so")
-SOURCES = ["fa_api.cu", "prefill.cu", "decode.cu"]
+SOURCES = ["fa_api.cu", "prefill.cu", "decode.cu", "backward.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

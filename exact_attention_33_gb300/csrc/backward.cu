@@ -1,0 +1,555 @@
+// backward.cu - gradient of exact attention (dQ, dK, dV) for sm_103a.
+//
+// The pages describe the forward streaming softmax only; the backward pass
+// is the chain rule through the same definition, O = softmax(scale Q K^T) V:
+//   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),  D = rowsum(dO * O),
+//   dQ = scale dS K,  dK = scale dS^T Q,
+// with P recomputed tile by tile from Q, K and the forward log-sum-exp, so
+// neither P nor S ever reaches HBM (the same IO argument as the forward).
+//
+// Three kernels:
+//   bwd_preprocess   D and the log-sum-exp in log2 units, per (b, h, row).
+//   bwd_dq           one CTA per (b, h, 128-row query tile); streams the
+//                    key tiles: S = Q K^T and dP = dO V^T (tcgen05, TMEM),
+//                    dS in registers, dQ += dS K (A = dS from TMEM).
+//   bwd_dkdv         one CTA per (b, kv head, 128-key tile); streams the
+//                    query tiles of every query head of the group:
+//                    S^T = K Q^T and dP^T = V dO^T, then dV += P^T dO and
+//                    dK += dS^T Q (A from TMEM), so the group's sum stays in
+//                    TMEM and no atomics are needed.
+// Roles per CTA: warps 0-3 elementwise (thread = TMEM lane = row), warp 4
+// issues the MMAs (converged, elect.sync), warp 5 is the TMA producer.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+
+namespace {
+
+constexpr float kLog2eF = 1.4426950408889634f;
+
+template <int D>
+struct BwdLayout {
+  static constexpr int kChunkBytes = 128 * 128;  // 128 rows x one 128-byte swizzle row
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTileBytes = kChunks * kChunkBytes;
+  static constexpr int kStages = 2;
+  // dq kernel: Q, dO, then K and V rings.  dkdv kernel: K, V, then Q and dO
+  // rings plus the per-stage log-sum-exp and D vectors (128 floats each).
+  static constexpr int kA = 0;                          // Q (dq) / K (dkdv)
+  static constexpr int kB = kA + kTileBytes;            // dO (dq) / V (dkdv)
+  static constexpr int kR0 = kB + kTileBytes;           // ring of tile pairs
+  static constexpr int kVec = kR0 + 2 * kStages * kTileBytes;
+  static constexpr int kBar = kVec + kStages * 2 * 512;
+  static constexpr int kNumBars = 2 + 2 * kStages + 4;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kSmemAlloc = kBytes + 1024;
+};
+
+// S-like MMA (both operands K-major over d): D[tmem] = A[128 x d] B[128 x d]^T
+template <int D>
+__device__ __forceinline__ void mma_tile_ss(uint32_t d_t, uint32_t a_base, uint32_t b_base) {
+  using L = BwdLayout<D>;
+  constexpr uint32_t kIdesc = idesc_bf16_f32(128, 128, false, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
+    mma_ss_elect(d_t, sdesc_sw128(a_base + off, 16, 1024), sdesc_sw128(b_base + off, 16, 1024),
+                 kIdesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O-like MMA: D[tmem, 128 x d] (+)= A[tmem, 128 x 128 bf16] B[128 x d]
+// with B a [rows x d] tile read MN-major (the contraction runs over rows).
+template <int D>
+__device__ __forceinline__ void mma_tile_ts(uint32_t d_t, uint32_t a_t, uint32_t b_base,
+                                            bool acc) {
+  using L = BwdLayout<D>;
+  constexpr uint32_t kIdesc = idesc_bf16_f32(128, D, false, true);
+#pragma unroll
+  for (int kk = 0; kk < 128 / 16; ++kk)
+    mma_ts_elect(d_t, a_t + kk * 8, sdesc_sw128(b_base + kk * 16 * 128, L::kChunkBytes, 1024),
+                 kIdesc, (acc || kk > 0) ? 1u : 0u);
+}
+
+// Converts a row of 128 fp32 TMEM columns into 64 columns of bf16 pairs is
+// done chunk by chunk in the callers; this packs 32 values.
+__device__ __forceinline__ void store_row_scaled_bf16(void *dst_row, const uint32_t (&o)[32],
+                                                      float mul) {
+  uint4 *dst = reinterpret_cast<uint4 *>(dst_row);
+#pragma unroll
+  for (int v4 = 0; v4 < 4; ++v4) {
+    uint4 w;
+    w.x = pack_bf16x2(__uint_as_float(o[v4 * 8 + 0]) * mul, __uint_as_float(o[v4 * 8 + 1]) * mul);
+    w.y = pack_bf16x2(__uint_as_float(o[v4 * 8 + 2]) * mul, __uint_as_float(o[v4 * 8 + 3]) * mul);
+    w.z = pack_bf16x2(__uint_as_float(o[v4 * 8 + 4]) * mul, __uint_as_float(o[v4 * 8 + 5]) * mul);
+    w.w = pack_bf16x2(__uint_as_float(o[v4 * 8 + 6]) * mul, __uint_as_float(o[v4 * 8 + 7]) * mul);
+    dst[v4] = w;
+  }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ preprocess
+// One warp per (b, row, h): D = sum_c dO * O (fp32 from bf16) and the forward
+// log-sum-exp in log2 units (+inf for rows past N or rows without a visible
+// key, so that every weight recomputed from it is 0).
+template <int D>
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) {
+  const int lane = threadIdx.x & 31;
+  const long long gw = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const long long total = static_cast<long long>(p.B) * p.Npad * p.H;
+  if (gw >= total) return;
+  const int h = static_cast<int>(gw % p.H);
+  const long long bn = gw / p.H;
+  const int row = static_cast<int>(bn % p.Npad);
+  const int b = static_cast<int>(bn / p.Npad);
+  const size_t vec = (static_cast<size_t>(b) * p.H + h) * p.Npad + row;
+  if (row >= p.N) {
+    if (lane == 0) {
+      p.lse2[vec] = CUDART_INF_F;
+      p.dsum[vec] = 0.f;
+    }
+    return;
+  }
+  constexpr int E = D / 32;  // bf16 values per lane
+  const size_t off = ((static_cast<size_t>(b) * p.N + row) * p.H + h) * D + lane * E;
+  const uint16_t *o = static_cast<const uint16_t *>(p.out) + off;
+  const uint16_t *g = static_cast<const uint16_t *>(p.dout) + off;
+  float acc = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; e += 2) {
+    const float2 a = bf16x2_to_float2(*reinterpret_cast<const uint32_t *>(o + e));
+    const float2 c = bf16x2_to_float2(*reinterpret_cast<const uint32_t *>(g + e));
+    acc = fmaf(a.x, c.x, acc);
+    acc = fmaf(a.y, c.y, acc);
+  }
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (lane == 0) {
+    const float l = p.lse[(static_cast<size_t>(b) * p.H + h) * p.N + row];
+    p.lse2[vec] = (l == -CUDART_INF_F) ? CUDART_INF_F : l * kLog2eF;
+    p.dsum[vec] = acc;
+  }
+}
+
+// ------------------------------------------------------------------------- dQ
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const BwdParams p) {
+  using L = BwdLayout<D>;
+  constexpr int ST = L::kStages;
+  // heaviest query tiles first (causal), heads fastest
+  const int h = static_cast<int>(blockIdx.x % p.H);
+  const int rest = static_cast<int>(blockIdx.x / p.H);
+  const int t_rank = rest % p.n_tiles;
+  const int b = rest / p.n_tiles;
+  const int t = CAUSAL ? (p.n_tiles - 1 - t_rank) : t_rank;
+  const int kvh = h / p.group;
+  const int n_kv = CAUSAL ? (t + 1) : p.n_tiles;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBar);
+  uint64_t *in_full = bars;        // Q and dO
+  uint64_t *kv_full = bars + 1;    // [ST]
+  uint64_t *kv_empty = kv_full + ST;
+  uint64_t *s_full = kv_empty + ST;
+  uint64_t *p_full = s_full + 1;
+  uint64_t *dq_done = p_full + 1;
+  uint64_t *drain = dq_done + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
+  uint8_t *sQ = smem + L::kA;
+  uint8_t *sDO = smem + L::kB;
+  uint8_t *sR = smem + L::kR0;  // stage s: K at 2s, V at 2s + 1
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp == 5 && lane == 0) {
+    mbar_init(in_full, 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(dq_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 4) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 5) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(in_full, 2 * L::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < L::kChunks; ++c) {
+        tma_load_4d(sQ + c * L::kChunkBytes, &tm_q, in_full, c * 64, h, t * 128, b);
+        tma_load_4d(sDO + c * L::kChunkBytes, &tm_do, in_full, c * 64, h, t * 128, b);
+      }
+      int issued = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        const int s = j % ST;
+        if (j >= ST && !mbar_wait(&kv_empty[s], ((j / ST) - 1) & 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&kv_full[s], 2 * L::kTileBytes);
+        uint8_t *sk = sR + (2 * s) * L::kTileBytes;
+        uint8_t *sv = sk + L::kTileBytes;
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c) {
+          tma_load_4d(sk + c * L::kChunkBytes, &tm_k, &kv_full[s], c * 64, kvh, j * 128, b);
+          tma_load_4d(sv + c * L::kChunkBytes, &tm_v, &kv_full[s], c * 64, kvh, j * 128, b);
+        }
+        issued = j + 1;
+      }
+      mbar_drain(in_full, 0, p.status);
+      for (int j = max(0, issued - ST); j < issued; ++j)
+        mbar_drain(&kv_full[j % ST], (j / ST) & 1, p.status);
+    }
+  } else if (warp == 4) {
+    // ------------------------------------------------------------ MMA issuer
+    // Per key tile j: S = Q K_j^T into TMEM [0,128), dP = dO V_j^T into
+    // [128,256); after the elementwise warps wrote dS (bf16) over S:
+    // dQ += dS K_j into [256, 256 + d).  S of the next tile is issued after
+    // dQ(j) by this thread, so dS is read before it is overwritten.
+    const uint32_t q_base = smem_u32(sQ), do_base = smem_u32(sDO);
+    bool ok = mbar_wait_warp(in_full, 0, abort_flag, p.status);
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const int s = j % ST;
+      const uint32_t k_base = smem_u32(sR + (2 * s) * L::kTileBytes);
+      const uint32_t v_base = k_base + L::kTileBytes;
+      if (!mbar_wait_warp(&kv_full[s], (j / ST) & 1, abort_flag, p.status)) break;
+      tc_fence_after();
+      mma_tile_ss<D>(tmem, q_base, k_base);
+      mma_tile_ss<D>(tmem + 128, do_base, v_base);
+      mma_commit_elect(s_full);
+      if (!mbar_wait_warp(p_full, j & 1, abort_flag, p.status)) break;
+      tc_fence_after();
+      mma_tile_ts<D>(tmem + 256, tmem, k_base, j > 0);
+      mma_commit_elect(&kv_empty[s]);
+    }
+    mma_commit_elect(dq_done);
+    mma_commit_elect(drain);
+    mbar_drain(drain, 0, p.status);
+  } else {
+    // ------------------------------------------------------------ elementwise
+    const int row = warp * 32 + lane;
+    const int qi = t * 128 + row;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tS = tmem + lane_off, tP = tmem + 128 + lane_off, tQ = tmem + 256 + lane_off;
+    const size_t vec = (static_cast<size_t>(b) * p.H + h) * p.Npad + min(qi, p.Npad - 1);
+    const float lse2 = p.lse2[vec];
+    const float dsum = p.dsum[vec];
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      ok = mbar_wait(s_full, j & 1, abort_flag, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      // keys [0, nvis) of this tile are visible to the row
+      const int nvis = min(128, (CAUSAL ? min(p.N, qi + 1) : p.N) - j * 128);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sv[32], dp[32], pk[16];
+        tmem_ld32_wait(tS + c * 32, sv);
+        tmem_ld32_wait(tP + c * 32, dp);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float2 w;
+          w.x = (c * 32 + e < nvis) ? ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse2)) : 0.f;
+          w.y = (c * 32 + e + 1 < nvis) ? ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -lse2)) : 0.f;
+          const float d0 = w.x * (__uint_as_float(dp[e]) - dsum);
+          const float d1 = w.y * (__uint_as_float(dp[e + 1]) - dsum);
+          pk[e >> 1] = pack_bf16x2(d0, d1);
+        }
+        tmem_st16(tS + c * 16, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok) {
+      ok = mbar_wait(dq_done, 0, abort_flag, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      uint16_t *dst = static_cast<uint16_t *>(p.dq) +
+                      ((static_cast<size_t>(b) * p.N + qi) * p.H + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32_wait(tQ + c * 32, o);
+        if (qi < p.N) store_row_scaled_bf16(dst + c * 32, o, p.scale);
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ----------------------------------------------------------------------- dK dV
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const BwdParams p) {
+  using L = BwdLayout<D>;
+  constexpr int ST = L::kStages;
+  // heaviest key tiles first (causal: tile 0 sees every query tile)
+  const int kvh = static_cast<int>(blockIdx.x % p.Hkv);
+  const int rest = static_cast<int>(blockIdx.x / p.Hkv);
+  const int jt = rest % p.n_tiles;
+  const int b = rest / p.n_tiles;
+  const int i0 = CAUSAL ? jt : 0;  // first query tile that sees a key of this tile
+  const int n_it = (p.n_tiles - i0) * p.group;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBar);
+  uint64_t *in_full = bars;          // K and V of this key tile
+  uint64_t *qd_full = bars + 1;      // [ST] Q, dO, lse2, D
+  uint64_t *qd_empty = qd_full + ST;
+  uint64_t *s_full = qd_empty + ST;
+  uint64_t *p_full = s_full + 1;
+  uint64_t *kv_done = p_full + 1;
+  uint64_t *drain = kv_done + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
+  uint8_t *sK = smem + L::kA;
+  uint8_t *sV = smem + L::kB;
+  uint8_t *sR = smem + L::kR0;  // stage s: Q at 2s, dO at 2s + 1
+  float *sVec = reinterpret_cast<float *>(smem + L::kVec);  // stage s: lse2 at 256s, D at 256s+128
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp == 5 && lane == 0) {
+    mbar_init(in_full, 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&qd_full[s], 1);
+      mbar_init(&qd_empty[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(kv_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 4) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 5) {
+    // ------------------------------------------------------------ producer
+    // Iteration it: query head kvh * group + it % group, query tile
+    // i0 + it / group.
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(in_full, 2 * L::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < L::kChunks; ++c) {
+        tma_load_4d(sK + c * L::kChunkBytes, &tm_k, in_full, c * 64, kvh, jt * 128, b);
+        tma_load_4d(sV + c * L::kChunkBytes, &tm_v, in_full, c * 64, kvh, jt * 128, b);
+      }
+      int issued = 0;
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it % ST;
+        if (it >= ST && !mbar_wait(&qd_empty[s], ((it / ST) - 1) & 1, abort_flag, p.status))
+          break;
+        const int hq = kvh * p.group + it % p.group;
+        const int i = i0 + it / p.group;
+        mbar_arrive_expect_tx(&qd_full[s], 2 * L::kTileBytes + 2 * 512);
+        uint8_t *sq = sR + (2 * s) * L::kTileBytes;
+        uint8_t *sd = sq + L::kTileBytes;
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c) {
+          tma_load_4d(sq + c * L::kChunkBytes, &tm_q, &qd_full[s], c * 64, hq, i * 128, b);
+          tma_load_4d(sd + c * L::kChunkBytes, &tm_do, &qd_full[s], c * 64, hq, i * 128, b);
+        }
+        const size_t vec = (static_cast<size_t>(b) * p.H + hq) * p.Npad + i * 128;
+        bulk_load(sVec + 256 * s, p.lse2 + vec, 512, &qd_full[s]);
+        bulk_load(sVec + 256 * s + 128, p.dsum + vec, 512, &qd_full[s]);
+        issued = it + 1;
+      }
+      mbar_drain(in_full, 0, p.status);
+      for (int it = max(0, issued - ST); it < issued; ++it)
+        mbar_drain(&qd_full[it % ST], (it / ST) & 1, p.status);
+    }
+  } else if (warp == 4) {
+    // ------------------------------------------------------------ MMA issuer
+    // S^T = K Q_i^T into TMEM [0,128), dP^T = V dO_i^T into [128,256); after
+    // the elementwise warps wrote P^T over S^T and dS^T over dP^T (bf16):
+    // dV += P^T dO_i into [256, 256 + d), dK += dS^T Q_i after it.
+    const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV);
+    bool ok = mbar_wait_warp(in_full, 0, abort_flag, p.status);
+    for (int it = 0; ok && it < n_it; ++it) {
+      const int s = it % ST;
+      const uint32_t q_base = smem_u32(sR + (2 * s) * L::kTileBytes);
+      const uint32_t do_base = q_base + L::kTileBytes;
+      if (!mbar_wait_warp(&qd_full[s], (it / ST) & 1, abort_flag, p.status)) break;
+      tc_fence_after();
+      mma_tile_ss<D>(tmem, k_base, q_base);
+      mma_tile_ss<D>(tmem + 128, v_base, do_base);
+      mma_commit_elect(s_full);
+      if (!mbar_wait_warp(p_full, it & 1, abort_flag, p.status)) break;
+      tc_fence_after();
+      mma_tile_ts<D>(tmem + 256, tmem, do_base, it > 0);
+      mma_tile_ts<D>(tmem + 256 + D, tmem + 128, q_base, it > 0);
+      mma_commit_elect(&qd_empty[s]);
+    }
+    mma_commit_elect(kv_done);
+    mma_commit_elect(drain);
+    mbar_drain(drain, 0, p.status);
+  } else {
+    // ------------------------------------------------------------ elementwise
+    const int row = warp * 32 + lane;   // key row of the tile
+    const int kj = jt * 128 + row;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tS = tmem + lane_off, tP = tmem + 128 + lane_off;
+    const uint32_t tV = tmem + 256 + lane_off, tK = tmem + 256 + D + lane_off;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it % ST;
+      const int i = i0 + it / p.group;
+      // the stage's vectors arrived with its tiles (async copies): observe
+      // that barrier too before reading them
+      ok = mbar_wait(&qd_full[s], (it / ST) & 1, abort_flag, p.status) &&
+           mbar_wait(s_full, it & 1, abort_flag, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const float *vl = sVec + 256 * s;  // log-sum-exp (log2 units) of the 128 queries
+      const float *vd = vl + 128;        // D of the 128 queries
+      // queries [qfirst, 128) of this tile see the key (causal); earlier
+      // ones do not.  Queries past N carry lse2 = +inf, so their weight is 0.
+      const int qfirst = CAUSAL ? max(0, kj - i * 128) : 0;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sv[32], dp[32], pp[16], pd[16];
+        tmem_ld32_wait(tS + c * 32, sv);
+        tmem_ld32_wait(tP + c * 32, dp);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int q0 = c * 32 + e;
+          const float w0 = (q0 >= qfirst) ? ex2(fmaf(__uint_as_float(sv[e]), sl2, -vl[q0])) : 0.f;
+          const float w1 =
+              (q0 + 1 >= qfirst) ? ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -vl[q0 + 1])) : 0.f;
+          pp[e >> 1] = pack_bf16x2(w0, w1);
+          pd[e >> 1] = pack_bf16x2(w0 * (__uint_as_float(dp[e]) - vd[q0]),
+                                   w1 * (__uint_as_float(dp[e + 1]) - vd[q0 + 1]));
+        }
+        tmem_st16(tS + c * 16, pp);
+        tmem_st16(tP + c * 16, pd);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok) {
+      ok = mbar_wait(kv_done, 0, abort_flag, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const size_t orow = ((static_cast<size_t>(b) * p.N + kj) * p.Hkv + kvh) * D;
+      uint16_t *dv = static_cast<uint16_t *>(p.dv) + orow;
+      uint16_t *dk = static_cast<uint16_t *>(p.dk) + orow;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32_wait(tV + c * 32, o);
+        if (kj < p.N) store_row_scaled_bf16(dv + c * 32, o, 1.f);
+      }
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32_wait(tK + c * 32, o);
+        if (kj < p.N) store_row_scaled_bf16(dk + c * 32, o, p.scale);
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------- launch
+
+template <int D>
+static cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tdo,
+                                const CUtensorMap &tk, const CUtensorMap &tv, const BwdParams &p,
+                                bool causal, cudaStream_t stream) {
+  using L = BwdLayout<D>;
+  const long long pre_warps = static_cast<long long>(p.B) * p.Npad * p.H;
+  bwd_preprocess_kernel<D><<<static_cast<unsigned>((pre_warps + 7) / 8), 256, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  auto dq = causal ? bwd_dq_kernel<D, true> : bwd_dq_kernel<D, false>;
+  auto dkdv = causal ? bwd_dkdv_kernel<D, true> : bwd_dkdv_kernel<D, false>;
+  e = cudaFuncSetAttribute(dq, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(dkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
+  if (e != cudaSuccess) return e;
+  const unsigned grid_kv = static_cast<unsigned>(p.B * p.Hkv * p.n_tiles);
+  dkdv<<<grid_kv, kBwdThreads, L::kSmemAlloc, stream>>>(tq, tdo, tk, tv, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const unsigned grid_q = static_cast<unsigned>(p.B * p.H * p.n_tiles);
+  dq<<<grid_q, kBwdThreads, L::kSmemAlloc, stream>>>(tq, tdo, tk, tv, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUtensorMap &tk,
+                       const CUtensorMap &tv, const BwdParams &p, int d, bool causal,
+                       cudaStream_t stream) {
+  return d == 64 ? launch_bwd_d<64>(tq, tdo, tk, tv, p, causal, stream)
+                 : launch_bwd_d<128>(tq, tdo, tk, tv, p, causal, stream);
+}
+
+}  // namespace fa

@@ -26,6 +26,9 @@ cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const C
                            const CUtensorMap &tv1, const CUtensorMap &to, const PrefillParams &p,
                            int d, bool causal, int kind, int grid, cudaStream_t stream);
 cudaError_t launch_prefill_split_combine(const PrefillParams &p, int d, cudaStream_t stream);
+cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUtensorMap &tk,
+                       const CUtensorMap &tv, const BwdParams &p, int d, bool causal,
+                       cudaStream_t stream);
 cudaError_t launch_prefill_fp8(const CUtensorMap &tq, const CUtensorMap &tk,
                                const CUtensorMap &tv, const PrefillParams &p, bool causal,
                                int grid, cudaStream_t stream);
@@ -385,6 +388,64 @@ int fa_fwd_fp8(const void *q, const void *k, const void *v, void *out, float *ls
   p.causal = causal;
   cudaError_t e = launch_prefill_fp8(tq, tk, tv, p, causal != 0, static_cast<int>(grid),
                                      reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N) {
+  if (B <= 0 || H <= 0 || N <= 0) return 0;
+  const size_t npad = (static_cast<size_t>(N) + 127) / 128 * 128;
+  return 2 * static_cast<size_t>(B) * H * npad * sizeof(float);
+}
+
+int fa_bwd(const void *q, const void *k, const void *v, const void *out, const float *lse,
+           const void *dout, void *dq, void *dk, void *dv, int B, int H, int Hkv, int N, int d,
+           float scale, int causal, void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+  if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  for (const void *ptr : {q, k, v, out, dout, static_cast<const void *>(dq),
+                          static_cast<const void *>(dk), static_cast<const void *>(dv)})
+    if (!aligned(ptr, 16)) return FA_ERR_INVALID_ARG;
+  if (!aligned(lse, 4)) return FA_ERR_INVALID_ARG;
+  if (B < 0 || N < 0 || H < 1 || Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (B == 0 || N == 0) return FA_OK;
+  const size_t need = fa_bwd_workspace_size(B, H, N);
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
+    return FA_ERR_WORKSPACE;
+  const long long n_tiles = (N + 127) / 128;
+  if (n_tiles * B * H > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(N) * H * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
+
+  CUtensorMap tq, tdo, tk, tv;
+  int rc = make_map(&tq, q, d, H, N, B, 128);
+  if (rc == FA_OK) rc = make_map(&tdo, dout, d, H, N, B, 128);
+  if (rc == FA_OK) rc = make_map(&tk, k, d, Hkv, N, B, 128);
+  if (rc == FA_OK) rc = make_map(&tv, v, d, Hkv, N, B, 128);
+  if (rc != FA_OK) return rc;
+
+  BwdParams p{};
+  p.status = status_ptr();
+  if (p.status == nullptr) return FA_ERR_CUDA;
+  p.out = out;
+  p.dout = dout;
+  p.lse = lse;
+  p.n_tiles = static_cast<int>(n_tiles);
+  p.Npad = p.n_tiles * 128;
+  p.lse2 = static_cast<float *>(workspace);
+  p.dsum = p.lse2 + static_cast<size_t>(B) * H * p.Npad;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.group = H / Hkv;
+  p.N = N;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  cudaError_t e = launch_bwd(tq, tdo, tk, tv, p, d, causal != 0,
+                             reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -54,6 +54,25 @@ struct PrefillParams {
   int num_blocks;
 };
 
+// ----------------------------------------------------------------- backward
+
+constexpr int kBwdThreads = 192;  // 4 elementwise warps + 1 MMA warp + 1 TMA warp
+
+struct BwdParams {
+  unsigned int *status;   // per-device sticky FA_DEV_* word
+  const void *out;        // forward output O, bf16 [B, N, H, d]
+  const void *dout;       // upstream gradient dO, bf16 [B, N, H, d]
+  const float *lse;       // forward log-sum-exp, fp32 [B, H, N] (natural log)
+  float *lse2;            // workspace: lse in log2 units, [B, H, Npad]
+  float *dsum;            // workspace: D = rowsum(dO * O), [B, H, Npad]
+  void *dq, *dk, *dv;     // bf16, layouts of q, k, v
+  int B, H, Hkv, group, N;
+  int Npad;               // N rounded up to 128
+  int n_tiles;            // Npad / 128
+  float scale;            // softmax scale
+  float scale_log2;       // scale * log2(e)
+};
+
 // ------------------------------------------------------------------- decode
 
 constexpr int kDecodeBlock = 16;     // tokens per KV block (paged pool granularity)

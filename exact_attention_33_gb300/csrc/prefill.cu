@@ -67,37 +67,6 @@ struct PrefillLayout {
   static constexpr int kTmemO = 256;
 };
 
-// Wait that ignores the abort flag (used only to drain in-flight copies
-// before the CTA exits); bounded by the same time limit.
-__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity, unsigned int *status) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      raise_status(status, FA_DEV_TIMEOUT);
-      return;
-    }
-  }
-}
-
-// Loads 32 TMEM columns and waits for them in one asm block, so that no use
-// of the registers can be scheduled before the data has arrived.
-__device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
-      "[%32];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-        "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-}
-
 // KIND: dense batch, packed varlen batch, or packed queries over a paged KV
 // cache (chunked prefill).
 template <int D, bool CAUSAL, int KIND, bool FP8 = false>

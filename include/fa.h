@@ -115,6 +115,31 @@ int fa_fwd_fp8(const void *q, const void *k, const void *v, void *out, float *ls
                float v_descale, int causal, fa_stream_t stream);
 
 /*
+ * Gradient of dense attention (backward pass): given the forward inputs, its
+ * output O and log-sum-exp, and the upstream gradient dO, writes
+ *   dV = P^T dO,  dQ = scale dS K,  dK = scale dS^T Q,
+ *   dS = P * (dO V^T - rowsum(dO * O)),  P = exp(scale Q K^T - lse)
+ * (masked entries 0), summed over the query heads of each KV head.  The pages
+ * describe only the forward streaming softmax ("S12 FlashAttention"); this
+ * is the chain rule through that definition, with P recomputed tile by tile
+ * from Q, K and the forward log-sum-exp instead of being stored.  No
+ * gradient flows through the log-sum-exp output.
+ *   q, out, dout, dq : [B, N, H, d] bf16     k, v, dk, dv : [B, N, Hkv, d] bf16
+ *   lse              : [B, H, N] fp32, as written by fa_fwd (same q, k, v,
+ *                      scale and causal flag)
+ *   workspace        : caller-owned device memory of at least
+ *                      fa_bwd_workspace_size(B, H, N) bytes, 256-byte aligned;
+ *                      overwritten (fp32 rowsums and rescaled lse)
+ * Supported: d in {64, 128}.  All buffers device memory; asynchronous on
+ * `stream`.  Errors as for fa_fwd; FA_ERR_WORKSPACE for a missing, small or
+ * misaligned workspace.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N);
+int fa_bwd(const void *q, const void *k, const void *v, const void *out, const float *lse,
+           const void *dout, void *dq, void *dk, void *dv, int B, int H, int Hkv, int N, int d,
+           float scale, int causal, void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * Dense prefill with the key tiles of every query tile split over several
  * CTAs, for batches whose B * H * ceil(N / 256) work items cannot fill the
  * GPU (long single sequences).  "S12 FlashAttention", "What this unlocks

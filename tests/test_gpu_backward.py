@@ -1,0 +1,108 @@
+"""GPU parity of the backward pass (fa_bwd) against the fp64 gradient oracle.
+
+The kernel takes the bf16 output and fp32 log-sum-exp of fa_fwd, recomputes
+the weights P in fp32, and rounds P and dS to bf16 for the tensor-core
+products (fp32 accumulation); D = rowsum(dO * O) is formed from the bf16 O;
+the three gradients are written in bf16.  Each of those roundings moves an
+element by at most 2^-9 of its size.  Five such steps, with independent
+errors, give a relative RMS error near 5 * 2^-9 / sqrt(3) = 5.6e-3 per
+gradient tensor; the test allows REL_RMS_MAX = 1.5e-2.  Element-wise, an
+error of a few of those roundings of the largest terms is allowed:
+|err| <= MAX_OVER_MAX * max|reference| (the scale of the gradient rows varies
+widely under a causal mask, so the tensor's RMS is not the reference here).
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from exact_attention_33_gb300 import workloads as W
+from gpu_helpers import assert_device_clean, dev_bf16, host_f64, torch_mod
+
+pytestmark = pytest.mark.gpu
+
+REL_RMS_MAX = 1.5e-2
+MAX_OVER_MAX = 2e-2
+
+
+@pytest.fixture(scope="module")
+def fa():
+    from exact_attention_33_gb300.build import build
+    build()
+    import exact_attention_33_gb300 as fa_mod
+    fa_mod.fa_device_status(clear=True)
+    return fa_mod
+
+
+def f64(bits):
+    return W.bf16_bits_to_f64(bits)
+
+
+def check_grad(name, got, ref, what):
+    err = got - ref
+    rms = math.sqrt(float(np.mean(ref ** 2))) if ref.size else 0.0
+    if rms < 1e-12:
+        # an exactly-zero gradient (a single visible key: dS = P (dP - D) with
+        # dP and D the same dot product summed in two orders) is met to
+        # fp32 reassociation error
+        assert float(np.abs(got).max()) <= 1e-4, f"{what} {name}: nonzero where the gradient is 0"
+        return 0.0
+    rel = math.sqrt(float(np.mean(err ** 2))) / rms
+    mx = float(np.abs(err).max()) / float(np.abs(ref).max())
+    assert np.all(np.isfinite(got)), f"{what} {name}: non-finite values"
+    assert rel <= REL_RMS_MAX, f"{what} {name}: relative RMS error {rel:.3e}"
+    assert mx <= MAX_OVER_MAX, f"{what} {name}: max error {mx:.3e} of the largest gradient"
+    return rel
+
+
+def run_case(fa, B, N, H, Hkv, d, causal, seed, scale=None):
+    torch = torch_mod()
+    inp = W.dense_inputs(B, N, H, Hkv, d, seed=seed)
+    do_bits = W.normal_bf16_bits((B, N, H, d), seed, 3)
+    q, k, v, do = dev_bf16(inp.q), dev_bf16(inp.k), dev_bf16(inp.v), dev_bf16(do_bits)
+    out, lse = fa.fa_fwd(q, k, v, causal=causal, scale=scale)
+    dq, dk, dv = fa.fa_bwd(q, k, v, out, lse, do, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    rq, rk, rv = oracle.attention_backward_dense(f64(inp.q), f64(inp.k), f64(inp.v), f64(do_bits),
+                                                 scale=scale, causal=causal)
+    what = f"B{B} N{N} H{H}/{Hkv} d{d} causal={causal}"
+    errs = [check_grad(n, host_f64(g), r, what) for n, g, r in
+            (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv))]
+    print(f"{what}: relative RMS errors dq {errs[0]:.2e} dk {errs[1]:.2e} dv {errs[2]:.2e}")
+    assert_device_clean()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,N,H,Hkv", [(1, 1, 2, 1), (1, 100, 2, 1), (2, 128, 2, 2),
+                                       (1, 300, 4, 2), (1, 777, 2, 1)])
+def test_backward_small(fa, d, causal, B, N, H, Hkv):
+    run_case(fa, B, N, H, Hkv, d, causal, seed=90 + N)
+
+
+def test_backward_medium(fa):
+    """Many tiles in both directions (16 query and 16 key tiles)."""
+    run_case(fa, 1, 2048, 2, 1, 128, True, seed=95)
+
+
+def test_backward_explicit_scale(fa):
+    run_case(fa, 1, 260, 2, 2, 64, False, seed=96, scale=0.3)
+
+
+def test_backward_deterministic_and_rejects(fa):
+    torch = torch_mod()
+    inp = W.dense_inputs(1, 500, 4, 2, 128, seed=97)
+    q, k, v = dev_bf16(inp.q), dev_bf16(inp.k), dev_bf16(inp.v)
+    do = dev_bf16(W.normal_bf16_bits((1, 500, 4, 128), 97, 3))
+    out, lse = fa.fa_fwd(q, k, v, causal=True)
+    a = fa.fa_bwd(q, k, v, out, lse, do, causal=True)
+    b = fa.fa_bwd(q, k, v, out, lse, do, causal=True)
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fa.FaError) as e:
+        fa.fa_bwd(q, k, v, out, lse, do, causal=True, workspace=small)
+    assert e.value.status == -4
+    assert_device_clean()
