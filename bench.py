@@ -367,6 +367,44 @@ def measure_fp8_prefill(torch, device, fa, steps, warmup, peak_bf16):
             "launches_per_call": 1}
 
 
+def measure_backward(torch, device, fa, steps, warmup, peak):
+    """Backward pass (fa_bwd: dQ, dK, dV) of the long-context causal prefill
+    (B=2, H=32, N=8192, d=128, the forward's own workload), timed with CUDA
+    events on its own.  Work: the five products of the gradient, 2.5 times
+    the forward count (5 * N^2 * d per (batch, head) causal); the kernels
+    recompute S and dP once more, which is not counted."""
+    cfg = W.WORKLOADS["long_causal_d128"]
+    B, N, H, d = cfg["B"], cfg["N"], cfg["H"], cfg["d"]
+    inp = W.dense_inputs(B, N, H, cfg["Hkv"], d, seed=0, outlier_frac=cfg["outlier_frac"],
+                         outlier_scale=cfg["outlier_scale"])
+    q, k, v = (to_dev(getattr(inp, n), torch, device) for n in ("q", "k", "v"))
+    do = to_dev(W.normal_bf16_bits((B, N, H, d), 0, 3), torch, device)
+    out, lse = fa.fa_fwd(q, k, v, causal=True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N), dtype=torch.uint8, device=device)
+    flops = 2.5 * W.prefill_flops(B, N, H, d, True)
+
+    def run():
+        fa.fa_bwd(q, k, v, out, lse, do, causal=True, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    tf = flops / (ms / 1e3) / 1e12
+    return {"workload": "backward of the long-context causal prefill: B2 H32 N8192 d128 "
+                        "(dQ, dK, dV from O, lse, dO)",
+            "ms": ms, "tflops": tf, "frac_of_peak": tf / peak, "flops": flops,
+            "launches_per_call": 3}
+
+
 LEG_ORDER = ("long", "varlen", "decode")
 LAUNCHES_PER_STEP = {"long": 1, "varlen": 1, "decode": 2}
 
@@ -562,6 +600,10 @@ def bench_ours(args, rank, world, local):
                                                  args.warmup, peaks0["bf16_tflops"])
         if fa.fa_device_status(clear=True) != 0:
             raise RuntimeError("device status word set during the fp8 prefill leg")
+        nxt["backward"] = measure_backward(torch, device, fa, min(args.steps, 20), args.warmup,
+                                           peaks0["bf16_tflops"])
+        if fa.fa_device_status(clear=True) != 0:
+            raise RuntimeError("device status word set during the backward leg")
 
     # ---- numbers (max over ranks of each time)
     K = args.steps

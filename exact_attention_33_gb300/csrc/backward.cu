@@ -46,7 +46,7 @@ struct BwdLayout {
   static constexpr int kR0 = kB + kTileBytes;           // ring of tile pairs
   static constexpr int kVec = kR0 + 2 * kStages * kTileBytes;
   static constexpr int kBar = kVec + kStages * 2 * 512;
-  static constexpr int kNumBars = 2 + 2 * kStages + 4;
+  static constexpr int kNumBars = 2 + 2 * kStages + 8;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kSmemAlloc = kBytes + 1024;
@@ -97,45 +97,46 @@ __device__ __forceinline__ void store_row_scaled_bf16(void *dst_row, const uint3
 }  // namespace
 
 // ------------------------------------------------------------------ preprocess
-// One warp per (b, row, h): D = sum_c dO * O (fp32 from bf16) and the forward
-// log-sum-exp in log2 units (+inf for rows past N or rows without a visible
-// key, so that every weight recomputed from it is 0).
+// D / 8 threads per (b, row, h), 16 bytes each: D = sum_c dO * O (fp32 from
+// bf16) and the forward log-sum-exp in log2 units (+inf for rows past N or
+// rows without a visible key, so that every weight recomputed from it is 0).
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) {
-  const int lane = threadIdx.x & 31;
-  const long long gw = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  constexpr int TPR = D / 8;  // threads per row
+  const int sub = threadIdx.x % TPR;
+  const long long gr = static_cast<long long>(blockIdx.x) * (256 / TPR) + threadIdx.x / TPR;
   const long long total = static_cast<long long>(p.B) * p.Npad * p.H;
-  if (gw >= total) return;
-  const int h = static_cast<int>(gw % p.H);
-  const long long bn = gw / p.H;
+  if (gr >= total) return;  // whole row groups leave together (TPR divides 32)
+  const int h = static_cast<int>(gr % p.H);
+  const long long bn = gr / p.H;
   const int row = static_cast<int>(bn % p.Npad);
   const int b = static_cast<int>(bn / p.Npad);
   const size_t vec = (static_cast<size_t>(b) * p.H + h) * p.Npad + row;
-  if (row >= p.N) {
-    if (lane == 0) {
+  float acc = 0.f;
+  if (row < p.N) {
+    const size_t off = ((static_cast<size_t>(b) * p.N + row) * p.H + h) * D + sub * 8;
+    const uint4 o = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.out) + off);
+    const uint4 g = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.dout) + off);
+    const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 a2 = bf16x2_to_float2(ow[e]);
+      const float2 c2 = bf16x2_to_float2(gw[e]);
+      acc = fmaf(a2.x, c2.x, acc);
+      acc = fmaf(a2.y, c2.y, acc);
+    }
+  }
+#pragma unroll
+  for (int sft = TPR / 2; sft > 0; sft >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sft);
+  if (sub == 0) {
+    if (row < p.N) {
+      const float l = p.lse[(static_cast<size_t>(b) * p.H + h) * p.N + row];
+      p.lse2[vec] = (l == -CUDART_INF_F) ? CUDART_INF_F : l * kLog2eF;
+      p.dsum[vec] = acc;
+    } else {
       p.lse2[vec] = CUDART_INF_F;
       p.dsum[vec] = 0.f;
     }
-    return;
-  }
-  constexpr int E = D / 32;  // bf16 values per lane
-  const size_t off = ((static_cast<size_t>(b) * p.N + row) * p.H + h) * D + lane * E;
-  const uint16_t *o = static_cast<const uint16_t *>(p.out) + off;
-  const uint16_t *g = static_cast<const uint16_t *>(p.dout) + off;
-  float acc = 0.f;
-#pragma unroll
-  for (int e = 0; e < E; e += 2) {
-    const float2 a = bf16x2_to_float2(*reinterpret_cast<const uint32_t *>(o + e));
-    const float2 c = bf16x2_to_float2(*reinterpret_cast<const uint32_t *>(g + e));
-    acc = fmaf(a.x, c.x, acc);
-    acc = fmaf(a.y, c.y, acc);
-  }
-#pragma unroll
-  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (lane == 0) {
-    const float l = p.lse[(static_cast<size_t>(b) * p.H + h) * p.N + row];
-    p.lse2[vec] = (l == -CUDART_INF_F) ? CUDART_INF_F : l * kLog2eF;
-    p.dsum[vec] = acc;
   }
 }
 
@@ -164,7 +165,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t *kv_full = bars + 1;    // [ST]
   uint64_t *kv_empty = kv_full + ST;
   uint64_t *s_full = kv_empty + ST;
-  uint64_t *p_full = s_full + 1;
+  uint64_t *s_read = s_full + 1;    // the elementwise warps have read S_j
+  uint64_t *dp_full = s_read + 1;
+  uint64_t *p_full = dp_full + 1;   // dS_j (bf16) is in TMEM
   uint64_t *dq_done = p_full + 1;
   uint64_t *drain = dq_done + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
@@ -182,6 +185,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&kv_empty[s], 1);
     }
     mbar_init(s_full, 1);
+    mbar_init(s_read, 128);
+    mbar_init(dp_full, 1);
     mbar_init(p_full, 128);
     mbar_init(dq_done, 1);
     mbar_init(drain, 1);
@@ -231,25 +236,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 4) {
     // ------------------------------------------------------------ MMA issuer
-    // Per key tile j: S = Q K_j^T into TMEM [0,128), dP = dO V_j^T into
-    // [128,256); after the elementwise warps wrote dS (bf16) over S:
-    // dQ += dS K_j into [256, 256 + d).  S of the next tile is issued after
-    // dQ(j) by this thread, so dS is read before it is overwritten.
+    // S lives in TMEM [0,128), dP in [128,256), dQ in [256, 256 + d).  Per
+    // key tile j: dP_j; then S_{j+1} as soon as the elementwise warps have
+    // read S_j (s_read), so it runs while they finish tile j; then
+    // dQ += dS_j K_j once dS_j (bf16, written over dP_j) is in TMEM.  dP_{j+1}
+    // is issued after dQ_j by this thread, so it overwrites dS_j only after
+    // dQ_j has read it.
     const uint32_t q_base = smem_u32(sQ), do_base = smem_u32(sDO);
-    bool ok = mbar_wait_warp(in_full, 0, abort_flag, p.status);
-    for (int j = 0; ok && j < n_kv; ++j) {
-      const int s = j % ST;
-      const uint32_t k_base = smem_u32(sR + (2 * s) * L::kTileBytes);
-      const uint32_t v_base = k_base + L::kTileBytes;
-      if (!mbar_wait_warp(&kv_full[s], (j / ST) & 1, abort_flag, p.status)) break;
+    auto k_at = [&](int j) { return smem_u32(sR + (2 * (j % ST)) * L::kTileBytes); };
+    bool ok = mbar_wait_warp(in_full, 0, abort_flag, p.status) &&
+              mbar_wait_warp(&kv_full[0], 0, abort_flag, p.status);
+    if (ok) {
       tc_fence_after();
-      mma_tile_ss<D>(tmem, q_base, k_base);
-      mma_tile_ss<D>(tmem + 128, do_base, v_base);
+      mma_tile_ss<D>(tmem, q_base, k_at(0));
       mma_commit_elect(s_full);
+    }
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const uint32_t k_base = k_at(j);
+      mma_tile_ss<D>(tmem + 128, do_base, k_base + L::kTileBytes);
+      mma_commit_elect(dp_full);
+      if (j + 1 < n_kv) {
+        ok = mbar_wait_warp(s_read, j & 1, abort_flag, p.status) &&
+             mbar_wait_warp(&kv_full[(j + 1) % ST], ((j + 1) / ST) & 1, abort_flag, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        mma_tile_ss<D>(tmem, q_base, k_at(j + 1));
+        mma_commit_elect(s_full);
+      }
       if (!mbar_wait_warp(p_full, j & 1, abort_flag, p.status)) break;
       tc_fence_after();
-      mma_tile_ts<D>(tmem + 256, tmem, k_base, j > 0);
-      mma_commit_elect(&kv_empty[s]);
+      mma_tile_ts<D>(tmem + 256, tmem + 128, k_base, j > 0);
+      mma_commit_elect(&kv_empty[j % ST]);
     }
     mma_commit_elect(dq_done);
     mma_commit_elect(drain);
@@ -272,21 +289,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       // keys [0, nvis) of this tile are visible to the row
       const int nvis = min(128, (CAUSAL ? min(p.N, qi + 1) : p.N) - j * 128);
+      // P = exp(S * scale - lse), kept as bf16 pairs (the values the dQ
+      // product uses through dS)
+      uint32_t pp[64];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t sv[32], dp[32], pk[16];
+        uint32_t sv[32];
         tmem_ld32_wait(tS + c * 32, sv);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float w0 = (c * 32 + e < nvis) ? ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse2)) : 0.f;
+          const float w1 =
+              (c * 32 + e + 1 < nvis) ? ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -lse2)) : 0.f;
+          pp[c * 16 + (e >> 1)] = pack_bf16x2(w0, w1);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(s_read);
+      ok = mbar_wait(dp_full, j & 1, abort_flag, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      // dS = P (dP - D), written over dP chunk by chunk (chunk c of dS lands
+      // in columns already read)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t dp[32], pk[16];
         tmem_ld32_wait(tP + c * 32, dp);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float2 w;
-          w.x = (c * 32 + e < nvis) ? ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse2)) : 0.f;
-          w.y = (c * 32 + e + 1 < nvis) ? ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -lse2)) : 0.f;
-          const float d0 = w.x * (__uint_as_float(dp[e]) - dsum);
-          const float d1 = w.y * (__uint_as_float(dp[e + 1]) - dsum);
-          pk[e >> 1] = pack_bf16x2(d0, d1);
+          const float2 w = bf16x2_to_float2(pp[c * 16 + (e >> 1)]);
+          pk[e >> 1] = pack_bf16x2(w.x * (__uint_as_float(dp[e]) - dsum),
+                                   w.y * (__uint_as_float(dp[e + 1]) - dsum));
         }
-        tmem_st16(tS + c * 16, pk);
+        tmem_st16(tP + c * 16, pk);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -342,7 +378,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t *qd_full = bars + 1;      // [ST] Q, dO, lse2, D
   uint64_t *qd_empty = qd_full + ST;
   uint64_t *s_full = qd_empty + ST;
-  uint64_t *p_full = s_full + 1;
+  uint64_t *dp_full = s_full + 1;
+  uint64_t *pt_full = dp_full + 1;  // P^T (bf16) is in TMEM
+  uint64_t *p_full = pt_full + 1;   // dS^T (bf16) is in TMEM
   uint64_t *kv_done = p_full + 1;
   uint64_t *drain = kv_done + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
@@ -361,6 +399,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&qd_empty[s], 1);
     }
     mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(pt_full, 128);
     mbar_init(p_full, 128);
     mbar_init(kv_done, 1);
     mbar_init(drain, 1);
@@ -418,25 +458,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 4) {
     // ------------------------------------------------------------ MMA issuer
-    // S^T = K Q_i^T into TMEM [0,128), dP^T = V dO_i^T into [128,256); after
-    // the elementwise warps wrote P^T over S^T and dS^T over dP^T (bf16):
-    // dV += P^T dO_i into [256, 256 + d), dK += dS^T Q_i after it.
+    // S^T lives in TMEM [0,128), dP^T in [128,256), dV and dK after them.
+    // Per iteration: dV += P^T dO once P^T (bf16, over S^T) is in TMEM; then
+    // S^T of the next iteration (issued after dV by this thread, so it
+    // overwrites P^T only after dV has read it); dK += dS^T Q once dS^T
+    // (over dP^T) is in TMEM; then dP^T of the next iteration.
     const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV);
-    bool ok = mbar_wait_warp(in_full, 0, abort_flag, p.status);
-    for (int it = 0; ok && it < n_it; ++it) {
-      const int s = it % ST;
-      const uint32_t q_base = smem_u32(sR + (2 * s) * L::kTileBytes);
-      const uint32_t do_base = q_base + L::kTileBytes;
-      if (!mbar_wait_warp(&qd_full[s], (it / ST) & 1, abort_flag, p.status)) break;
+    auto q_at = [&](int it) { return smem_u32(sR + (2 * (it % ST)) * L::kTileBytes); };
+    bool ok = mbar_wait_warp(in_full, 0, abort_flag, p.status) &&
+              mbar_wait_warp(&qd_full[0], 0, abort_flag, p.status);
+    if (ok) {
       tc_fence_after();
-      mma_tile_ss<D>(tmem, k_base, q_base);
-      mma_tile_ss<D>(tmem + 128, v_base, do_base);
+      mma_tile_ss<D>(tmem, k_base, q_at(0));
       mma_commit_elect(s_full);
+      mma_tile_ss<D>(tmem + 128, v_base, q_at(0) + L::kTileBytes);
+      mma_commit_elect(dp_full);
+    }
+    for (int it = 0; ok && it < n_it; ++it) {
+      const uint32_t q_base = q_at(it);
+      if (!mbar_wait_warp(pt_full, it & 1, abort_flag, p.status)) break;
+      tc_fence_after();
+      mma_tile_ts<D>(tmem + 256, tmem, q_base + L::kTileBytes, it > 0);
+      if (it + 1 < n_it) {
+        if (!mbar_wait_warp(&qd_full[(it + 1) % ST], ((it + 1) / ST) & 1, abort_flag, p.status))
+          break;
+        tc_fence_after();
+        mma_tile_ss<D>(tmem, k_base, q_at(it + 1));
+        mma_commit_elect(s_full);
+      }
       if (!mbar_wait_warp(p_full, it & 1, abort_flag, p.status)) break;
       tc_fence_after();
-      mma_tile_ts<D>(tmem + 256, tmem, do_base, it > 0);
       mma_tile_ts<D>(tmem + 256 + D, tmem + 128, q_base, it > 0);
-      mma_commit_elect(&qd_empty[s]);
+      mma_commit_elect(&qd_empty[it % ST]);
+      if (it + 1 < n_it) {
+        mma_tile_ss<D>(tmem + 128, v_base, q_at(it + 1) + L::kTileBytes);
+        mma_commit_elect(dp_full);
+      }
     }
     mma_commit_elect(kv_done);
     mma_commit_elect(drain);
@@ -465,22 +522,51 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // queries [qfirst, 128) of this tile see the key (causal); earlier
       // ones do not.  Queries past N carry lse2 = +inf, so their weight is 0.
       const int qfirst = CAUSAL ? max(0, kj - i * 128) : 0;
+      // P^T = exp(S^T * scale - lse[q]) as bf16 pairs, stored over S^T
+      uint32_t pp[64];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t sv[32], dp[32], pp[16], pd[16];
+        uint32_t sv[32];
         tmem_ld32_wait(tS + c * 32, sv);
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const int q0 = c * 32 + e;
+          const float4 l4 = *reinterpret_cast<const float4 *>(vl + q0);
+          const float w0 = (q0 >= qfirst) ? ex2(fmaf(__uint_as_float(sv[e]), sl2, -l4.x)) : 0.f;
+          const float w1 = (q0 + 1 >= qfirst) ? ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -l4.y)) : 0.f;
+          const float w2 = (q0 + 2 >= qfirst) ? ex2(fmaf(__uint_as_float(sv[e + 2]), sl2, -l4.z)) : 0.f;
+          const float w3 = (q0 + 3 >= qfirst) ? ex2(fmaf(__uint_as_float(sv[e + 3]), sl2, -l4.w)) : 0.f;
+          pp[c * 16 + (e >> 1)] = pack_bf16x2(w0, w1);
+          pp[c * 16 + (e >> 1) + 1] = pack_bf16x2(w2, w3);
+        }
+        uint32_t chunk[16];
+#pragma unroll
+        for (int t2 = 0; t2 < 16; ++t2) chunk[t2] = pp[c * 16 + t2];
+        tmem_st16(tS + c * 16, chunk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(pt_full);
+      ok = mbar_wait(dp_full, it & 1, abort_flag, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      // dS^T = P^T (dP^T - D[q]), stored over dP^T chunk by chunk
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t dp[32], pd[16];
         tmem_ld32_wait(tP + c * 32, dp);
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
+        for (int e = 0; e < 32; e += 4) {
           const int q0 = c * 32 + e;
-          const float w0 = (q0 >= qfirst) ? ex2(fmaf(__uint_as_float(sv[e]), sl2, -vl[q0])) : 0.f;
-          const float w1 =
-              (q0 + 1 >= qfirst) ? ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -vl[q0 + 1])) : 0.f;
-          pp[e >> 1] = pack_bf16x2(w0, w1);
-          pd[e >> 1] = pack_bf16x2(w0 * (__uint_as_float(dp[e]) - vd[q0]),
-                                   w1 * (__uint_as_float(dp[e + 1]) - vd[q0 + 1]));
+          const float4 d4 = *reinterpret_cast<const float4 *>(vd + q0);
+          const float2 wa = bf16x2_to_float2(pp[c * 16 + (e >> 1)]);
+          const float2 wb = bf16x2_to_float2(pp[c * 16 + (e >> 1) + 1]);
+          pd[e >> 1] = pack_bf16x2(wa.x * (__uint_as_float(dp[e]) - d4.x),
+                                   wa.y * (__uint_as_float(dp[e + 1]) - d4.y));
+          pd[(e >> 1) + 1] = pack_bf16x2(wb.x * (__uint_as_float(dp[e + 2]) - d4.z),
+                                         wb.y * (__uint_as_float(dp[e + 3]) - d4.w));
         }
-        tmem_st16(tS + c * 16, pp);
         tmem_st16(tP + c * 16, pd);
       }
       tmem_wait_st();
@@ -526,8 +612,10 @@ static cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tdo,
                                 const CUtensorMap &tk, const CUtensorMap &tv, const BwdParams &p,
                                 bool causal, cudaStream_t stream) {
   using L = BwdLayout<D>;
-  const long long pre_warps = static_cast<long long>(p.B) * p.Npad * p.H;
-  bwd_preprocess_kernel<D><<<static_cast<unsigned>((pre_warps + 7) / 8), 256, 0, stream>>>(p);
+  const long long pre_rows = static_cast<long long>(p.B) * p.Npad * p.H;
+  const long long rows_per_block = 256 / (D / 8);
+  bwd_preprocess_kernel<D><<<static_cast<unsigned>((pre_rows + rows_per_block - 1) / rows_per_block),
+                             256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   auto dq = causal ? bwd_dq_kernel<D, true> : bwd_dq_kernel<D, false>;
