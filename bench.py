@@ -405,6 +405,55 @@ def measure_backward(torch, device, fa, steps, warmup, peak):
             "launches_per_call": 3}
 
 
+def measure_splitkv(torch, device, fa, steps, warmup, peak):
+    """Split-KV dense prefill (fa_fwd_splitkv, automatic split count) on a
+    long sequence with few heads (B=1, H=4, N=8192, d=128, causal: 128
+    query-tile pairs, fewer than the SMs), timed beside fa_fwd on the same
+    inputs."""
+    cfg = W.WORKLOADS["splitkv_small_bh_d128"]
+    B, N, H, d = cfg["B"], cfg["N"], cfg["H"], cfg["d"]
+    inp = W.dense_inputs(B, N, H, cfg["Hkv"], d, seed=0)
+    q, k, v = (to_dev(getattr(inp, n), torch, device) for n in ("q", "k", "v"))
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    ws = torch.empty(fa.fa_fwd_splitkv_workspace_size(B, H, N, d, 0), dtype=torch.uint8,
+                     device=device)
+    flops = W.prefill_flops(B, N, H, d, True)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    ms = timed(lambda: fa.fa_fwd_splitkv(q, k, v, causal=True, out=out, lse=lse, workspace=ws))
+    ms_plain = timed(lambda: fa.fa_fwd(q, k, v, causal=True, out=out, lse=lse))
+    tf = flops / (ms / 1e3) / 1e12
+    return {"workload": "split-KV causal prefill, few heads: B1 H4 N8192 d128",
+            "ms": ms, "tflops": tf, "frac_of_peak": tf / peak, "flops": flops,
+            "unsplit_ms": ms_plain, "unsplit_tflops": flops / (ms_plain / 1e3) / 1e12,
+            "launches_per_call": 2}
+
+
+NEXT_LEGS = ("paged_prefill", "splitkv", "fp8_prefill", "backward")
+
+
+def run_next_leg(name, torch, device, fa, steps, warmup, peak):
+    fn = {"paged_prefill": measure_paged_prefill, "splitkv": measure_splitkv,
+          "fp8_prefill": measure_fp8_prefill, "backward": measure_backward}[name]
+    res = fn(torch, device, fa, steps, warmup, peak)
+    if fa.fa_device_status(clear=True) != 0:
+        raise RuntimeError(f"device status word set during the {name} leg")
+    return res
+
+
 LEG_ORDER = ("long", "varlen", "decode")
 LAUNCHES_PER_STEP = {"long": 1, "varlen": 1, "decode": 2}
 
@@ -592,18 +641,10 @@ def bench_ours(args, rank, world, local):
     nxt = {}
     if args.next_legs and "long" in order:
         peaks0 = measured_peaks()
-        nxt["paged_prefill"] = measure_paged_prefill(torch, device, fa, min(args.steps, 50),
-                                                     args.warmup, peaks0["bf16_tflops"])
-        if fa.fa_device_status(clear=True) != 0:
-            raise RuntimeError("device status word set during the paged-prefill leg")
-        nxt["fp8_prefill"] = measure_fp8_prefill(torch, device, fa, min(args.steps, 50),
-                                                 args.warmup, peaks0["bf16_tflops"])
-        if fa.fa_device_status(clear=True) != 0:
-            raise RuntimeError("device status word set during the fp8 prefill leg")
-        nxt["backward"] = measure_backward(torch, device, fa, min(args.steps, 20), args.warmup,
-                                           peaks0["bf16_tflops"])
-        if fa.fa_device_status(clear=True) != 0:
-            raise RuntimeError("device status word set during the backward leg")
+        for name in NEXT_LEGS:
+            nxt[name] = run_next_leg(name, torch, device, fa,
+                                     min(args.steps, 20 if name == "backward" else 50),
+                                     args.warmup, peaks0["bf16_tflops"])
 
     # ---- numbers (max over ranks of each time)
     K = args.steps
@@ -706,14 +747,24 @@ def main(argv=None):
     ap.add_argument("--legs", default="long,varlen,decode",
                     help="comma-separated subset of the step (for profiling runs)")
     ap.add_argument("--no-next", dest="next_legs", action="store_false",
-                    help="skip the separately timed paged-prefill leg")
+                    help="skip the separately timed legs (paged prefill, split-KV, FP8, backward)")
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="use only the first B decode sequences (for profiling runs)")
+    ap.add_argument("--profile-leg", choices=NEXT_LEGS, default=None,
+                    help="run only this separately timed leg, --steps times (for ncu runs)")
     args = ap.parse_args(argv)
     args.legs = [x for x in args.legs.split(",") if x]
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_env()
+    if args.profile_leg:
+        import torch
+        import exact_attention_33_gb300 as fa
+        fa.load_library()
+        res = run_next_leg(args.profile_leg, torch, torch.device("cuda", 0), fa, args.steps,
+                           args.warmup, measured_peaks()["bf16_tflops"])
+        print(json.dumps({"profile_leg": args.profile_leg, **res}))
+        return 0
     if args.impl == "reference":
         return bench_reference(args, rank, world)
     return bench_ours(args, rank, world, local)

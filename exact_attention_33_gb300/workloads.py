@@ -45,6 +45,7 @@ WORKLOADS = {
                                   ctx_lo=512, ctx_hi=32768),
     # chunked prefill over a paged cache: each sequence has a cached prefix of
     # U[1024, 16384] tokens (seed 6) and appends a chunk of 1024 new tokens
+    "splitkv_small_bh_d128": dict(kind="dense", B=1, H=4, Hkv=4, N=8192, d=128, causal=True),
     "long_causal_fp8_d128": dict(kind="dense_fp8", B=2, H=32, Hkv=32, N=8192, d=128,
                                  causal=True),
     "paged_prefill_gqa_d128": dict(kind="paged_prefill", batch=8, H=32, Hkv=8, d=128,
