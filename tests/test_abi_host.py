@@ -102,3 +102,47 @@ def test_workspace_size(lib):
     assert n >= 64 * 32 * 128 * 4 and n % 256 == 0
     assert fa.fa_decode_workspace_size(1, 32, 8, 128, 1024, 32) == 0
     assert fa.fa_decode_workspace_size(1, 30, 8, 128, 1024, 16) == 0
+
+
+def test_bwd_host_validation(lib):
+    import exact_attention_33_gb300  # noqa: F401  (sets argtypes)
+    f = lib.fa_bwd
+
+    def call(q=P, lse=P, ws=P, ws_bytes=1 << 30, B=1, H=4, Hkv=2, N=300, d=128, causal=1,
+             scale=0.1):
+        return f(q, P, P, P, lse, P, P, P, P, B, H, Hkv, N, d, scale, causal, ws, ws_bytes, NULL)
+    assert call(q=NULL) == -1
+    assert call(lse=NULL) == -1
+    assert call(q=P_BAD) == -1
+    assert call(H=3) == -1
+    assert call(causal=5) == -1
+    assert call(scale=0.0) == -1
+    assert call(d=96) == -2
+    assert call(B=0) == 0
+    assert call(N=0) == 0
+    assert call(ws=NULL) == -4
+    assert call(ws_bytes=16) == -4
+    assert call(ws=ctypes.c_void_p(0x10010)) == -4   # not 256-byte aligned
+
+
+def test_bwd_workspace_size():
+    import exact_attention_33_gb300 as fa
+    # two fp32 vectors (rowsums and rescaled lse) per (batch, head), N padded to 128
+    assert fa.fa_bwd_workspace_size(2, 32, 8192) == 2 * 2 * 32 * 8192 * 4
+    assert fa.fa_bwd_workspace_size(1, 1, 1) == 2 * 128 * 4
+    assert fa.fa_bwd_workspace_size(1, 4, 129) == 2 * 4 * 256 * 4
+    assert fa.fa_bwd_workspace_size(0, 4, 129) == 0
+
+
+def test_fp8_host_validation(lib):
+    import exact_attention_33_gb300  # noqa: F401
+    f = lib.fa_fwd_fp8
+
+    def call(q=P, B=1, H=2, Hkv=1, N=64, d=128, descales=(1.0, 1.0, 1.0), causal=0):
+        return f(q, P, P, P, NULL, B, H, Hkv, N, d, 0.1, *descales, causal, NULL)
+    assert call(q=NULL) == -1
+    assert call(descales=(1.0, float("inf"), 1.0)) == -1
+    assert call(descales=(1.0, 1.0, -2.0)) == -1
+    assert call(d=64) == -2
+    assert call(H=3, Hkv=2) == -1
+    assert call(N=0) == 0
