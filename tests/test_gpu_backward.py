@@ -106,3 +106,57 @@ def test_backward_deterministic_and_rejects(fa):
         fa.fa_bwd(q, k, v, out, lse, do, causal=True, workspace=small)
     assert e.value.status == -4
     assert_device_clean()
+
+
+def test_backward_full_size_sampled(fa):
+    """The backward leg's launch at full size (the long causal workload:
+    B=2, H=32, N=8192, d=128, 1% x8 key outliers).  The oracle evaluates the
+    gradients of two seeded (batch, head) pairs: dQ on 256 seeded rows, dK and
+    dV on 256 seeded keys (their columns of P need every row's log-sum-exp,
+    so the pair's full forward runs in fp64)."""
+    torch = torch_mod()
+    cfg = W.WORKLOADS["long_causal_d128"]
+    B, N, H, d = cfg["B"], cfg["N"], cfg["H"], cfg["d"]
+    inp = W.dense_inputs(B, N, H, cfg["Hkv"], d, seed=0, outlier_frac=cfg["outlier_frac"],
+                         outlier_scale=cfg["outlier_scale"])
+    do_bits = W.normal_bf16_bits((B, N, H, d), 0, 3)
+    q, k, v, do = dev_bf16(inp.q), dev_bf16(inp.k), dev_bf16(inp.v), dev_bf16(do_bits)
+    out, lse = fa.fa_fwd(q, k, v, causal=True)
+    dq, dk, dv = fa.fa_bwd(q, k, v, out, lse, do, causal=True)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(11)
+    pairs = [(int(x) // H, int(x) % H) for x in rng.choice(B * H, 2, replace=False)]
+    scale = 1.0 / math.sqrt(d)
+    for b, h in pairs:
+        qh, kh, vh = f64(inp.q[b, :, h]), f64(inp.k[b, :, h]), f64(inp.v[b, :, h])
+        doh = f64(do_bits[b, :, h])
+        # the pair's forward in fp64, one block of rows at a time
+        o = np.zeros((N, d))
+        lse_ref = np.zeros(N)
+        for r0 in range(0, N, 1024):
+            o_blk, l_blk = oracle.attention_one(qh[:, None], kh[:, None], vh[:, None], causal=True,
+                                                rows=np.arange(r0, min(N, r0 + 1024)))
+            o[r0:r0 + 1024] = o_blk[r0:r0 + 1024, 0]
+            lse_ref[r0:r0 + 1024] = l_blk[0, r0:r0 + 1024]
+        dsum = (doh * o).sum(axis=1)
+        rows = np.sort(rng.choice(N, 256, replace=False))
+        keys = np.sort(rng.choice(N, 256, replace=False))
+        # dQ rows: dS_i = P_i (dP_i - D_i), dQ_i = scale dS_i K
+        s_rows = scale * (qh[rows] @ kh.T)
+        s_rows[np.arange(N)[None, :] > rows[:, None]] = -np.inf
+        p_rows = np.exp(s_rows - lse_ref[rows, None])
+        ds_rows = p_rows * (doh[rows] @ vh.T - dsum[rows, None])
+        dq_ref = scale * (ds_rows @ kh)
+        # dK / dV keys: columns of P over every query
+        s_cols = scale * (qh @ kh[keys].T)
+        s_cols[np.arange(N)[:, None] < keys[None, :]] = -np.inf
+        p_cols = np.exp(s_cols - lse_ref[:, None])
+        dv_ref = p_cols.T @ doh
+        ds_cols = p_cols * (doh @ vh[keys].T - dsum[:, None])
+        dk_ref = scale * (ds_cols.T @ qh)
+        what = f"full b{b} h{h}"
+        errs = [check_grad("dq", host_f64(dq[b, rows, h]), dq_ref, what),
+                check_grad("dk", host_f64(dk[b, keys, h]), dk_ref, what),
+                check_grad("dv", host_f64(dv[b, keys, h]), dv_ref, what)]
+        print(f"{what}: relative RMS errors dq {errs[0]:.2e} dk {errs[1]:.2e} dv {errs[2]:.2e}")
+    assert_device_clean()

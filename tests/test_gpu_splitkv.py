@@ -65,3 +65,16 @@ def test_splitkv_workspace_checks(fa):
     with pytest.raises(fa.FaError) as e:
         fa.fa_fwd_splitkv(q, k, v, num_splits=3, workspace=ws)
     assert e.value.status == -4
+
+
+def test_splitkv_bench_workload_full(fa):
+    """The split-KV leg's workload (B=1, H=4, N=8192, d=128, causal, splits
+    chosen by the library), every element compared."""
+    torch = torch_mod()
+    cfg = W.WORKLOADS["splitkv_small_bh_d128"]
+    inp = W.dense_inputs(cfg["B"], cfg["N"], cfg["H"], cfg["Hkv"], cfg["d"], seed=0)
+    out, lse = fa.fa_fwd_splitkv(dev_bf16(inp.q), dev_bf16(inp.k), dev_bf16(inp.v), causal=True)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.attention_dense(f64(inp.q), f64(inp.k), f64(inp.v), causal=True)
+    compare(host_f64(out), o_ref, lse.cpu().numpy(), l_ref, "splitkv bench workload")
+    assert_device_clean()
