@@ -315,7 +315,13 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float 
   if (num_seqs == 0 || total_tokens == 0 || max_seqlen == 0) return FA_OK;
   if (max_seqlen > total_tokens) max_seqlen = total_tokens;
   const long long pairs = (max_seqlen + kPrefillRowsPerCta - 1) / kPrefillRowsPerCta;
-  const long long grid = pairs * num_seqs * H;
+  long long grid = pairs * num_seqs * H;
+  // Padding-free order: sum over sequences of ceil(len / 256) is at most
+  // ceil(T / 256) + num_seqs, so that many items per head cover every row.
+  const bool compact = num_seqs <= kVarlenCompactMaxSeqs;
+  if (compact)
+    grid = std::min(grid, ((total_tokens + kPrefillRowsPerCta - 1) / kPrefillRowsPerCta +
+                           static_cast<long long>(num_seqs)) * H);
   if (grid > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(total_tokens) * H * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
 
@@ -339,6 +345,7 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float 
   p.head_group = prefill_head_group(H);
   p.N = total_tokens;
   p.max_pairs = static_cast<int>(pairs);
+  p.compact = compact ? 1 : 0;
   p.total_tokens = total_tokens;
   p.scale_log2 = scale * kLog2e;
   p.v_descale = 1.f;

@@ -28,6 +28,10 @@ constexpr int kKindVarlen = 1;  // packed sequences, cu_seqlens
 constexpr int kKindPaged = 2;   // packed query chunks over a paged KV cache
 constexpr int kKindDenseSplit = 3;  // dense batch, key tiles split over CTAs
 
+// Packed batches of at most this many sequences use the padding-free order
+// of work items (each CTA finds its item with one pass over cu_seqlens).
+constexpr int kVarlenCompactMaxSeqs = 128;
+
 struct PrefillParams {
   unsigned int *status;   // per-device sticky FA_DEV_* word
   void *out;              // bf16 [rows, H, d] (dense rows = B*N, varlen rows = T)
@@ -38,6 +42,7 @@ struct PrefillParams {
   int head_group;         // heads per CTA-ordering group (divides H)
   int N;                  // dense: sequence length; varlen: total tokens
   int max_pairs;          // number of 256-row query-tile pairs of the longest sequence
+  int compact;            // varlen: work items enumerate only real (sequence, pair) items
   int total_tokens;       // varlen: T
   float scale_log2;       // scale * log2(e) (times the q and k descales for fp8)
   float v_descale;        // multiplies the output (1 for bf16)

@@ -67,6 +67,56 @@ struct PrefillLayout {
   static constexpr int kTmemO = 256;
 };
 
+// Work item `lin` of the padding-free order of a packed batch: sequences in
+// order; inside a sequence, groups of p.head_group heads; inside a group the
+// pair index varies slowest (heaviest first when causal) and the head
+// fastest.  A sequence of len rows owns H * ceil(len / 256) items, so the
+// grid needs no item per (sequence, pair) that has no rows.  Every warp
+// finds its item with one pass over cu_seqlens, 32 sequences at a time
+// (all lanes active).  Returns false past the last item.
+__device__ __forceinline__ bool varlen_compact_item(const PrefillParams &p, int lin, bool causal,
+                                                    int &unit, int &pair, int &h) {
+  const int lane = threadIdx.x & 31;
+  if (lin == 0 && threadIdx.x < 32) {
+    // A sequence with invalid bounds owns no item here; CTA 0 reports it.
+    for (int s = lane; s < p.B; s += 32) {
+      const int a = p.cu_seqlens[s], e = p.cu_seqlens[s + 1];
+      if (a < 0 || e < a || e > p.total_tokens) raise_status(p.status, FA_DEV_BAD_SEQLEN);
+    }
+  }
+  int base = 0;
+  for (int s0 = 0; s0 < p.B; s0 += 32) {
+    const int s = s0 + lane;
+    int np = 0;
+    if (s < p.B) {
+      const int a = p.cu_seqlens[s], e = p.cu_seqlens[s + 1];
+      const int n = min(max(e - a, 0), p.total_tokens);
+      np = (n + kPrefillRowsPerCta - 1) / kPrefillRowsPerCta;
+    }
+    const int mine = np * p.H;  // items of sequence s
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (lin < base + total) {
+      const int l = __ffs(__ballot_sync(0xffffffffu, lin < base + incl)) - 1;
+      unit = s0 + l;
+      const int lu = lin - base - __shfl_sync(0xffffffffu, incl - mine, l);
+      const int nps = __shfl_sync(0xffffffffu, np, l);
+      const int hgs = p.head_group;
+      const int rem = lu % (hgs * nps);
+      h = (lu / (hgs * nps)) * hgs + rem % hgs;
+      pair = causal ? (nps - 1 - rem / hgs) : rem / hgs;
+      return true;
+    }
+    base += total;
+  }
+  return false;
+}
+
 // KIND: dense batch, packed varlen batch, or packed queries over a paged KV
 // cache (chunked prefill).
 template <int D, bool CAUSAL, int KIND, bool FP8 = false>
@@ -91,14 +141,19 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   const int split = (KIND == kKindDenseSplit) ? static_cast<int>(blockIdx.x % p.num_splits) : 0;
   const int lin = (KIND == kKindDenseSplit) ? static_cast<int>(blockIdx.x / p.num_splits)
                                             : static_cast<int>(blockIdx.x);
-  const int hgs = p.head_group;
-  const int h_in = lin % hgs;
-  const int t_lin = lin / hgs;
-  const int pair_rank = t_lin % p.max_pairs;
-  const int grp = t_lin / p.max_pairs;
-  const int h = (grp % (p.H / hgs)) * hgs + h_in;
-  const int unit = grp / (p.H / hgs);  // batch element or sequence
-  const int pair = CAUSAL ? (p.max_pairs - 1 - pair_rank) : pair_rank;
+  int h, unit, pair;  // unit: batch element or sequence
+  if (KIND == kKindVarlen && p.compact) {
+    if (!varlen_compact_item(p, lin, CAUSAL, unit, pair, h)) return;  // past the last item
+  } else {
+    const int hgs = p.head_group;
+    const int h_in = lin % hgs;
+    const int t_lin = lin / hgs;
+    const int pair_rank = t_lin % p.max_pairs;
+    const int grp = t_lin / p.max_pairs;
+    h = (grp % (p.H / hgs)) * hgs + h_in;
+    unit = grp / (p.H / hgs);
+    pair = CAUSAL ? (p.max_pairs - 1 - pair_rank) : pair_rank;
+  }
   // len: query rows of the unit; kv_len: its keys; offset = kv_len - len
   // aligns causal masking to the bottom right (query i sees keys
   // j <= i + offset).
@@ -118,7 +173,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     }
     len = seq_end - seq_start;
     if (len > p.max_pairs * kPrefillRowsPerCta && pair == 0 && h == 0)
-      raise_status(p.status, FA_DEV_BAD_SEQLEN);  // longer than max_seqlen: tail not covered
+      raise_status(p.status, FA_DEV_BAD_SEQLEN);  // longer than max_seqlen (the padded order
+                                                  // misses its tail)
     b = 0;
     if (KIND == kKindVarlen) {
       kv_len = len;
