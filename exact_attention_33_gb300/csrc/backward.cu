@@ -17,8 +17,12 @@
 //                    S^T = K Q^T and dP^T = V dO^T, then dV += P^T dO and
 //                    dK += dS^T Q (A from TMEM), so the group's sum stays in
 //                    TMEM and no atomics are needed.
-// Roles per CTA: warps 0-3 elementwise (thread = TMEM lane = row), warp 4
-// issues the MMAs (converged, elect.sync), warp 5 is the TMA producer.
+// Roles per CTA: warps 0-7 elementwise (warps w and w + 4 share the TMEM
+// lanes of rows 32 (w % 4) .. + 31 and take the lower and upper 64 columns),
+// warp 8 issues the MMAs (converged, elect.sync), warp 9 is the TMA producer.
+// The bf16 operands the elementwise warps write (P, dS) land in the columns
+// each half has already read: keys 0-63 in columns [0, 32), keys 64-127 in
+// [64, 96) of the region, so the TMEM-sourced MMAs read them at that split.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -65,7 +69,7 @@ __device__ __forceinline__ void mma_tile_ss(uint32_t d_t, uint32_t a_base, uint3
   }
 }
 
-// O-like MMA: D[tmem, 128 x d] (+)= A[tmem, 128 x 128 bf16] B[128 x d]
+// O-like MMA: D[tmem, 128 x d] (+)= A[tmem, 128 x 128 bf16, split columns] B[128 x d]
 // with B a [rows x d] tile read MN-major (the contraction runs over rows).
 template <int D>
 __device__ __forceinline__ void mma_tile_ts(uint32_t d_t, uint32_t a_t, uint32_t b_base,
@@ -74,8 +78,9 @@ __device__ __forceinline__ void mma_tile_ts(uint32_t d_t, uint32_t a_t, uint32_t
   constexpr uint32_t kIdesc = idesc_bf16_f32(128, D, false, true);
 #pragma unroll
   for (int kk = 0; kk < 128 / 16; ++kk)
-    mma_ts_elect(d_t, a_t + kk * 8, sdesc_sw128(b_base + kk * 16 * 128, L::kChunkBytes, 1024),
-                 kIdesc, (acc || kk > 0) ? 1u : 0u);
+    mma_ts_elect(d_t, a_t + kk * 8 + (kk >= 4 ? 32 : 0),
+                 sdesc_sw128(b_base + kk * 16 * 128, L::kChunkBytes, 1024), kIdesc,
+                 (acc || kk > 0) ? 1u : 0u);
 }
 
 // Converts a row of 128 fp32 TMEM columns into 64 columns of bf16 pairs is
@@ -178,23 +183,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  if (warp == 5 && lane == 0) {
+  if (warp == 9 && lane == 0) {
     mbar_init(in_full, 1);
     for (int s = 0; s < ST; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(s_read, 128);
+    mbar_init(s_read, 256);
     mbar_init(dp_full, 1);
-    mbar_init(p_full, 128);
+    mbar_init(p_full, 256);
     mbar_init(dq_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
   }
-  if (warp == 4) {
+  if (warp == 8) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -203,7 +208,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 5) {
+  if (warp == 9) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -234,7 +239,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int j = max(0, issued - ST); j < issued; ++j)
         mbar_drain(&kv_full[j % ST], (j / ST) & 1, p.status);
     }
-  } else if (warp == 4) {
+  } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
     // S lives in TMEM [0,128), dP in [128,256), dQ in [256, 256 + d).  Per
     // key tile j: dP_j; then S_{j+1} as soon as the elementwise warps have
@@ -273,9 +278,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_drain(drain, 0, p.status);
   } else {
     // ------------------------------------------------------------ elementwise
-    const int row = warp * 32 + lane;
+    const int quad = warp & 3, hf = warp >> 2;  // TMEM lane group, column half
+    const int row = quad * 32 + lane;
     const int qi = t * 128 + row;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem + lane_off, tP = tmem + 128 + lane_off, tQ = tmem + 256 + lane_off;
     const size_t vec = (static_cast<size_t>(b) * p.H + h) * p.Npad + min(qi, p.Npad - 1);
     const float lse2 = p.lse2[vec];
@@ -289,11 +295,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       // keys [0, nvis) of this tile are visible to the row
       const int nvis = min(128, (CAUSAL ? min(p.N, qi + 1) : p.N) - j * 128);
-      // P = exp(S * scale - lse), kept as bf16 pairs (the values the dQ
-      // product uses through dS)
-      uint32_t pp[64];
+      // P = exp(S * scale - lse) of this half's 64 keys, kept as bf16 pairs
+      // (the values the dQ product uses through dS)
+      uint32_t pp[32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * hf + cc;
         uint32_t sv[32];
         tmem_ld32_wait(tS + c * 32, sv);
 #pragma unroll
@@ -301,7 +308,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const float w0 = (c * 32 + e < nvis) ? ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse2)) : 0.f;
           const float w1 =
               (c * 32 + e + 1 < nvis) ? ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -lse2)) : 0.f;
-          pp[c * 16 + (e >> 1)] = pack_bf16x2(w0, w1);
+          pp[cc * 16 + (e >> 1)] = pack_bf16x2(w0, w1);
         }
       }
       tc_fence_before();
@@ -310,19 +317,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      // dS = P (dP - D), written over dP chunk by chunk (chunk c of dS lands
-      // in columns already read)
+      // dS = P (dP - D), written over this half's dP columns
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * hf + cc;
         uint32_t dp[32], pk[16];
         tmem_ld32_wait(tP + c * 32, dp);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float2 w = bf16x2_to_float2(pp[c * 16 + (e >> 1)]);
+          const float2 w = bf16x2_to_float2(pp[cc * 16 + (e >> 1)]);
           pk[e >> 1] = pack_bf16x2(w.x * (__uint_as_float(dp[e]) - dsum),
                                    w.y * (__uint_as_float(dp[e + 1]) - dsum));
         }
-        tmem_st16(tP + c * 16, pk);
+        tmem_st16(tP + hf * 64 + cc * 16, pk);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -337,7 +344,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint16_t *dst = static_cast<uint16_t *>(p.dq) +
                       ((static_cast<size_t>(b) * p.N + qi) * p.H + h) * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = hf * (D / 64); c < (hf + 1) * (D / 64); ++c) {
         uint32_t o[32];
         tmem_ld32_wait(tQ + c * 32, o);
         if (qi < p.N) store_row_scaled_bf16(dst + c * 32, o, p.scale);
@@ -347,7 +354,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -392,7 +399,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  if (warp == 5 && lane == 0) {
+  if (warp == 9 && lane == 0) {
     mbar_init(in_full, 1);
     for (int s = 0; s < ST; ++s) {
       mbar_init(&qd_full[s], 1);
@@ -400,15 +407,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(pt_full, 128);
-    mbar_init(p_full, 128);
+    mbar_init(pt_full, 256);
+    mbar_init(p_full, 256);
     mbar_init(kv_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
   }
-  if (warp == 4) {
+  if (warp == 8) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -417,7 +424,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 5) {
+  if (warp == 9) {
     // ------------------------------------------------------------ producer
     // Iteration it: query head kvh * group + it % group, query tile
     // i0 + it / group.
@@ -456,7 +463,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int it = max(0, issued - ST); it < issued; ++it)
         mbar_drain(&qd_full[it % ST], (it / ST) & 1, p.status);
     }
-  } else if (warp == 4) {
+  } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
     // S^T lives in TMEM [0,128), dP^T in [128,256), dV and dK after them.
     // Per iteration: dV += P^T dO once P^T (bf16, over S^T) is in TMEM; then
@@ -500,9 +507,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_drain(drain, 0, p.status);
   } else {
     // ------------------------------------------------------------ elementwise
-    const int row = warp * 32 + lane;   // key row of the tile
+    const int quad = warp & 3, hf = warp >> 2;  // TMEM lane group, column half
+    const int row = quad * 32 + lane;   // key row of the tile
     const int kj = jt * 128 + row;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem + lane_off, tP = tmem + 128 + lane_off;
     const uint32_t tV = tmem + 256 + lane_off, tK = tmem + 256 + D + lane_off;
     const float sl2 = p.scale_log2;
@@ -522,10 +530,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // queries [qfirst, 128) of this tile see the key (causal); earlier
       // ones do not.  Queries past N carry lse2 = +inf, so their weight is 0.
       const int qfirst = CAUSAL ? max(0, kj - i * 128) : 0;
-      // P^T = exp(S^T * scale - lse[q]) as bf16 pairs, stored over S^T
-      uint32_t pp[64];
+      // P^T = exp(S^T * scale - lse[q]) of this half's 64 queries as bf16
+      // pairs, stored over S^T
+      uint32_t pp[32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * hf + cc;
         uint32_t sv[32];
         tmem_ld32_wait(tS + c * 32, sv);
 #pragma unroll
@@ -536,13 +546,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const float w1 = (q0 + 1 >= qfirst) ? ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -l4.y)) : 0.f;
           const float w2 = (q0 + 2 >= qfirst) ? ex2(fmaf(__uint_as_float(sv[e + 2]), sl2, -l4.z)) : 0.f;
           const float w3 = (q0 + 3 >= qfirst) ? ex2(fmaf(__uint_as_float(sv[e + 3]), sl2, -l4.w)) : 0.f;
-          pp[c * 16 + (e >> 1)] = pack_bf16x2(w0, w1);
-          pp[c * 16 + (e >> 1) + 1] = pack_bf16x2(w2, w3);
+          pp[cc * 16 + (e >> 1)] = pack_bf16x2(w0, w1);
+          pp[cc * 16 + (e >> 1) + 1] = pack_bf16x2(w2, w3);
         }
         uint32_t chunk[16];
 #pragma unroll
-        for (int t2 = 0; t2 < 16; ++t2) chunk[t2] = pp[c * 16 + t2];
-        tmem_st16(tS + c * 16, chunk);
+        for (int t2 = 0; t2 < 16; ++t2) chunk[t2] = pp[cc * 16 + t2];
+        tmem_st16(tS + hf * 64 + cc * 16, chunk);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -551,23 +561,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      // dS^T = P^T (dP^T - D[q]), stored over dP^T chunk by chunk
+      // dS^T = P^T (dP^T - D[q]), stored over this half's dP^T columns
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * hf + cc;
         uint32_t dp[32], pd[16];
         tmem_ld32_wait(tP + c * 32, dp);
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           const int q0 = c * 32 + e;
           const float4 d4 = *reinterpret_cast<const float4 *>(vd + q0);
-          const float2 wa = bf16x2_to_float2(pp[c * 16 + (e >> 1)]);
-          const float2 wb = bf16x2_to_float2(pp[c * 16 + (e >> 1) + 1]);
+          const float2 wa = bf16x2_to_float2(pp[cc * 16 + (e >> 1)]);
+          const float2 wb = bf16x2_to_float2(pp[cc * 16 + (e >> 1) + 1]);
           pd[e >> 1] = pack_bf16x2(wa.x * (__uint_as_float(dp[e]) - d4.x),
                                    wa.y * (__uint_as_float(dp[e + 1]) - d4.y));
           pd[(e >> 1) + 1] = pack_bf16x2(wb.x * (__uint_as_float(dp[e + 2]) - d4.z),
                                          wb.y * (__uint_as_float(dp[e + 3]) - d4.w));
         }
-        tmem_st16(tP + c * 16, pd);
+        tmem_st16(tP + hf * 64 + cc * 16, pd);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -583,13 +594,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint16_t *dv = static_cast<uint16_t *>(p.dv) + orow;
       uint16_t *dk = static_cast<uint16_t *>(p.dk) + orow;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = hf * (D / 64); c < (hf + 1) * (D / 64); ++c) {
         uint32_t o[32];
         tmem_ld32_wait(tV + c * 32, o);
         if (kj < p.N) store_row_scaled_bf16(dv + c * 32, o, 1.f);
       }
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = hf * (D / 64); c < (hf + 1) * (D / 64); ++c) {
         uint32_t o[32];
         tmem_ld32_wait(tK + c * 32, o);
         if (kj < p.N) store_row_scaled_bf16(dk + c * 32, o, p.scale);
@@ -599,7 +610,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

@@ -61,7 +61,7 @@ struct PrefillParams {
 
 // ----------------------------------------------------------------- backward
 
-constexpr int kBwdThreads = 192;  // 4 elementwise warps + 1 MMA warp + 1 TMA warp
+constexpr int kBwdThreads = 320;  // 8 elementwise warps + 1 MMA warp + 1 TMA warp
 
 struct BwdParams {
   unsigned int *status;   // per-device sticky FA_DEV_* word
