@@ -43,14 +43,35 @@ struct BwdLayout {
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
   static constexpr int kStages = 2;
-  // dq kernel: Q, dO, then K and V rings.  dkdv kernel: K, V, then Q and dO
-  // rings plus the per-stage log-sum-exp and D vectors (128 floats each).
-  static constexpr int kA = 0;                          // Q (dq) / K (dkdv)
-  static constexpr int kB = kA + kTileBytes;            // dO (dq) / V (dkdv)
+  // dK/dV kernel: K, V, then a ring of (Q, dO) tile pairs plus the
+  // per-stage log-sum-exp and D vectors (128 floats each).
+  static constexpr int kA = 0;                          // K
+  static constexpr int kB = kA + kTileBytes;            // V
   static constexpr int kR0 = kB + kTileBytes;           // ring of tile pairs
   static constexpr int kVec = kR0 + 2 * kStages * kTileBytes;
   static constexpr int kBar = kVec + kStages * 2 * 512;
   static constexpr int kNumBars = 2 + 2 * kStages + 8;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kSmemAlloc = kBytes + 1024;
+};
+
+// Shared memory of the dQ kernel: Q and dO of the query tile, then separate
+// K and V rings (V_j is released as soon as dP_j is done, K_j only after
+// dQ_j, so K gets the deeper ring).
+template <int D>
+struct BwdDqLayout {
+  static constexpr int kChunkBytes = 128 * 128;
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTileBytes = kChunks * kChunkBytes;
+  static constexpr int kStagesK = 3;
+  static constexpr int kStagesV = 2;
+  static constexpr int kQ = 0;
+  static constexpr int kDO = kQ + kTileBytes;
+  static constexpr int kK = kDO + kTileBytes;
+  static constexpr int kV = kK + kStagesK * kTileBytes;
+  static constexpr int kBar = kV + kStagesV * kTileBytes;
+  static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 6;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kSmemAlloc = kBytes + 1024;
@@ -151,8 +172,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const BwdParams p) {
-  using L = BwdLayout<D>;
-  constexpr int ST = L::kStages;
+  using L = BwdDqLayout<D>;
+  constexpr int SK = L::kStagesK;
+  constexpr int SV = L::kStagesV;
   // heaviest query tiles first (causal), heads fastest
   const int h = static_cast<int>(blockIdx.x % p.H);
   const int rest = static_cast<int>(blockIdx.x / p.H);
@@ -167,9 +189,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBar);
   uint64_t *in_full = bars;        // Q and dO
-  uint64_t *kv_full = bars + 1;    // [ST]
-  uint64_t *kv_empty = kv_full + ST;
-  uint64_t *s_full = kv_empty + ST;
+  uint64_t *k_full = bars + 1;     // [SK]
+  uint64_t *k_empty = k_full + SK;
+  uint64_t *v_full = k_empty + SK;  // [SV]
+  uint64_t *v_empty = v_full + SV;
+  uint64_t *s_full = v_empty + SV;
   uint64_t *s_read = s_full + 1;    // the elementwise warps have read S_j
   uint64_t *dp_full = s_read + 1;
   uint64_t *p_full = dp_full + 1;   // dS_j (bf16) is in TMEM
@@ -177,17 +201,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t *drain = dq_done + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
-  uint8_t *sQ = smem + L::kA;
-  uint8_t *sDO = smem + L::kB;
-  uint8_t *sR = smem + L::kR0;  // stage s: K at 2s, V at 2s + 1
+  uint8_t *sQ = smem + L::kQ;
+  uint8_t *sDO = smem + L::kDO;
+  uint8_t *sK = smem + L::kK;
+  uint8_t *sV = smem + L::kV;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   if (warp == 9 && lane == 0) {
     mbar_init(in_full, 1);
-    for (int s = 0; s < ST; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+    for (int s = 0; s < SK; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < SV; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     mbar_init(s_full, 1);
     mbar_init(s_read, 256);
@@ -221,23 +250,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_4d(sQ + c * L::kChunkBytes, &tm_q, in_full, c * 64, h, t * 128, b);
         tma_load_4d(sDO + c * L::kChunkBytes, &tm_do, in_full, c * 64, h, t * 128, b);
       }
-      int issued = 0;
+      // K(j) then V(j) for every j; each waits for its own ring
+      int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n_kv; ++j) {
-        const int s = j % ST;
-        if (j >= ST && !mbar_wait(&kv_empty[s], ((j / ST) - 1) & 1, abort_flag, p.status)) break;
-        mbar_arrive_expect_tx(&kv_full[s], 2 * L::kTileBytes);
-        uint8_t *sk = sR + (2 * s) * L::kTileBytes;
-        uint8_t *sv = sk + L::kTileBytes;
+        const int sk = j % SK, sv = j % SV;
+        if (j >= SK && !mbar_wait(&k_empty[sk], ((j / SK) - 1) & 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&k_full[sk], L::kTileBytes);
 #pragma unroll
-        for (int c = 0; c < L::kChunks; ++c) {
-          tma_load_4d(sk + c * L::kChunkBytes, &tm_k, &kv_full[s], c * 64, kvh, j * 128, b);
-          tma_load_4d(sv + c * L::kChunkBytes, &tm_v, &kv_full[s], c * 64, kvh, j * 128, b);
-        }
-        issued = j + 1;
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_4d(sK + sk * L::kTileBytes + c * L::kChunkBytes, &tm_k, &k_full[sk], c * 64,
+                      kvh, j * 128, b);
+        k_issued = j + 1;
+        if (j >= SV && !mbar_wait(&v_empty[sv], ((j / SV) - 1) & 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&v_full[sv], L::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_4d(sV + sv * L::kTileBytes + c * L::kChunkBytes, &tm_v, &v_full[sv], c * 64,
+                      kvh, j * 128, b);
+        v_issued = j + 1;
       }
       mbar_drain(in_full, 0, p.status);
-      for (int j = max(0, issued - ST); j < issued; ++j)
-        mbar_drain(&kv_full[j % ST], (j / ST) & 1, p.status);
+      for (int j = max(0, k_issued - SK); j < k_issued; ++j)
+        mbar_drain(&k_full[j % SK], (j / SK) & 1, p.status);
+      for (int j = max(0, v_issued - SV); j < v_issued; ++j)
+        mbar_drain(&v_full[j % SV], (j / SV) & 1, p.status);
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
@@ -248,30 +284,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // is issued after dQ_j by this thread, so it overwrites dS_j only after
     // dQ_j has read it.
     const uint32_t q_base = smem_u32(sQ), do_base = smem_u32(sDO);
-    auto k_at = [&](int j) { return smem_u32(sR + (2 * (j % ST)) * L::kTileBytes); };
+    const uint32_t k_ring = smem_u32(sK), v_ring = smem_u32(sV);
     bool ok = mbar_wait_warp(in_full, 0, abort_flag, p.status) &&
-              mbar_wait_warp(&kv_full[0], 0, abort_flag, p.status);
+              mbar_wait_warp(&k_full[0], 0, abort_flag, p.status);
     if (ok) {
       tc_fence_after();
-      mma_tile_ss<D>(tmem, q_base, k_at(0));
+      mma_tile_ss<D>(tmem, q_base, k_ring);
       mma_commit_elect(s_full);
     }
     for (int j = 0; ok && j < n_kv; ++j) {
-      const uint32_t k_base = k_at(j);
-      mma_tile_ss<D>(tmem + 128, do_base, k_base + L::kTileBytes);
+      const int sk = j % SK, sv = j % SV;
+      if (!mbar_wait_warp(&v_full[sv], (j / SV) & 1, abort_flag, p.status)) break;
+      tc_fence_after();
+      mma_tile_ss<D>(tmem + 128, do_base, v_ring + sv * L::kTileBytes);
       mma_commit_elect(dp_full);
+      mma_commit_elect(&v_empty[sv]);
       if (j + 1 < n_kv) {
+        const int sk1 = (j + 1) % SK;
         ok = mbar_wait_warp(s_read, j & 1, abort_flag, p.status) &&
-             mbar_wait_warp(&kv_full[(j + 1) % ST], ((j + 1) / ST) & 1, abort_flag, p.status);
+             mbar_wait_warp(&k_full[sk1], ((j + 1) / SK) & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
-        mma_tile_ss<D>(tmem, q_base, k_at(j + 1));
+        mma_tile_ss<D>(tmem, q_base, k_ring + sk1 * L::kTileBytes);
         mma_commit_elect(s_full);
       }
       if (!mbar_wait_warp(p_full, j & 1, abort_flag, p.status)) break;
       tc_fence_after();
-      mma_tile_ts<D>(tmem + 256, tmem + 128, k_base, j > 0);
-      mma_commit_elect(&kv_empty[j % ST]);
+      mma_tile_ts<D>(tmem + 256, tmem + 128, k_ring + sk * L::kTileBytes, j > 0);
+      mma_commit_elect(&k_empty[sk]);
     }
     mma_commit_elect(dq_done);
     mma_commit_elect(drain);
@@ -631,7 +671,8 @@ static cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tdo,
   if (e != cudaSuccess) return e;
   auto dq = causal ? bwd_dq_kernel<D, true> : bwd_dq_kernel<D, false>;
   auto dkdv = causal ? bwd_dkdv_kernel<D, true> : bwd_dkdv_kernel<D, false>;
-  e = cudaFuncSetAttribute(dq, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
+  e = cudaFuncSetAttribute(dq, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           BwdDqLayout<D>::kSmemAlloc);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(dkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
   if (e != cudaSuccess) return e;
@@ -640,7 +681,7 @@ static cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tdo,
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const unsigned grid_q = static_cast<unsigned>(p.B * p.H * p.n_tiles);
-  dq<<<grid_q, kBwdThreads, L::kSmemAlloc, stream>>>(tq, tdo, tk, tv, p);
+  dq<<<grid_q, kBwdThreads, BwdDqLayout<D>::kSmemAlloc, stream>>>(tq, tdo, tk, tv, p);
   return cudaGetLastError();
 }
 
