@@ -77,17 +77,22 @@ struct BwdDqLayout {
   static constexpr int kSmemAlloc = kBytes + 1024;
 };
 
-// S-like MMA (both operands K-major over d): D[tmem] = A[128 x d] B[128 x d]^T
+// S-like MMA (both operands K-major over d): D[tmem] = A[128 x d] B[128 x d]^T.
+// One lane of the converged MMA warp (the same one every time) issues the
+// whole product; the K-steps advance the descriptors' address fields.
 template <int D>
 __device__ __forceinline__ void mma_tile_ss(uint32_t d_t, uint32_t a_base, uint32_t b_base) {
   using L = BwdLayout<D>;
   constexpr uint32_t kIdesc = idesc_bf16_f32(128, 128, false, false);
+  if (elect_one()) {
+    const uint64_t a0 = sdesc_sw128(a_base, 16, 1024), b0 = sdesc_sw128(b_base, 16, 1024);
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-    mma_ss_elect(d_t, sdesc_sw128(a_base + off, 16, 1024), sdesc_sw128(b_base + off, 16, 1024),
-                 kIdesc, kk > 0 ? 1u : 0u);
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint64_t off = static_cast<uint64_t>(((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4);
+      mma_ss(d_t, a0 + off, b0 + off, kIdesc, kk > 0 ? 1u : 0u);
+    }
   }
+  __syncwarp();
 }
 
 // O-like MMA: D[tmem, 128 x d] (+)= A[tmem, 128 x 128 bf16, split columns] B[128 x d]
@@ -97,11 +102,14 @@ __device__ __forceinline__ void mma_tile_ts(uint32_t d_t, uint32_t a_t, uint32_t
                                             bool acc) {
   using L = BwdLayout<D>;
   constexpr uint32_t kIdesc = idesc_bf16_f32(128, D, false, true);
+  if (elect_one()) {
+    const uint64_t b0 = sdesc_sw128(b_base, L::kChunkBytes, 1024);
 #pragma unroll
-  for (int kk = 0; kk < 128 / 16; ++kk)
-    mma_ts_elect(d_t, a_t + kk * 8 + (kk >= 4 ? 32 : 0),
-                 sdesc_sw128(b_base + kk * 16 * 128, L::kChunkBytes, 1024), kIdesc,
-                 (acc || kk > 0) ? 1u : 0u);
+    for (int kk = 0; kk < 128 / 16; ++kk)
+      mma_ts(d_t, a_t + kk * 8 + (kk >= 4 ? 32 : 0),
+             b0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), kIdesc, (acc || kk > 0) ? 1u : 0u);
+  }
+  __syncwarp();
 }
 
 // Converts a row of 128 fp32 TMEM columns into 64 columns of bf16 pairs is

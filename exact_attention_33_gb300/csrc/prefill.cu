@@ -481,34 +481,43 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       const uint32_t k_base = smem_u32(sK);
       const uint32_t v_base = smem_u32(sV);
 
+      // One lane (the same one every time: the warp is converged) issues a
+      // whole product and its commit; the K-steps advance the descriptors'
+      // address fields (address / 16) by constants.
       auto issue_s = [&](int i, int st) {
         const uint32_t d_t = tmem + i * 128;
+        if (elect_one()) {
+          const uint64_t a0 = sdesc_sw128(q_base + i * L::kTileBytes, 16, 1024);
+          const uint64_t b0 = sdesc_sw128(k_base + st * L::kTileBytes, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < D / kKStep; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-          const uint64_t a = sdesc_sw128(q_base + i * L::kTileBytes + off, 16, 1024);
-          const uint64_t bd = sdesc_sw128(k_base + st * L::kTileBytes + off, 16, 1024);
-          if (FP8)
-            mma_ss_f8_elect(d_t, a, bd, kIdescS, kk > 0 ? 1u : 0u);
-          else
-            mma_ss_elect(d_t, a, bd, kIdescS, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / kKStep; ++kk) {
+            const uint64_t off = static_cast<uint64_t>(((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4);
+            if (FP8)
+              mma_ss_f8(d_t, a0 + off, b0 + off, kIdescS, kk > 0 ? 1u : 0u);
+            else
+              mma_ss(d_t, a0 + off, b0 + off, kIdescS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&s_full[i]);
         }
-        mma_commit_elect(&s_full[i]);
+        __syncwarp();
       };
       auto issue_o = [&](int i, int st, int j) {
         const uint32_t d_t = tmem + L::kTmemO + i * D;
         const uint32_t p_t = tmem + i * 128;
+        if (elect_one()) {
+          const uint64_t b0 = sdesc_sw128(v_base + st * L::kTileBytes, L::kChunkBytes, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kPrefillBN / kKStep; ++kk) {
-          // kKStep keys of 128-byte rows; P holds kKStep keys in 8 TMEM columns
-          const uint64_t bd = sdesc_sw128(v_base + st * L::kTileBytes + kk * kKStep * 128,
-                                          L::kChunkBytes, 1024);
-          if (FP8)
-            mma_ts_f8_elect(d_t, p_t + kk * 8, bd, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
-          else
-            mma_ts_elect(d_t, p_t + kk * 8, bd, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kPrefillBN / kKStep; ++kk) {
+            // kKStep keys of 128-byte rows; P holds kKStep keys in 8 TMEM columns
+            const uint64_t off = static_cast<uint64_t>((kk * kKStep * 128) >> 4);
+            if (FP8)
+              mma_ts_f8(d_t, p_t + kk * 8, b0 + off, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+            else
+              mma_ts(d_t, p_t + kk * 8, b0 + off, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&o_done[i]);
         }
-        mma_commit_elect(&o_done[i]);
+        __syncwarp();
       };
 
       // Issue order per key tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so
