@@ -57,9 +57,10 @@ struct PrefillLayout {
   static constexpr int kK = kQ + kPrefillQTiles * kTileBytes;
   static constexpr int kV = kK + kStagesK * kTileBytes;
   static constexpr int kBar = kV + kStagesV * kTileBytes;
-  // q_full, k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], s_full[2],
-  // p_full[2], o_done[2], drain
-  static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 7;
+  // q_full, k_full[SK], k_empty[SK], v_full[SV], s_full[2], p_full[2],
+  // o_done[2], drain.  A V stage has no release barrier of its own: the
+  // K-stage release that follows the P V products of a key tile frees it.
+  static constexpr int kNumBars = 1 + 2 * kStagesK + kStagesV + 7;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kSmemAlloc = kBytes + 1024;     // base is aligned up to 1024 in-kernel
@@ -233,8 +234,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   uint64_t *k_full = bars + 1;
   uint64_t *k_empty = k_full + SK;
   uint64_t *v_full = k_empty + SK;
-  uint64_t *v_empty = v_full + SV;
-  uint64_t *s_full = v_empty + SV;
+  uint64_t *s_full = v_full + SV;
   uint64_t *p_full = s_full + 2;
   uint64_t *o_done = p_full + 2;
   uint64_t *drain = o_done + 2;
@@ -261,7 +261,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     }
     for (int s = 0; s < SV; ++s) {
       mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -378,7 +377,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     };
     auto load_v = [&](int j) -> bool {
       const int sv = j % SV;
-      if (j >= SV && !mbar_wait_warp(&v_empty[sv], ((j / SV) - 1) & 1, abort_flag, p.status))
+      if (j >= SV && !mbar_wait_warp(&k_empty[(j - SV + 1) % SK], ((j - SV + 1) / SK) & 1,
+                                     abort_flag, p.status))
         return false;
       int rows;
       const int phys = lookup(j, rows);
@@ -442,7 +442,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       };
       auto load_v = [&](int j) -> bool {
         const int sv = j % SV;
-        if (j >= SV && !mbar_wait(&v_empty[sv], ((j / SV) - 1) & 1, abort_flag, p.status))
+        if (j >= SV && !mbar_wait(&k_empty[(j - SV + 1) % SK], ((j - SV + 1) / SK) & 1,
+                                  abort_flag, p.status))
           return false;
         mbar_arrive_expect_tx(&v_full[sv], L::kTileBytes);
 #pragma unroll
@@ -515,7 +516,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             else
               mma_ts(d_t, p_t + kk * 8, b0 + off, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(&o_done[i]);
+          // only the epilogue waits for O (the O rescale in the softmax is
+          // ordered by the S commit, which covers every earlier product)
+          if (j == kv_end[i] - 1) mma_commit(&o_done[i]);
         }
         __syncwarp();
       };
@@ -564,9 +567,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           issue_o(1, sv, j);
         }
         if (j + 1 < kv_end[1]) issue_s(1, sk1);
-        // Stage releases after the products (a commit costs as much as
-        // several MMA issues and would otherwise delay S_1(j+1)).
-        mma_commit_elect(&v_empty[sv]);
+        // One stage release per key tile, after the products (a commit costs
+        // as much as several MMA issues): it frees the stage of K(j+1) once
+        // S_0(j+1) and S_1(j+1) are done, and, since it also covers the
+        // P V products of this key tile, the stage of V(j).  The producer
+        // waits for V(t)'s stage on the release of key tile t - SV.
         if (j + 1 < n_kv) mma_commit_elect(&k_empty[sk1]);
       }
       // Everything this thread issued must finish before TMEM is released.
@@ -721,7 +726,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       const bool tile_live = row0 + i * kPrefillBM < len;
       bool have = ok && my_end > 0;
       if (have) {
-        have = mbar_wait(&o_done[i], (my_end - 1) & 1, abort_flag, p.status);
+        have = mbar_wait(&o_done[i], 0, abort_flag, p.status);
         have = __all_sync(0xffffffffu, have);
       }
       if (tile_live && (have || my_end == 0)) {
@@ -747,7 +752,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
               have ? make_float4(m, l, l_exact, 0.f) : make_float4(-CUDART_INF_F, 0.f, 0.f, 0.f);
       }
     } else if (ok && my_end > 0) {
-      ok = mbar_wait(&o_done[i], (my_end - 1) & 1, abort_flag, p.status);
+      ok = mbar_wait(&o_done[i], 0, abort_flag, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
