@@ -548,25 +548,33 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           k_next = true;
           return true;
         };
-        // V(j) and K(j+1) are normally resident long before P_0(j) is
-        // ready: waiting for them first keeps both waits off the path from
-        // P_i(j) to S_i(j+1).  (Their loads never depend on this iteration's
-        // releases, so the order cannot deadlock.)
+        // With dense K/V, V(j) and K(j+1) are resident long before P_0(j)
+        // is ready: waiting for them first keeps both waits off the path
+        // from P_i(j) to S_i(j+1).  (Their loads never depend on this
+        // iteration's releases, so the order cannot deadlock.)  Gathered
+        // paged K may still be in flight, so that kind waits for K(j+1)
+        // only before the S MMAs that read it.
         if (!mbar_wait_warp(&v_full[sv], (j / SV) & 1, abort_flag, p.status)) break;
-        if (j + 1 < n_kv && !wait_k_next()) break;
+        if (KIND != kKindPaged && j + 1 < n_kv && !wait_k_next()) break;
         tc_fence_after();
         if (j < kv_end[0]) {
           if (!mbar_wait_warp(&p_full[0], j & 1, abort_flag, p.status)) break;
           tc_fence_after();
           issue_o(0, sv, j);
         }
-        if (j + 1 < kv_end[0]) issue_s(0, sk1);
+        if (j + 1 < kv_end[0]) {
+          if (!wait_k_next()) break;
+          issue_s(0, sk1);
+        }
         if (j < kv_end[1]) {
           if (!mbar_wait_warp(&p_full[1], j & 1, abort_flag, p.status)) break;
           tc_fence_after();
           issue_o(1, sv, j);
         }
-        if (j + 1 < kv_end[1]) issue_s(1, sk1);
+        if (j + 1 < kv_end[1]) {
+          if (!wait_k_next()) break;
+          issue_s(1, sk1);
+        }
         // One stage release per key tile, after the products (a commit costs
         // as much as several MMA issues): it frees the stage of K(j+1) once
         // S_0(j+1) and S_1(j+1) are done, and, since it also covers the
