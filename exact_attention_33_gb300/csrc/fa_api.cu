@@ -24,7 +24,8 @@ __device__ unsigned int g_status = 0;
 
 cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                            const CUtensorMap &tv1, const CUtensorMap &to, const PrefillParams &p,
-                           int d, bool causal, int kind, int grid, cudaStream_t stream);
+                           int d, bool causal, int kind, int grid, cudaStream_t stream,
+                           int qtiles = 2);
 cudaError_t launch_prefill_split_combine(const PrefillParams &p, int d, cudaStream_t stream);
 cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUtensorMap &tk,
                        const CUtensorMap &tv, const BwdParams &p, int d, bool causal,
@@ -314,14 +315,19 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float 
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (num_seqs == 0 || total_tokens == 0 || max_seqlen == 0) return FA_OK;
   if (max_seqlen > total_tokens) max_seqlen = total_tokens;
-  const long long pairs = (max_seqlen + kPrefillRowsPerCta - 1) / kPrefillRowsPerCta;
+  // Batches of short sequences (under 4096 rows on average) run one query
+  // tile per CTA, two CTAs per SM: their CTAs are short, and the second CTA
+  // hides each one's launch, set-up and epilogue.  Longer sequences keep two
+  // query tiles per CTA, whose shared K/V stages make the key loop faster.
+  const int qtiles = (static_cast<long long>(total_tokens) < 4096LL * num_seqs) ? 1 : 2;
+  const int rows = kPrefillBM * qtiles;
+  const long long pairs = (max_seqlen + rows - 1) / rows;
   long long grid = pairs * num_seqs * H;
-  // Padding-free order: sum over sequences of ceil(len / 256) is at most
-  // ceil(T / 256) + num_seqs, so that many items per head cover every row.
+  // Padding-free order: sum over sequences of ceil(len / rows) is at most
+  // ceil(T / rows) + num_seqs, so that many items per head cover every row.
   const bool compact = num_seqs <= kVarlenCompactMaxSeqs;
   if (compact)
-    grid = std::min(grid, ((total_tokens + kPrefillRowsPerCta - 1) / kPrefillRowsPerCta +
-                           static_cast<long long>(num_seqs)) * H);
+    grid = std::min(grid, ((total_tokens + rows - 1) / rows + static_cast<long long>(num_seqs)) * H);
   if (grid > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(total_tokens) * H * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
 
@@ -351,7 +357,8 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float 
   p.v_descale = 1.f;
   p.causal = causal;
   cudaError_t e = launch_prefill(tq, tk, tv, tv, to, p, d, causal != 0, kKindVarlen,
-                                 static_cast<int>(grid), reinterpret_cast<cudaStream_t>(stream));
+                                 static_cast<int>(grid), reinterpret_cast<cudaStream_t>(stream),
+                                 qtiles);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -22,6 +22,31 @@ constexpr int kPrefillQTiles = 2;
 constexpr int kPrefillRowsPerCta = kPrefillBM * kPrefillQTiles;
 constexpr int kPrefillThreads = 320;  // 8 softmax warps + 1 MMA warp + 1 TMA warp
 
+// The same kernel with one query tile per CTA (packed batches of short
+// sequences): 256 threads, warps 0-3 softmax, 4 MMA, 5 TMA, 6-7 idle, and two
+// CTAs per SM, so that one CTA's launch, set-up and epilogue overlap the
+// other's key loop.  Each CTA is built for 128 registers per thread and moves
+// them with setmaxnreg: the softmax warpgroup up to 168, the other down to 88
+// (4 * 32 * 168 + 4 * 32 * 88 = 256 * 128; per SMSP, two CTAs use 2 * 32 *
+// 168 + 2 * 32 * 88 = 16384, the SMSP's register file).
+constexpr int kPrefill1LaunchRegs = 128;
+constexpr int kPrefill1SoftmaxRegs = 168;
+constexpr int kPrefill1CtlRegs = 88;
+static_assert(128 * kPrefill1SoftmaxRegs + 128 * kPrefill1CtlRegs <= 256 * kPrefill1LaunchRegs,
+              "one-tile prefill register split exceeds the launch allocation");
+
+// Shape of a prefill CTA with QT query tiles.
+template <int QT>
+struct PrefillShape {
+  static_assert(QT == 1 || QT == 2, "one or two query tiles per CTA");
+  static constexpr int kRows = kPrefillBM * QT;
+  static constexpr int kThreads = QT == 2 ? kPrefillThreads : 256;
+  static constexpr int kSoftmaxWarps = 4 * QT;
+  static constexpr int kMmaWarp = kSoftmaxWarps;
+  static constexpr int kTmaWarp = kSoftmaxWarps + 1;
+  static constexpr int kMinBlocks = QT == 2 ? 1 : 2;
+};
+
 // Work layouts of the prefill kernel.
 constexpr int kKindDense = 0;   // [B, N, H, d] batch
 constexpr int kKindVarlen = 1;  // packed sequences, cu_seqlens

@@ -38,7 +38,7 @@ namespace fa {
 // grows by more than this many powers of two.
 constexpr float kRescaleLog2 = 8.f;
 
-template <int D, bool FP8 = false>
+template <int D, bool FP8 = false, int QT = 2>
 struct PrefillLayout {
   static constexpr int kElemBytes = FP8 ? 1 : 2;
   static constexpr int kChunkElems = 128 / kElemBytes;   // elements per 128-byte swizzle row
@@ -51,10 +51,14 @@ struct PrefillLayout {
 #define FA_PREFILL_STAGES_K128 3
 #define FA_PREFILL_STAGES_V128 2
 #endif
-  static constexpr int kStagesK = (kTileBytes == 32768) ? FA_PREFILL_STAGES_K128 : 5;
-  static constexpr int kStagesV = (kTileBytes == 32768) ? FA_PREFILL_STAGES_V128 : 5;
+  // With one query tile per CTA two CTAs share an SM's shared memory, so
+  // 32 KiB tiles get one stage each.
+  static constexpr int kStagesK =
+      (QT == 1) ? ((kTileBytes == 32768) ? 1 : 2) : ((kTileBytes == 32768) ? FA_PREFILL_STAGES_K128 : 5);
+  static constexpr int kStagesV =
+      (QT == 1) ? ((kTileBytes == 32768) ? 1 : 2) : ((kTileBytes == 32768) ? FA_PREFILL_STAGES_V128 : 5);
   static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kPrefillQTiles * kTileBytes;
+  static constexpr int kK = kQ + QT * kTileBytes;
   static constexpr int kV = kK + kStagesK * kTileBytes;
   static constexpr int kBar = kV + kStagesV * kTileBytes;
   // q_full, k_full[SK], k_empty[SK], v_full[SV], s_full[2], p_full[2],
@@ -64,8 +68,8 @@ struct PrefillLayout {
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kSmemAlloc = kBytes + 1024;     // base is aligned up to 1024 in-kernel
-  static constexpr uint32_t kTmemCols = 512;
-  static constexpr int kTmemO = 256;
+  static constexpr uint32_t kTmemCols = QT * 256;
+  static constexpr int kTmemO = QT * 128;
 };
 
 // Work item `lin` of the padding-free order of a packed batch: sequences in
@@ -75,6 +79,7 @@ struct PrefillLayout {
 // grid needs no item per (sequence, pair) that has no rows.  Every warp
 // finds its item with one pass over cu_seqlens, 32 sequences at a time
 // (all lanes active).  Returns false past the last item.
+template <int ROWS>
 __device__ __forceinline__ bool varlen_compact_item(const PrefillParams &p, int lin, bool causal,
                                                     int &unit, int &pair, int &h) {
   const int lane = threadIdx.x & 31;
@@ -92,7 +97,7 @@ __device__ __forceinline__ bool varlen_compact_item(const PrefillParams &p, int 
     if (s < p.B) {
       const int a = p.cu_seqlens[s], e = p.cu_seqlens[s + 1];
       const int n = min(max(e - a, 0), p.total_tokens);
-      np = (n + kPrefillRowsPerCta - 1) / kPrefillRowsPerCta;
+      np = (n + ROWS - 1) / ROWS;
     }
     const int mine = np * p.H;  // items of sequence s
     int incl = mine;
@@ -120,14 +125,15 @@ __device__ __forceinline__ bool varlen_compact_item(const PrefillParams &p, int 
 
 // KIND: dense batch, packed varlen batch, or packed queries over a paged KV
 // cache (chunked prefill).
-template <int D, bool CAUSAL, int KIND, bool FP8 = false>
-__global__ void __launch_bounds__(kPrefillThreads, 1)
+template <int D, bool CAUSAL, int KIND, bool FP8 = false, int QT = 2>
+__global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::kMinBlocks)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v,
                    const __grid_constant__ CUtensorMap tm_v1,
                    const __grid_constant__ CUtensorMap tm_o, const PrefillParams p) {
-  using L = PrefillLayout<D, FP8>;
+  using L = PrefillLayout<D, FP8, QT>;
+  using Sh = PrefillShape<QT>;
   constexpr int SK = L::kStagesK;
   constexpr int SV = L::kStagesV;
 
@@ -144,7 +150,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                                             : static_cast<int>(blockIdx.x);
   int h, unit, pair;  // unit: batch element or sequence
   if (KIND == kKindVarlen && p.compact) {
-    if (!varlen_compact_item(p, lin, CAUSAL, unit, pair, h)) return;  // past the last item
+    if (!varlen_compact_item<Sh::kRows>(p, lin, CAUSAL, unit, pair, h)) return;  // past the last item
   } else {
     const int hgs = p.head_group;
     const int h_in = lin % hgs;
@@ -173,7 +179,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       return;
     }
     len = seq_end - seq_start;
-    if (len > p.max_pairs * kPrefillRowsPerCta && pair == 0 && h == 0)
+    if (len > p.max_pairs * Sh::kRows && pair == 0 && h == 0)
       raise_status(p.status, FA_DEV_BAD_SEQLEN);  // longer than max_seqlen (the padded order
                                                   // misses its tail)
     b = 0;
@@ -190,7 +196,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       offset = kv_len - len;
     }
   }
-  const int row0 = pair * kPrefillRowsPerCta;
+  const int row0 = pair * Sh::kRows;
   if (row0 >= len) return;  // no padding work: the whole CTA leaves before any set-up
 
   const int n_kv_all = (kv_len + kPrefillBN - 1) / kPrefillBN;
@@ -198,7 +204,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
   for (int i = 0; i < kPrefillQTiles; ++i) {
     const int t0 = row0 + i * kPrefillBM;
-    if (t0 >= len) {
+    if (i >= QT || t0 >= len) {
       kv_end[i] = 0;
     } else {
       int e = n_kv_all;
@@ -223,7 +229,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     for (int i = 0; i < kPrefillQTiles; ++i) kv_end[i] = max(0, min(kv_end[i], stop) - kv0);
   }
   const int n_kv = max(kv_end[0], kv_end[1]);
-  const bool live1 = row0 + kPrefillBM < len;  // the second query tile has rows
+  const bool live1 = QT == 2 && row0 + kPrefillBM < len;  // the second query tile has rows
 
   // ---------------------------------------------------------- shared memory
   extern __shared__ uint8_t smem_raw[];
@@ -251,7 +257,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   // Dense kinds: K(0) is copied with Q, before the block-wide set-up ends.
   const bool k0_early = (KIND != kKindPaged) && n_kv > 0;
 
-  if (warp == 9 && lane == 0) {
+  if (warp == Sh::kTmaWarp && lane == 0) {
     // The producer thread initialises the barriers and starts the Q copies
     // (and K(0)) right away; the other warps wait for it at __syncthreads.
     mbar_init(q_full, 1);
@@ -292,7 +298,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                     seq_start + kv0 * kPrefillBN, b);
     }
   }
-  if (warp == 8) {
+  if (warp == Sh::kMmaWarp) {
     tmem_alloc(tmem_slot, L::kTmemCols);
     tmem_relinquish();
   }
@@ -300,7 +306,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     // Rows of a V stage that no load fills (keys past the context in the last
     // key tile) must hold finite values: P is 0 there, but 0 * NaN is NaN.
     uint4 *z = reinterpret_cast<uint4 *>(smem + L::kV);
-    for (int t = threadIdx.x; t < SV * L::kTileBytes / 16; t += kPrefillThreads)
+    for (int t = threadIdx.x; t < SV * L::kTileBytes / 16; t += Sh::kThreads)
       z[t] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
   }
@@ -309,7 +315,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 9 && KIND == kKindPaged) {
+  if (warp >= Sh::kSoftmaxWarps) {
+  // One query tile per CTA: this warpgroup (MMA, TMA, two idle warps) hands
+  // registers to the softmax warpgroup.
+  if constexpr (QT == 1) setmaxnreg_dec<kPrefill1CtlRegs>();
+  if (warp == Sh::kTmaWarp && KIND == kKindPaged) {
     // ------------------------------------------------------ TMA producer, paged
     // The warp runs converged: lanes 0..7 look up the 8 physical blocks of a
     // 128-key tile in the block table, lane 0 issues the copies.  A block
@@ -422,7 +432,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       for (int j = max(0, v_issued - SV); j < v_issued; ++j)
         mbar_drain(&v_full[j % SV], (j / SV) & 1, p.status);
     }
-  } else if (warp == 9) {
+  } else if (warp == Sh::kTmaWarp) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       // Issue order K(0) (already issued with Q), then V(j), K(j+1) for
@@ -467,7 +477,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       for (int j = max(0, v_issued - SV); j < v_issued; ++j)
         mbar_drain(&v_full[j % SV], (j / SV) & 1, p.status);
     }
-  } else if (warp == 8) {
+  } else if (warp == Sh::kMmaWarp) {
     // ------------------------------------------------------ MMA issuer
     // The whole warp runs this loop converged; elect.sync picks the lane
     // that issues each tcgen05 instruction.
@@ -555,7 +565,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         // paged K may still be in flight, so that kind waits for K(j+1)
         // only before the S MMAs that read it.
         if (!mbar_wait_warp(&v_full[sv], (j / SV) & 1, abort_flag, p.status)) break;
-        if (KIND != kKindPaged && j + 1 < n_kv && !wait_k_next()) break;
+        if (KIND != kKindPaged && SK > 1 && j + 1 < n_kv && !wait_k_next()) break;
         tc_fence_after();
         if (j < kv_end[0]) {
           if (!mbar_wait_warp(&p_full[0], j & 1, abort_flag, p.status)) break;
@@ -586,7 +596,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       mma_commit_elect(drain);
       mbar_drain(drain, 0, p.status);
     }
+  }
   } else {
+    if constexpr (QT == 1) setmaxnreg_inc<kPrefill1SoftmaxRegs>();
     // ------------------------------------------------------ softmax warpgroups
     const int i = warp >> 2;
     const int quad = warp & 3;
@@ -851,7 +863,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == Sh::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
   }
@@ -916,27 +928,38 @@ cudaError_t launch_prefill_split_combine(const PrefillParams &p, int d, cudaStre
 
 // ------------------------------------------------------------------ launch
 
-template <int D, bool CAUSAL, int KIND, bool FP8 = false>
+template <int D, bool CAUSAL, int KIND, bool FP8 = false, int QT = 2>
 static cudaError_t launch_prefill_t(const CUtensorMap &tq, const CUtensorMap &tk,
                                     const CUtensorMap &tv, const CUtensorMap &tv1,
                                     const CUtensorMap &to, const PrefillParams &p, int grid,
                                     cudaStream_t stream) {
-  using L = PrefillLayout<D, FP8>;
-  auto kern = prefill_kernel<D, CAUSAL, KIND, FP8>;
+  using L = PrefillLayout<D, FP8, QT>;
+  using Sh = PrefillShape<QT>;
+  auto kern = prefill_kernel<D, CAUSAL, KIND, FP8, QT>;
+  if constexpr (QT == 1) {
+    // The setmaxnreg split assumes kPrefill1LaunchRegs registers per thread
+    // at launch; with fewer, the register increase could never be granted,
+    // so such a build is refused instead of launched.
+    static const int launch_regs = [&] {
+      cudaFuncAttributes a{};
+      return cudaFuncGetAttributes(&a, kern) == cudaSuccess ? a.numRegs : -1;
+    }();
+    if (launch_regs != kPrefill1LaunchRegs) return cudaErrorInvalidKernelImage;
+  }
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kPrefillThreads, L::kSmemAlloc, stream>>>(tq, tk, tv, tv1, to, p);
+  kern<<<grid, Sh::kThreads, L::kSmemAlloc, stream>>>(tq, tk, tv, tv1, to, p);
   return cudaGetLastError();
 }
 
-template <int D, int KIND>
+template <int D, int KIND, int QT = 2>
 static cudaError_t launch_prefill_k(const CUtensorMap &tq, const CUtensorMap &tk,
                                     const CUtensorMap &tv, const CUtensorMap &tv1,
                                     const CUtensorMap &to, const PrefillParams &p, bool causal,
                                     int grid, cudaStream_t stream) {
-  return causal ? launch_prefill_t<D, true, KIND>(tq, tk, tv, tv1, to, p, grid, stream)
-                : launch_prefill_t<D, false, KIND>(tq, tk, tv, tv1, to, p, grid, stream);
+  return causal ? launch_prefill_t<D, true, KIND, false, QT>(tq, tk, tv, tv1, to, p, grid, stream)
+                : launch_prefill_t<D, false, KIND, false, QT>(tq, tk, tv, tv1, to, p, grid, stream);
 }
 
 cudaError_t launch_prefill_fp8(const CUtensorMap &tq, const CUtensorMap &tk,
@@ -949,7 +972,11 @@ cudaError_t launch_prefill_fp8(const CUtensorMap &tq, const CUtensorMap &tk,
 
 cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                            const CUtensorMap &tv1, const CUtensorMap &to, const PrefillParams &p,
-                           int d, bool causal, int kind, int grid, cudaStream_t stream) {
+                           int d, bool causal, int kind, int grid, cudaStream_t stream,
+                           int qtiles) {
+  if (kind == kKindVarlen && qtiles == 1)
+    return d == 64 ? launch_prefill_k<64, kKindVarlen, 1>(tq, tk, tv, tv1, to, p, causal, grid, stream)
+                   : launch_prefill_k<128, kKindVarlen, 1>(tq, tk, tv, tv1, to, p, causal, grid, stream);
   if (d == 64) {
     if (kind == kKindDense)
       return launch_prefill_k<64, kKindDense>(tq, tk, tv, tv1, to, p, causal, grid, stream);

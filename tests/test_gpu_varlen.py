@@ -42,6 +42,20 @@ def test_varlen_ragged(fa, d, causal):
     assert_device_clean()
 
 
+@pytest.mark.parametrize("d,causal", [(128, True), (64, False)])
+def test_varlen_long_sequences(fa, d, causal):
+    """Batches of 4096 rows or more per sequence on average run two query
+    tiles per CTA (the shorter batches above run one): ragged long sequences
+    with GQA, every element against the oracle."""
+    lengths = [4100, 5000, 4300]
+    inp = W.varlen_inputs(lengths, 2, 1, d, seed=33)
+    out, lse = run_varlen(fa, inp, causal)
+    o_ref, l_ref = oracle.attention_varlen(f64(inp.q), f64(inp.k), f64(inp.v), inp.cu_seqlens,
+                                           causal=causal)
+    compare(out, o_ref, lse, l_ref, f"long varlen d{d} causal={causal}")
+    assert_device_clean()
+
+
 def test_varlen_config_sampled(fa):
     """Full-size packed batch (32 sequences, lengths U[64, 4096], GQA 16/4,
     d = 128, causal); the oracle evaluates every sequence for 2 seeded heads."""
