@@ -16,8 +16,10 @@ Reported (one JSON line from rank 0):
   decode   HBM GB/s of the decode step (algorithmic bytes: K/V of every cached
            token, q, out, lse, ctx lengths and block-table entries)
   roofline / roofline_decode   the two kernels against the measured peaks
-  e2e      the same metrics with pinned-host inputs copied in and outputs
-           copied back inside the timed region
+  e2e      the same metrics with every step's inputs copied in from pinned
+           host memory and its results copied back inside the timed region;
+           the copies run on two copy streams against double-buffered device
+           tensors, so they overlap the neighbouring steps' kernels
   cpu_baseline  the fp64 oracle (NumPy) timed on the host cores on a bounded
            sample of the long-context workload
 
@@ -278,16 +280,64 @@ def _add_decode(legs, dec_in, cfg_d):
         Hkv=cfg_d["Hkv"])
 
 
-def run_leg(fa, name, leg, dev):
+def run_leg(fa, name, leg, dev, out=None, lse=None):
+    out = leg["out"] if out is None else out
+    lse = leg["lse"] if lse is None else lse
     if name == "long":
-        fa.fa_fwd(dev["q"], dev["k"], dev["v"], causal=True, out=leg["out"], lse=leg["lse"])
+        fa.fa_fwd(dev["q"], dev["k"], dev["v"], causal=True, out=out, lse=lse)
     elif name == "varlen":
         fa.fa_fwd_varlen(dev["q"], dev["k"], dev["v"], leg["cu_dev"], leg["max_seqlen"],
-                         causal=True, out=leg["out"], lse=leg["lse"])
+                         causal=True, out=out, lse=lse)
     else:
         fa.fa_decode_paged(dev["q"], dev["k_pool"], dev["v_pool"], leg["table_dev"],
-                           leg["ctx_dev"], leg["max_ctx"], out=leg["out"], lse=leg["lse"],
+                           leg["ctx_dev"], leg["max_ctx"], out=out, lse=lse,
                            workspace=leg["ws"])
+
+
+def e2e_pipelined(torch, fa, names, legs, pinned, host_out, steps):
+    """End-to-end time (ms) of `steps` steps over the legs `names`: every step
+    copies its inputs in from pinned host memory and reads its results back,
+    on two copy streams, with the device tensors double-buffered so that step
+    k+1's inputs arrive and step k-1's results leave while step k's kernels
+    run on the compute stream."""
+    comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    devs = {n: [legs[n]["dev"], {k: torch.empty_like(v) for k, v in legs[n]["dev"].items()}]
+            for n in names}
+    outs = {n: [(legs[n]["out"], legs[n]["lse"]),
+                (torch.empty_like(legs[n]["out"]), torch.empty_like(legs[n]["lse"]))]
+            for n in names}
+    in_done = {n: [None, None] for n in names}
+    comp_done = {n: [None, None] for n in names}
+    out_done = {n: [None, None] for n in names}
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(s_in)
+    for it in range(steps):
+        b = it % 2
+        for n in names:
+            with torch.cuda.stream(s_in):
+                if comp_done[n][b] is not None:       # step it-2 has read this input buffer
+                    s_in.wait_event(comp_done[n][b])
+                for k, t in pinned[n].items():
+                    devs[n][b][k].copy_(t, non_blocking=True)
+                in_done[n][b] = torch.cuda.Event()
+                in_done[n][b].record(s_in)
+            comp.wait_event(in_done[n][b])
+            if out_done[n][b] is not None:            # step it-2's results have left
+                comp.wait_event(out_done[n][b])
+            run_leg(fa, n, legs[n], devs[n][b], out=outs[n][b][0], lse=outs[n][b][1])
+            comp_done[n][b] = torch.cuda.Event()
+            comp_done[n][b].record(comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[n][b])
+                host_out[n][0].copy_(outs[n][b][0], non_blocking=True)
+                host_out[n][1].copy_(outs[n][b][1], non_blocking=True)
+                out_done[n][b] = torch.cuda.Event()
+                out_done[n][b].record(s_out)
+    t1.record(s_out)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1)
 
 
 def measure_paged_prefill(torch, device, fa, steps, warmup, peak):
@@ -618,25 +668,13 @@ def bench_ours(args, rank, world, local):
     h2d = sum(t.numel() * t.element_size() for n in order for t in pinned[n].values())
     d2h = sum(o.numel() * o.element_size() + l.numel() * l.element_size()
               for o, l in host_out.values())
-    e2e_steps = max(1, min(args.steps, 10))
-    e2e_ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in order]
-              for _ in range(e2e_steps)]
+    e2e_steps = max(2, min(args.steps, 10))
+    pre = [n for n in ("long", "varlen") if n in order]
     barrier(world)
-    torch.cuda.synchronize()
-    for it in range(e2e_steps):
-        for i, name in enumerate(order):
-            leg = legs[name]
-            e2e_ev[it][i][0].record(stream)
-            for k, t in pinned[name].items():
-                leg["dev"][k].copy_(t, non_blocking=True)
-            run_leg(fa, name, leg, leg["dev"])
-            host_out[name][0].copy_(leg["out"], non_blocking=True)
-            host_out[name][1].copy_(leg["lse"], non_blocking=True)
-            e2e_ev[it][i][1].record(stream)
-    torch.cuda.synchronize()
+    e2e_pre_ms = e2e_pipelined(torch, fa, pre, legs, pinned, host_out, e2e_steps) if pre else None
+    e2e_dec_ms = (e2e_pipelined(torch, fa, ["decode"], legs, pinned, host_out, e2e_steps)
+                  if "decode" in order else None)
     barrier(world)
-    e2e_ms = {name: [e2e_ev[it][i][0].elapsed_time(e2e_ev[it][i][1]) for it in range(e2e_steps)]
-              for i, name in enumerate(order)}
 
     nxt = {}
     if args.next_legs and "long" in order:
@@ -649,17 +687,17 @@ def bench_ours(args, rank, world, local):
     # ---- numbers (max over ranks of each time)
     K = args.steps
     t = {n: max_over_ranks(sum(leg_ms[n]) / 1e3, world, device) for n in order}
-    te = {n: max_over_ranks(sum(e2e_ms[n]) / 1e3, world, device) for n in order}
+    te_pre = max_over_ranks(e2e_pre_ms / 1e3, world, device) if pre else None
+    te_dec = max_over_ranks(e2e_dec_ms / 1e3, world, device) if "decode" in order else None
     t_total = max_over_ranks(total_ms / 1e3, world, device)
-    pre = [n for n in ("long", "varlen") if n in order]
     f_pre = sum(legs[n]["flops"] for n in pre)
     prefill_tflops = (weak_scaling_value(f_pre * K, world, sum(t[n] for n in pre)) / 1e12
                       if pre else None)
-    e2e_tflops = (weak_scaling_value(f_pre * e2e_steps, world, sum(te[n] for n in pre)) / 1e12
+    e2e_tflops = (weak_scaling_value(f_pre * e2e_steps, world, te_pre) / 1e12
                   if pre else None)
     dbytes = legs["decode"]["bytes"] if "decode" in order else None
     decode_gbs = weak_scaling_value(dbytes * K, world, t["decode"]) / 1e9 if dbytes else None
-    e2e_gbs = weak_scaling_value(dbytes * e2e_steps, world, te["decode"]) / 1e9 if dbytes else None
+    e2e_gbs = weak_scaling_value(dbytes * e2e_steps, world, te_dec) / 1e9 if dbytes else None
 
     if rank != 0:
         return 0
@@ -726,7 +764,10 @@ def bench_ours(args, rank, world, local):
         "roofline": roof,
         "roofline_decode": roof_dec,
         "e2e": {"value": e2e_tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "decode_gbs": e2e_gbs, "steps": e2e_steps},
+                "d2h_bytes_per_step": d2h, "decode_gbs": e2e_gbs, "steps": e2e_steps,
+                "pipelined": "inputs of step k+1 copied in and results of step k-1 read back "
+                             "on two copy streams while step k runs (double-buffered device "
+                             "tensors)"},
         "next": nxt or None,
         "gpu_launches": sum(LAUNCHES_PER_STEP[n] for n in order) * K,
         "clocks": clk,
