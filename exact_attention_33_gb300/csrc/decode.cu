@@ -21,7 +21,7 @@
 // The work is bound by HBM reads of K and V; the tensor-core ops are a small
 // fraction of the issue slots.
 //
-// decode_combine_kernel: one warp per (sequence, query head) merges the
+// decode_combine_kernel: one CTA per (sequence, query head) merges the
 // partial states: M = max m_i, L = sum 2^(m_i - M) l_i,
 // o = sum 2^(m_i - M) o_i / L, lse = (M + log2 L) ln 2.
 #include <cuda.h>
@@ -309,10 +309,18 @@ __global__ void __launch_bounds__(32)
 template <int D>
 __global__ void __launch_bounds__(32 * kCombineWarps)
     decode_combine_kernel(const DecodeParams p) {
+  // One CTA per (sequence, query head): warp w merges splits w, w + W, ...
+  // (W = kCombineWarps), U of them per memory round trip, and the warps'
+  // sums are added through shared memory.  Lane l owns output elements
+  // [l E, l E + E).
+  constexpr int W = kCombineWarps;
+  constexpr int E = D / 32;
+  constexpr int U = 4;
+  __shared__ float s_acc[W][D];
+  __shared__ float s_l[W];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * kCombineWarps + warp;
-  if (gw >= p.batch * p.H) return;
+  const int gw = blockIdx.x;
   const int b = gw / p.H;
   int ctx = p.ctx_lens[b];
   if (ctx < 0 || ctx > p.max_ctx_len || ctx > p.max_blocks_per_seq * kDecodeBlock) ctx = 0;
@@ -325,30 +333,67 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
 
-  constexpr int E = D / 32;  // output elements per lane
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   float Lsum = 0.f;
+  // Split i adds 2^(m_i - M) (l_i, o_i).  An empty split (m_i = -inf) is
+  // passed over by a select, never multiplied in, so whatever its o_i slot
+  // holds cannot reach the output.
   if (M != -CUDART_INF_F) {
-    for (int i = 0; i < ns; ++i) {
-      const float2 st = ml[i];
-      if (st.x == -CUDART_INF_F) continue;  // empty split: contributes nothing
+    auto add = [&](const float2 st, const float (&v)[E]) {
+      const bool live = st.x != -CUDART_INF_F;
       const float w = ex2(st.x - M);
-      Lsum += w * st.y;
+      Lsum = live ? fmaf(w, st.y, Lsum) : Lsum;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = live ? fmaf(w, v[e], acc[e]) : acc[e];
+    };
+    auto load_o = [&](int i, float (&v)[E]) {
       const float *orow = p.o_part + (row0 + i) * D + lane * E;
-      if (E == 4) {
-        const float4 v = *reinterpret_cast<const float4 *>(orow);
-        acc[0] += w * v.x;
-        acc[1] += w * v.y;
-        acc[2 % E] += w * v.z;
-        acc[3 % E] += w * v.w;
+      if constexpr (E == 4) {
+        const float4 x = *reinterpret_cast<const float4 *>(orow);
+        v[0] = x.x;
+        v[1 % E] = x.y;
+        v[2 % E] = x.z;
+        v[3 % E] = x.w;
       } else {
-        const float2 v = *reinterpret_cast<const float2 *>(orow);
-        acc[0] += w * v.x;
-        acc[1 % E] += w * v.y;
+        const float2 x = *reinterpret_cast<const float2 *>(orow);
+        v[0] = x.x;
+        v[1 % E] = x.y;
       }
+    };
+    int i = warp;
+    for (; i + (U - 1) * W < ns; i += U * W) {
+      float2 st[U];
+      float v[U][E];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        st[u] = ml[i + u * W];
+        load_o(i + u * W, v[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) add(st[u], v[u]);
     }
+    for (; i < ns; i += W) {
+      float v[E];
+      load_o(i, v);
+      add(ml[i], v);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) s_acc[warp][lane * E + e] = acc[e];
+  if (lane == 0) s_l[warp] = Lsum;
+  __syncthreads();
+  if (warp != 0) return;
+  Lsum = 0.f;
+#pragma unroll
+  for (int w = 0; w < W; ++w) Lsum += s_l[w];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < W; ++w) t += s_acc[w][lane * E + e];
+    acc[e] = t;
   }
   const float inv = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
   uint16_t *dst = static_cast<uint16_t *>(p.out) + static_cast<size_t>(gw) * D + lane * E;
@@ -382,9 +427,7 @@ static cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv,
   kern<<<grid, 32, L::kSmemAlloc, stream>>>(tk, tv, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int warps = p.batch * p.H;
-  decode_combine_kernel<D><<<(warps + kCombineWarps - 1) / kCombineWarps, 32 * kCombineWarps, 0,
-                             stream>>>(p);
+  decode_combine_kernel<D><<<p.batch * p.H, 32 * kCombineWarps, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
