@@ -885,23 +885,49 @@ __global__ void __launch_bounds__(128) prefill_split_combine_kernel(const Prefil
   const int h = static_cast<int>(gw % p.H);
   const size_t stride = static_cast<size_t>(p.B) * p.N * p.H;  // between splits
   const float4 *ml = reinterpret_cast<const float4 *>(p.ml_part) + gw;
-  float M = -CUDART_INF_F;
-  for (int s = 0; s < p.num_splits; ++s) M = fmaxf(M, ml[s * stride].x);
+  // M = max over the splits, one split per lane (at most 16 splits)
+  float M = (lane < p.num_splits) ? ml[lane * stride].x : -CUDART_INF_F;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   constexpr int E = D / 32;
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   float Ls = 0.f, Le = 0.f;
+  // Split s adds 2^(m_s - M) (l_s, l_exact_s, o_s), four splits per memory
+  // round trip; a split without keys for this row (m_s = -inf) is passed
+  // over by a select, so its o_s slot never reaches the output.
   if (M != -CUDART_INF_F) {
-    for (int s = 0; s < p.num_splits; ++s) {
-      const float4 st = ml[s * stride];
-      if (st.x == -CUDART_INF_F) continue;  // a split without keys for this row
+    auto add = [&](const float4 st, const float (&v)[E]) {
+      const bool live = st.x != -CUDART_INF_F;
       const float w = ex2(st.x - M);
-      Ls += w * st.y;
-      Le += w * st.z;
-      const float *orow = p.o_part + (s * stride + gw) * D + lane * E;
+      Ls = live ? fmaf(w, st.y, Ls) : Ls;
+      Le = live ? fmaf(w, st.z, Le) : Le;
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] += w * orow[e];
+      for (int e = 0; e < E; ++e) acc[e] = live ? fmaf(w, v[e], acc[e]) : acc[e];
+    };
+    auto load_o = [&](int sp, float (&v)[E]) {
+      const float *orow = p.o_part + (sp * stride + gw) * D + lane * E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[e] = orow[e];
+    };
+    constexpr int U = 4;
+    int sp = 0;
+    for (; sp + U <= p.num_splits; sp += U) {
+      float4 st[U];
+      float v[U][E];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        st[u] = ml[(sp + u) * stride];
+        load_o(sp + u, v[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) add(st[u], v[u]);
+    }
+    for (; sp < p.num_splits; ++sp) {
+      float v[E];
+      load_o(sp, v);
+      add(ml[sp * stride], v);
     }
   }
   const float inv = (Ls > 0.f) ? 1.f / Ls : 0.f;
