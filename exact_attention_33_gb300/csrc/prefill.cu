@@ -24,6 +24,11 @@
 //
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256, 256+d), O_1 after it.
 // P_i (bf16, two per column) occupies the first 64 columns of S_i.
+//
+// With one query tile per CTA (template QT = 1, used for packed batches of
+// short sequences) the same roles run as warps 0-3 (softmax), 4 (MMA) and 5
+// (TMA) of 256 threads, with S_0 [0,128) and O_0 [128, 128+d) in 256 TMEM
+// columns and one K and one V stage at d = 128, so two CTAs share an SM.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
