@@ -56,6 +56,21 @@ def test_varlen_long_sequences(fa, d, causal):
     assert_device_clean()
 
 
+@pytest.mark.parametrize("num_seqs", [100, 150])
+def test_varlen_many_sequences(fa, num_seqs):
+    """More than 32 sequences: the padding-free order looks its item up over
+    several 32-sequence chunks (up to 128 sequences); beyond 128 the launch
+    uses the padded order, whose CTAs past a sequence's end leave at once.
+    Short ragged lengths (zero included), causal, GQA, every element."""
+    lengths = np.random.default_rng(34 + num_seqs).integers(0, 300, num_seqs)
+    inp = W.varlen_inputs(lengths, 4, 2, 64, seed=35)
+    out, lse = run_varlen(fa, inp, True)
+    o_ref, l_ref = oracle.attention_varlen(f64(inp.q), f64(inp.k), f64(inp.v), inp.cu_seqlens,
+                                           causal=True)
+    compare(out, o_ref, lse, l_ref, f"varlen {num_seqs} sequences")
+    assert_device_clean()
+
+
 def test_varlen_config_sampled(fa):
     """Full-size packed batch (32 sequences, lengths U[64, 4096], GQA 16/4,
     d = 128, causal); the oracle evaluates every sequence for 2 seeded heads."""
