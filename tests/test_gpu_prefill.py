@@ -84,6 +84,40 @@ def test_long_causal_config_sampled(fa, long_inputs):
     assert_device_clean()
 
 
+def dominant_key_inputs(N, H, d, pos, target_log2, seed):
+    """Query rows close to one direction u per head, and key `pos` equal to
+    c u with c chosen so that its scaled score is about `target_log2` (in
+    log2 units) above the typical row maximum: one key that dominates every
+    row and moves the reference maximum when its key tile arrives."""
+    rng = np.random.default_rng(seed)
+    u = rng.standard_normal((H, d)).astype(np.float32)
+    q = (u[None, None] + 0.1 * rng.standard_normal((1, N, H, d))).astype(np.float32)
+    k = rng.standard_normal((1, N, H, d)).astype(np.float32)
+    v = rng.standard_normal((1, N, H, d)).astype(np.float32)
+    c = target_log2 / (np.einsum("hd,hd->h", u, u) / math.sqrt(d) * math.log2(math.e))
+    k[0, pos] = u * c[:, None]
+    bits = W.f32_to_bf16_bits
+    return W.DenseInputs(1, N, H, H, d, bits(q), bits(k), bits(v))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("pos", [10, 300, 356, 600])
+@pytest.mark.parametrize("target_log2", [40.0, 200.0])
+def test_dominant_key_moves_the_reference(fa, d, pos, target_log2):
+    """A key far above the running maximum, in the first key tile (handled
+    by that tile's maximum), in the first or second 64-key half of a later
+    tile, and in the last tile.  At 40 (log2 units) its weight passes the
+    lazy re-centring bound but is kept for the tile; at 200 it overflows fp32
+    against the old reference, and the tile is redone (first half) or its
+    stored first half rescaled (second half).  Causal and not, every element."""
+    inp = dominant_key_inputs(640, 2, d, pos, target_log2, seed=41 + pos)
+    for causal in (False, True):
+        out, lse = run_dense(fa, inp, causal)
+        o_ref, l_ref = oracle.attention_dense(f64(inp.q), f64(inp.k), f64(inp.v), causal=causal)
+        compare(out, o_ref, lse, l_ref, f"dominant key d{d} pos {pos} {target_log2} causal={causal}")
+    assert_device_clean()
+
+
 def test_deterministic(fa):
     torch = torch_mod()
     inp = W.dense_inputs(2, 700, 4, 2, 128, seed=7)
