@@ -22,6 +22,9 @@ Reported (one JSON line from rank 0):
            tensors, so they overlap the neighbouring steps' kernels
   cpu_baseline  the fp64 oracle (NumPy) timed on the host cores on a bounded
            sample of the long-context workload
+  next     the further rows (chunked prefill over a paged cache, split-KV
+           prefill, FP8 prefill, the backward pass), each on its own workload
+  other_configs  the dense d = 64 configuration (B4 H16 N2048), causal and not
 
 ``--impl reference`` times the oracle instead (the slow reference arm).
 Multi-GPU: one process per GPU (torchrun); every rank runs the full step on
@@ -492,6 +495,40 @@ def measure_splitkv(torch, device, fa, steps, warmup, peak):
             "launches_per_call": 2}
 
 
+def measure_dense_d64(torch, device, fa, steps, warmup):
+    """The dense configuration of the workload list (B=4, H=Hkv=16, N=2048,
+    d=64, bf16 N(0,1)), non-causal and causal.  Its inputs fit in L2, so L2
+    is flushed (a 256 MiB write) before every timed launch and only the
+    launch is timed."""
+    cfg = W.WORKLOADS["dense_d64"]
+    B, N, H, Hkv, d = cfg["B"], cfg["N"], cfg["H"], cfg["Hkv"], cfg["d"]
+    inp = W.dense_inputs(B, N, H, Hkv, d, seed=0)
+    q, k, v = (to_dev(getattr(inp, n), torch, device) for n in ("q", "k", "v"))
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+    res = {"workload": "dense prefill B4 H16 N2048 d64 (L2 flushed before each launch)"}
+    for causal in (False, True):
+        for _ in range(warmup):
+            fa.fa_fwd(q, k, v, causal=causal, out=out, lse=lse)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            fa.fa_fwd(q, k, v, causal=causal, out=out, lse=lse)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
+        flops = W.prefill_flops(B, N, H, d, causal)
+        res["causal" if causal else "non_causal"] = {"ms": ms, "tflops": flops / (ms / 1e3) / 1e12,
+                                                     "flops": flops}
+    if fa.fa_device_status(clear=True) != 0:
+        raise RuntimeError("device status word set during the dense d64 leg")
+    return res
+
+
 NEXT_LEGS = ("paged_prefill", "splitkv", "fp8_prefill", "backward")
 
 
@@ -677,12 +714,15 @@ def bench_ours(args, rank, world, local):
     barrier(world)
 
     nxt = {}
+    other = {}
     if args.next_legs and "long" in order:
         peaks0 = measured_peaks()
         for name in NEXT_LEGS:
             nxt[name] = run_next_leg(name, torch, device, fa,
                                      min(args.steps, 20 if name == "backward" else 50),
                                      args.warmup, peaks0["bf16_tflops"])
+        other["dense_d64"] = measure_dense_d64(torch, device, fa, min(args.steps, 50),
+                                               args.warmup)
 
     # ---- numbers (max over ranks of each time)
     K = args.steps
@@ -769,6 +809,7 @@ def bench_ours(args, rank, world, local):
                              "on two copy streams while step k runs (double-buffered device "
                              "tensors)"},
         "next": nxt or None,
+        "other_configs": other or None,
         "gpu_launches": sum(LAUNCHES_PER_STEP[n] for n in order) * K,
         "clocks": clk,
         "cpu_baseline": cpu,
