@@ -141,11 +141,14 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
   const long long gr = static_cast<long long>(blockIdx.x) * (256 / TPR) + threadIdx.x / TPR;
   const long long total = static_cast<long long>(p.B) * p.Npad * p.H;
   if (gr >= total) return;  // whole row groups leave together (TPR divides 32)
-  const int h = static_cast<int>(gr % p.H);
-  const long long bn = gr / p.H;
-  const int row = static_cast<int>(bn % p.Npad);
-  const int b = static_cast<int>(bn / p.Npad);
-  const size_t vec = (static_cast<size_t>(b) * p.H + h) * p.Npad + row;
+  // Row groups run over the rows of one (b, h) first, so that the lse reads
+  // and the D / lse2 writes of a warp are contiguous; each row's O and dO
+  // are still read as whole 16-byte chunks.
+  const int row = static_cast<int>(gr % p.Npad);
+  const long long bh = gr / p.Npad;
+  const int h = static_cast<int>(bh % p.H);
+  const int b = static_cast<int>(bh / p.H);
+  const size_t vec = static_cast<size_t>(gr);  // (b * H + h) * Npad + row
   float acc = 0.f;
   if (row < p.N) {
     const size_t off = ((static_cast<size_t>(b) * p.N + row) * p.H + h) * D + sub * 8;
