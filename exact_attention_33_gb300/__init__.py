@@ -6,9 +6,11 @@ the returned status; all arithmetic runs in the library's CUDA kernels.  There
 is no fallback: if ``libfa.so`` is missing or a call fails, an exception is
 raised.
 
-Functions keep the C names: :func:`fa_fwd`, :func:`fa_fwd_varlen`,
-:func:`fa_decode_paged`, :func:`fa_decode_workspace_size`,
-:func:`fa_status_string`, :func:`fa_device_status`.
+Functions keep the C names (see ``__all__``).  Every tensor a call touches,
+inputs, caller-supplied outputs and workspaces alike, is checked for device,
+dtype, shape and contiguity before the library is called, since the kernels
+trust the sizes they are given.  A call runs on the device of its ``q`` and
+on that device's current stream unless ``stream`` is given.
 """
 
 from __future__ import annotations
@@ -136,9 +138,9 @@ def _torch():
     return torch
 
 
-def _stream_handle(stream=None):
+def _stream_handle(stream=None, device=None):
     torch = _torch()
-    s = torch.cuda.current_stream() if stream is None else stream
+    s = torch.cuda.current_stream(device) if stream is None else stream
     return ctypes.c_void_p(int(s.cuda_stream))
 
 
@@ -146,14 +148,62 @@ def _ptr(t):
     return ctypes.c_void_p(0 if t is None else int(t.data_ptr()))
 
 
-def _check_bf16_cuda(name, t, ndim):
+def _check_bf16_cuda(name, t, ndim, device=None):
     torch = _torch()
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}")
     if t.dtype != torch.bfloat16:
         raise ValueError(f"{name} must be bfloat16")
     if t.dim() != ndim or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous {ndim}-D tensor")
+
+
+def _check_tensor(name, t, shape, dtype, device):
+    """A tensor the kernels read or write with exactly this shape and dtype."""
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or t.device != device:
+        raise ValueError(f"{name} must be a CUDA tensor on {device}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}")
+    if tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous tensor of shape {tuple(shape)}")
+
+
+def _check_int32(name, t, device, ndim=1, numel=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or t.device != device:
+        raise ValueError(f"{name} must be a CUDA tensor on {device}")
+    if t.dtype != torch.int32 or t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-D int32 tensor")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} must hold {numel} values")
+
+
+def _workspace(t, need, device, minimum=1):
+    """The caller's workspace (a 1-D uint8 tensor, its length in bytes), or a
+    new one of at least ``need`` bytes."""
+    torch = _torch()
+    if t is None:
+        return torch.empty(max(need, minimum), dtype=torch.uint8, device=device)
+    if not isinstance(t, torch.Tensor) or t.device != device or t.dtype != torch.uint8 \
+            or t.dim() != 1 or not t.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous 1-D uint8 tensor on {device}")
+    return t
+
+
+def _outputs(q_like_shape, lse_shape, out, lse, want_lse, device):
+    torch = _torch()
+    if out is None:
+        out = torch.empty(q_like_shape, dtype=torch.bfloat16, device=device)
+    else:
+        _check_tensor("out", out, q_like_shape, torch.bfloat16, device)
+    if lse is None and want_lse:
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=device)
+    elif lse is not None:
+        _check_tensor("lse", lse, lse_shape, torch.float32, device)
+    return out, lse
 
 
 def _scale(scale, d):
@@ -168,18 +218,19 @@ def fa_fwd(q, k, v, causal=False, scale=None, out=None, lse=None, want_lse=True,
     Returns (out [B,N,H,d] bf16, lse [B,H,N] fp32 or None).
     """
     torch = _torch()
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        _check_bf16_cuda(name, t, 4)
+    _check_bf16_cuda("q", q, 4)
+    dev = q.device
+    for name, t in (("k", k), ("v", v)):
+        _check_bf16_cuda(name, t, 4, dev)
     B, N, H, d = q.shape
     Hkv = k.shape[2]
     if k.shape != (B, N, Hkv, d) or v.shape != k.shape:
         raise ValueError("k and v must be [B, N, Hkv, d] matching q")
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None and want_lse:
-        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    rc = load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, N, d,
-                               _scale(scale, d), 1 if causal else 0, _stream_handle(stream))
+    out, lse = _outputs(q.shape, (B, H, N), out, lse, want_lse, dev)
+    with torch.cuda.device(dev):
+        rc = load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv,
+                                   N, d, _scale(scale, d), 1 if causal else 0,
+                                   _stream_handle(stream, dev))
     if rc != FA_OK:
         raise FaError("fa_fwd", rc)
     return out, lse
@@ -194,25 +245,30 @@ def fa_bwd(q, k, v, out, lse, dout, causal=False, scale=None, dq=None, dk=None, 
     """Gradient of dense attention.  q, out, dout [B,N,H,d]; k, v [B,N,Hkv,d]
     bf16 CUDA tensors; lse [B,H,N] fp32 from fa_fwd.  Returns (dq, dk, dv)."""
     torch = _torch()
-    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
-        _check_bf16_cuda(name, t, 4)
+    _check_bf16_cuda("q", q, 4)
+    dev = q.device
+    for name, t in (("k", k), ("v", v), ("out", out), ("dout", dout)):
+        _check_bf16_cuda(name, t, 4, dev)
     B, N, H, d = q.shape
     Hkv = k.shape[2]
     if k.shape != (B, N, Hkv, d) or v.shape != k.shape or out.shape != q.shape \
             or dout.shape != q.shape:
         raise ValueError("shapes must be q/out/dout [B,N,H,d], k/v [B,N,Hkv,d]")
-    if not lse.is_cuda or lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N):
-        raise ValueError("lse must be a [B,H,N] fp32 CUDA tensor")
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    need = fa_bwd_workspace_size(B, H, N)
-    if workspace is None:
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    rc = load_library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
-                               _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, N, d, _scale(scale, d),
-                               1 if causal else 0, _ptr(workspace), workspace.numel(),
-                               _stream_handle(stream))
+    _check_tensor("lse", lse, (B, H, N), torch.float32, dev)
+    grads = []
+    for name, g, like in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        if g is None:
+            g = torch.empty_like(like)
+        else:
+            _check_tensor(name, g, like.shape, torch.bfloat16, dev)
+        grads.append(g)
+    dq, dk, dv = grads
+    workspace = _workspace(workspace, fa_bwd_workspace_size(B, H, N), dev)
+    with torch.cuda.device(dev):
+        rc = load_library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, N, d,
+                                   _scale(scale, d), 1 if causal else 0, _ptr(workspace),
+                                   workspace.numel(), _stream_handle(stream, dev))
     if rc != FA_OK:
         raise FaError("fa_bwd", rc)
     return dq, dk, dv
@@ -223,19 +279,23 @@ def fa_fwd_fp8(q, k, v, q_descale, k_descale, v_descale, causal=False, scale=Non
     """Dense prefill on e4m3 codes.  q [B,N,H,d], k/v [B,N,Hkv,d] uint8 CUDA
     tensors holding e4m3 bits; per-tensor descales.  Returns (out bf16, lse)."""
     torch = _torch()
+    dev = q.device if isinstance(q, torch.Tensor) else None
     for name, t in (("q", q), ("k", k), ("v", v)):
-        if not t.is_cuda or t.dtype not in (torch.uint8, torch.float8_e4m3fn) or t.dim() != 4 \
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.device != dev \
+                or t.dtype not in (torch.uint8, torch.float8_e4m3fn) or t.dim() != 4 \
                 or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous 4-D uint8/e4m3 CUDA tensor")
+            raise ValueError(f"{name} must be a contiguous 4-D uint8/e4m3 CUDA tensor on the "
+                             "device of q")
     B, N, H, d = q.shape
     Hkv = k.shape[2]
-    if out is None:
-        out = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=q.device)
-    if lse is None and want_lse:
-        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    rc = load_library().fa_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv,
-                                   N, d, _scale(scale, d), float(q_descale), float(k_descale),
-                                   float(v_descale), 1 if causal else 0, _stream_handle(stream))
+    if k.shape != (B, N, Hkv, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, N, Hkv, d] matching q")
+    out, lse = _outputs((B, N, H, d), (B, H, N), out, lse, want_lse, dev)
+    with torch.cuda.device(dev):
+        rc = load_library().fa_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H,
+                                       Hkv, N, d, _scale(scale, d), float(q_descale),
+                                       float(k_descale), float(v_descale), 1 if causal else 0,
+                                       _stream_handle(stream, dev))
     if rc != FA_OK:
         raise FaError("fa_fwd_fp8", rc)
     return out, lse
@@ -250,23 +310,22 @@ def fa_fwd_splitkv(q, k, v, causal=False, scale=None, num_splits=0, out=None, ls
     """Dense prefill with split-KV partial states and a combine (for small
     B * H).  Same layouts as :func:`fa_fwd`."""
     torch = _torch()
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        _check_bf16_cuda(name, t, 4)
+    _check_bf16_cuda("q", q, 4)
+    dev = q.device
+    for name, t in (("k", k), ("v", v)):
+        _check_bf16_cuda(name, t, 4, dev)
     B, N, H, d = q.shape
     Hkv = k.shape[2]
     if k.shape != (B, N, Hkv, d) or v.shape != k.shape:
         raise ValueError("k and v must be [B, N, Hkv, d] matching q")
-    need = fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits)
-    if workspace is None:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None and want_lse:
-        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    rc = load_library().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H,
-                                       Hkv, N, d, _scale(scale, d), 1 if causal else 0,
-                                       int(num_splits), _ptr(workspace), workspace.numel(),
-                                       _stream_handle(stream))
+    workspace = _workspace(workspace, fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits),
+                           dev, 256)
+    out, lse = _outputs(q.shape, (B, H, N), out, lse, want_lse, dev)
+    with torch.cuda.device(dev):
+        rc = load_library().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B,
+                                           H, Hkv, N, d, _scale(scale, d), 1 if causal else 0,
+                                           int(num_splits), _ptr(workspace), workspace.numel(),
+                                           _stream_handle(stream, dev))
     if rc != FA_OK:
         raise FaError("fa_fwd_splitkv", rc)
     return out, lse
@@ -279,23 +338,34 @@ def fa_fwd_varlen(q, k, v, cu_seqlens, max_seqlen, causal=False, scale=None, out
     Returns (out [T,H,d] bf16, lse [H,T] fp32 or None).
     """
     torch = _torch()
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        _check_bf16_cuda(name, t, 3)
-    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
-        raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
+    _check_bf16_cuda("q", q, 3)
+    dev = q.device
+    for name, t in (("k", k), ("v", v)):
+        _check_bf16_cuda(name, t, 3, dev)
+    _check_int32("cu_seqlens", cu_seqlens, dev)
+    if cu_seqlens.numel() < 1:
+        raise ValueError("cu_seqlens must hold num_seqs + 1 offsets")
     T, H, d = q.shape
     Hkv = k.shape[1]
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None and want_lse:
-        lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
-    rc = load_library().fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
-                                      _ptr(cu_seqlens), cu_seqlens.numel() - 1, T,
-                                      int(max_seqlen), H, Hkv, d, _scale(scale, d),
-                                      1 if causal else 0, _stream_handle(stream))
+    if k.shape != (T, Hkv, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [T, Hkv, d] matching q")
+    out, lse = _outputs(q.shape, (H, T), out, lse, want_lse, dev)
+    with torch.cuda.device(dev):
+        rc = load_library().fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                          _ptr(cu_seqlens), cu_seqlens.numel() - 1, T,
+                                          int(max_seqlen), H, Hkv, d, _scale(scale, d),
+                                          1 if causal else 0, _stream_handle(stream, dev))
     if rc != FA_OK:
         raise FaError("fa_fwd_varlen", rc)
     return out, lse
+
+
+def _check_pools(k_pool, v_pool, dev):
+    _check_bf16_cuda("k_pool", k_pool, 4, dev)
+    _check_bf16_cuda("v_pool", v_pool, 4, dev)
+    if v_pool.shape != k_pool.shape:
+        raise ValueError("k_pool and v_pool must have the same shape [num_blocks,16,Hkv,d]")
+    return k_pool.shape
 
 
 def fa_fwd_paged(q, k_pool, v_pool, block_table, ctx_lens, cu_seqlens_q, max_seqlen_q,
@@ -309,23 +379,22 @@ def fa_fwd_paged(q, k_pool, v_pool, block_table, ctx_lens, cu_seqlens_q, max_seq
     """
     torch = _torch()
     _check_bf16_cuda("q", q, 3)
-    _check_bf16_cuda("k_pool", k_pool, 4)
-    _check_bf16_cuda("v_pool", v_pool, 4)
-    for name, t in (("block_table", block_table), ("ctx_lens", ctx_lens),
-                    ("cu_seqlens_q", cu_seqlens_q)):
-        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    dev = q.device
+    num_blocks, block_size, Hkv, dp = _check_pools(k_pool, v_pool, dev)
+    _check_int32("block_table", block_table, dev, ndim=2)
+    batch = block_table.shape[0]
+    _check_int32("ctx_lens", ctx_lens, dev, numel=batch)
+    _check_int32("cu_seqlens_q", cu_seqlens_q, dev, numel=batch + 1)
     Tq, H, d = q.shape
-    num_blocks, block_size, Hkv, _ = k_pool.shape
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None and want_lse:
-        lse = torch.empty((H, Tq), dtype=torch.float32, device=q.device)
-    rc = load_library().fa_fwd_paged(
-        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), block_table.shape[1],
-        _ptr(ctx_lens), _ptr(cu_seqlens_q), cu_seqlens_q.numel() - 1, Tq, int(max_seqlen_q),
-        int(max_ctx_len), H, Hkv, d, block_size, num_blocks, _scale(scale, d),
-        1 if causal else 0, _ptr(out), _ptr(lse), _stream_handle(stream))
+    if dp != d:
+        raise ValueError("the pools' head size must match q")
+    out, lse = _outputs(q.shape, (H, Tq), out, lse, want_lse, dev)
+    with torch.cuda.device(dev):
+        rc = load_library().fa_fwd_paged(
+            _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), block_table.shape[1],
+            _ptr(ctx_lens), _ptr(cu_seqlens_q), batch, Tq, int(max_seqlen_q),
+            int(max_ctx_len), H, Hkv, d, block_size, num_blocks, _scale(scale, d),
+            1 if causal else 0, _ptr(out), _ptr(lse), _stream_handle(stream, dev))
     if rc != FA_OK:
         raise FaError("fa_fwd_paged", rc)
     return out, lse
@@ -334,6 +403,20 @@ def fa_fwd_paged(q, k_pool, v_pool, block_table, ctx_lens, cu_seqlens_q, max_seq
 def fa_decode_workspace_size(batch, H, Hkv, d, max_ctx_len, block_size=16) -> int:
     return int(load_library().fa_decode_workspace_size(batch, H, Hkv, d, max_ctx_len,
                                                        block_size))
+
+
+def _decode_args(q, k_pool, v_pool, block_table, ctx_lens):
+    _check_bf16_cuda("q", q, 3)
+    dev = q.device
+    num_blocks, block_size, Hkv, dp = _check_pools(k_pool, v_pool, dev)
+    batch, H, d = q.shape
+    if dp != d:
+        raise ValueError("the pools' head size must match q")
+    _check_int32("block_table", block_table, dev, ndim=2)
+    if block_table.shape[0] != batch:
+        raise ValueError("block_table must have one row per sequence of q")
+    _check_int32("ctx_lens", ctx_lens, dev, numel=batch)
+    return dev, batch, H, Hkv, d, num_blocks, block_size
 
 
 def fa_decode_paged(q, k_pool, v_pool, block_table, ctx_lens, max_ctx_len, scale=None,
@@ -345,26 +428,17 @@ def fa_decode_paged(q, k_pool, v_pool, block_table, ctx_lens, max_ctx_len, scale
     Returns (out [batch,H,d] bf16, lse [batch,H] fp32 or None).
     """
     torch = _torch()
-    _check_bf16_cuda("q", q, 3)
-    _check_bf16_cuda("k_pool", k_pool, 4)
-    _check_bf16_cuda("v_pool", v_pool, 4)
-    for name, t in (("block_table", block_table), ("ctx_lens", ctx_lens)):
-        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
-    batch, H, d = q.shape
-    num_blocks, block_size, Hkv, _ = k_pool.shape
-    need = fa_decode_workspace_size(batch, H, Hkv, d, max_ctx_len, block_size)
-    if workspace is None:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None and want_lse:
-        lse = torch.empty((batch, H), dtype=torch.float32, device=q.device)
-    rc = load_library().fa_decode_paged(
-        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), block_table.shape[1],
-        _ptr(ctx_lens), int(max_ctx_len), batch, H, Hkv, d, block_size, num_blocks,
-        _scale(scale, d), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
-        _stream_handle(stream))
+    dev, batch, H, Hkv, d, num_blocks, block_size = _decode_args(q, k_pool, v_pool,
+                                                                 block_table, ctx_lens)
+    workspace = _workspace(
+        workspace, fa_decode_workspace_size(batch, H, Hkv, d, max_ctx_len, block_size), dev, 256)
+    out, lse = _outputs(q.shape, (batch, H), out, lse, want_lse, dev)
+    with torch.cuda.device(dev):
+        rc = load_library().fa_decode_paged(
+            _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), block_table.shape[1],
+            _ptr(ctx_lens), int(max_ctx_len), batch, H, Hkv, d, block_size, num_blocks,
+            _scale(scale, d), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+            _stream_handle(stream, dev))
     if rc != FA_OK:
         raise FaError("fa_decode_paged", rc)
     return out, lse
@@ -382,12 +456,17 @@ def fa_decode_paged_noalloc(q, k_pool, v_pool, block_table, ctx_lens, max_ctx_le
     static scratch array of FA_DECODE_NOALLOC_SCRATCH_BYTES; larger requests
     are rejected.  The caller passes ``out`` (and optionally ``lse``); calls
     whose kernels overlap on the GPU race on the shared scratch."""
-    batch, H, d = q.shape
-    num_blocks, block_size, Hkv, _ = k_pool.shape
-    rc = load_library().fa_decode_paged_noalloc(
-        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), block_table.shape[1],
-        _ptr(ctx_lens), int(max_ctx_len), batch, H, Hkv, d, block_size, num_blocks,
-        _scale(scale, d), _ptr(out), _ptr(lse), _stream_handle(stream))
+    torch = _torch()
+    dev, batch, H, Hkv, d, num_blocks, block_size = _decode_args(q, k_pool, v_pool,
+                                                                 block_table, ctx_lens)
+    _check_tensor("out", out, q.shape, torch.bfloat16, dev)
+    if lse is not None:
+        _check_tensor("lse", lse, (batch, H), torch.float32, dev)
+    with torch.cuda.device(dev):
+        rc = load_library().fa_decode_paged_noalloc(
+            _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), block_table.shape[1],
+            _ptr(ctx_lens), int(max_ctx_len), batch, H, Hkv, d, block_size, num_blocks,
+            _scale(scale, d), _ptr(out), _ptr(lse), _stream_handle(stream, dev))
     if rc != FA_OK:
         raise FaError("fa_decode_paged_noalloc", rc)
     return out, lse

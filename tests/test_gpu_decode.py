@@ -110,3 +110,36 @@ def test_decode_workspace_too_small(fa):
                            dev_i32(inp.block_table), dev_i32(inp.ctx_lens), inp.max_ctx_len,
                            workspace=ws)
     assert e.value.status == -4
+
+
+def test_decode_binding_checks_caller_buffers(fa):
+    """The decode calls check the pools, the table, the context lengths and
+    the caller's outputs before any launch (the no-allocation call included:
+    its output is always the caller's)."""
+    torch = torch_mod()
+    inp = W.decode_inputs([40, 70], 4, 2, 128, seed=44)
+    q, kp, vp = dev_bf16(inp.q), dev_bf16(inp.k_pool), dev_bf16(inp.v_pool)
+    table, ctx = dev_i32(inp.block_table), dev_i32(inp.ctx_lens)
+    good_out = torch.empty_like(q)
+    with pytest.raises(ValueError):   # v_pool shape differs from k_pool
+        fa.fa_decode_paged(q, kp, vp[:-1].contiguous(), table, ctx, inp.max_ctx_len)
+    with pytest.raises(ValueError):   # one context length too few
+        fa.fa_decode_paged(q, kp, vp, table, ctx[:1].contiguous(), inp.max_ctx_len)
+    with pytest.raises(ValueError):   # table rows do not match the batch
+        fa.fa_decode_paged(q, kp, vp, table[:1].contiguous(), ctx, inp.max_ctx_len)
+    with pytest.raises(ValueError):
+        fa.fa_decode_paged(q, kp, vp, table, ctx, inp.max_ctx_len,
+                           out=torch.empty((2, 4, 64), dtype=torch.bfloat16, device="cuda"))
+    with pytest.raises(ValueError):
+        fa.fa_decode_paged_noalloc(q, kp, vp, table, ctx, inp.max_ctx_len,
+                                   out=good_out[:1].contiguous())
+    with pytest.raises(ValueError):
+        fa.fa_decode_paged_noalloc(q, kp, vp, table, ctx, inp.max_ctx_len, out=good_out,
+                                   lse=torch.empty((2, 4), dtype=torch.float64, device="cuda"))
+    out, lse = fa.fa_decode_paged_noalloc(q, kp, vp, table, ctx, inp.max_ctx_len, out=good_out,
+                                          lse=torch.empty((2, 4), dtype=torch.float32,
+                                                          device="cuda"))
+    torch.cuda.synchronize()
+    o_ref, l_ref = ref_decode(inp)
+    compare(host_f64(out), o_ref, lse.cpu().numpy().astype(np.float64), l_ref, "noalloc binding")
+    assert_device_clean()

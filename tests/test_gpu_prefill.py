@@ -150,3 +150,39 @@ def test_rejects_bad_arguments(fa):
     with pytest.raises(fa.FaError) as e:
         fa.fa_fwd(q, k, k)
     assert e.value.status == -1
+
+
+def test_binding_checks_caller_buffers(fa):
+    """Buffers the caller supplies are checked before any launch: the kernels
+    write exactly the sizes they are given, so a short output, a wrong dtype
+    or a workspace that is not bytes must never reach them."""
+    torch = torch_mod()
+    q = torch.zeros((1, 130, 2, 64), dtype=torch.bfloat16, device="cuda")
+    bad_outputs = [
+        dict(out=torch.empty((1, 129, 2, 64), dtype=torch.bfloat16, device="cuda")),
+        dict(out=torch.empty((1, 130, 2, 64), dtype=torch.float16, device="cuda")),
+        dict(out=torch.empty((1, 130, 2, 128), dtype=torch.bfloat16, device="cuda")[..., :64]),
+        dict(lse=torch.empty((1, 2, 129), dtype=torch.float32, device="cuda")),
+        dict(lse=torch.empty((1, 2, 130), dtype=torch.bfloat16, device="cuda")),
+        dict(out=torch.empty((1, 130, 2, 64), dtype=torch.bfloat16)),   # host memory
+    ]
+    for kw in bad_outputs:
+        with pytest.raises(ValueError):
+            fa.fa_fwd(q, q, q, causal=True, **kw)
+        with pytest.raises(ValueError):
+            fa.fa_fwd_splitkv(q, q, q, causal=True, **kw)
+    with pytest.raises(ValueError):   # a workspace given as fp32 words, not bytes
+        fa.fa_fwd_splitkv(q, q, q, workspace=torch.empty(1 << 20, dtype=torch.float32,
+                                                         device="cuda"))
+    lse = torch.zeros((1, 2, 130), dtype=torch.float32, device="cuda")
+    with pytest.raises(ValueError):
+        fa.fa_bwd(q, q, q, q, lse, q, dq=torch.empty((1, 130, 2, 32), dtype=torch.bfloat16,
+                                                      device="cuda"))
+    with pytest.raises(ValueError):
+        fa.fa_bwd(q, q, q, q, lse[:, :1], q)
+    with pytest.raises(ValueError):   # k and v of different shapes
+        fa.fa_fwd_varlen(q[0], q[0], q[0, :, :1].contiguous(),
+                         torch.tensor([0, 130], dtype=torch.int32, device="cuda"), 130)
+    with pytest.raises(ValueError):   # offsets on the host
+        fa.fa_fwd_varlen(q[0], q[0], q[0], torch.tensor([0, 130], dtype=torch.int32), 130)
+    assert_device_clean()
