@@ -26,6 +26,9 @@ Reported (one JSON line from rank 0):
            prefill, FP8 prefill, the backward pass), each on its own workload
   other_configs  the dense d = 64 configuration (B4 H16 N2048), causal and not
 
+The split-KV and d = 64 workloads fit in L2, so those two are timed launch by
+launch with L2 flushed (a 256 MiB write) before each launch.
+
 ``--impl reference`` times the oracle instead (the slow reference arm).
 Multi-GPU: one process per GPU (torchrun); every rank runs the full step on
 its own GPU (weak scaling, no collective on the data path); the timed region
@@ -458,6 +461,27 @@ def measure_backward(torch, device, fa, steps, warmup, peak):
             "launches_per_call": 3}
 
 
+L2_FLUSH_BYTES = 256 << 20   # twice the GB300's L2
+
+
+def time_flushed(torch, fn, steps, warmup, flush):
+    """Mean device time of fn() over `steps` calls, each timed alone with CUDA
+    events on the current stream after `flush` (a buffer larger than L2) has
+    been rewritten, so no call finds its inputs or partial states in L2."""
+    for _ in range(warmup):
+        fn()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
+
+
 def measure_splitkv(torch, device, fa, steps, warmup, peak):
     """Split-KV dense prefill (fa_fwd_splitkv, automatic split count) on a
     long sequence with few heads (B=1, H=4, N=8192, d=128, causal: 128
@@ -472,24 +496,14 @@ def measure_splitkv(torch, device, fa, steps, warmup, peak):
     ws = torch.empty(fa.fa_fwd_splitkv_workspace_size(B, H, N, d, 0), dtype=torch.uint8,
                      device=device)
     flops = W.prefill_flops(B, N, H, d, True)
-
-    def timed(fn):
-        for _ in range(warmup):
-            fn()
-        torch.cuda.synchronize()
-        stream = torch.cuda.current_stream()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / steps
-
-    ms = timed(lambda: fa.fa_fwd_splitkv(q, k, v, causal=True, out=out, lse=lse, workspace=ws))
-    ms_plain = timed(lambda: fa.fa_fwd(q, k, v, causal=True, out=out, lse=lse))
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    ms = time_flushed(torch, lambda: fa.fa_fwd_splitkv(q, k, v, causal=True, out=out, lse=lse,
+                                                       workspace=ws), steps, warmup, flush)
+    ms_plain = time_flushed(torch, lambda: fa.fa_fwd(q, k, v, causal=True, out=out, lse=lse),
+                            steps, warmup, flush)
     tf = flops / (ms / 1e3) / 1e12
-    return {"workload": "split-KV causal prefill, few heads: B1 H4 N8192 d128",
+    return {"workload": "split-KV causal prefill, few heads: B1 H4 N8192 d128 "
+                        "(L2 flushed before each launch)",
             "ms": ms, "tflops": tf, "frac_of_peak": tf / peak, "flops": flops,
             "unsplit_ms": ms_plain, "unsplit_tflops": flops / (ms_plain / 1e3) / 1e12,
             "launches_per_call": 2}
@@ -506,21 +520,11 @@ def measure_dense_d64(torch, device, fa, steps, warmup):
     q, k, v = (to_dev(getattr(inp, n), torch, device) for n in ("q", "k", "v"))
     out = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
-    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     res = {"workload": "dense prefill B4 H16 N2048 d64 (L2 flushed before each launch)"}
     for causal in (False, True):
-        for _ in range(warmup):
-            fa.fa_fwd(q, k, v, causal=causal, out=out, lse=lse)
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(steps)]
-        for e0, e1 in ev:
-            flush.zero_()
-            e0.record(stream)
-            fa.fa_fwd(q, k, v, causal=causal, out=out, lse=lse)
-            e1.record(stream)
-        torch.cuda.synchronize()
-        ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
+        ms = time_flushed(torch, lambda: fa.fa_fwd(q, k, v, causal=causal, out=out, lse=lse),
+                          steps, warmup, flush)
         flops = W.prefill_flops(B, N, H, d, causal)
         res["causal" if causal else "non_causal"] = {"ms": ms, "tflops": flops / (ms / 1e3) / 1e12,
                                                      "flops": flops}
@@ -792,7 +796,8 @@ def bench_ours(args, rank, world, local):
             "decode_batch": args.decode_batch or 64,
             "prefill_flops_per_step": f_pre,
             "decode_bytes_per_step": dbytes,
-            "l2": "every input is larger than L2 (no flush needed)",
+            "l2": "step inputs are larger than L2 (no flush needed); the split-KV and "
+                  "d=64 legs, which fit in L2, flush it before each timed launch",
             "parallelism": f"replicas x{world}",
         },
         "decode": None if dbytes is None else {

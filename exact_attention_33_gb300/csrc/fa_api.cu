@@ -56,9 +56,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// bf16 tensor [outer][rows][heads][d] (d innermost) as a 4-D TMA map with
-// dims {d, heads, rows, outer}; each copy moves a box of {64, 1, box_rows, 1}
-// with 128-byte swizzle.  Out-of-range rows read as zero.
+// Tensor [outer][rows][heads][d] (d innermost) of bf16 (or one-byte, or
+// fp32) elements as a 4-D TMA map with dims {d, heads, rows, outer}; each
+// copy moves a box of one 128-byte swizzle row per (head, row): {64, 1,
+// box_rows, 1} bf16 values.  Out-of-range rows read as zero and are not
+// stored.
 int make_map(CUtensorMap *map, const void *base, int d, int heads, long long rows,
              long long outer, int box_rows, int elem_bytes = 2) {
   auto fn = encode_fn();
@@ -73,8 +75,9 @@ int make_map(CUtensorMap *map, const void *base, int d, int heads, long long row
   const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / elem_bytes), 1,
                              static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUtensorMapDataType dt =
-      elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType dt = elem_bytes == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUresult r = fn(map, dt, 4, const_cast<void *>(base), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -153,8 +156,12 @@ int prefill_head_group(int H) {
   return 1;
 }
 
-// Splits of the split-KV prefill: enough CTAs for about two per SM, at most
-// 16 splits and at most one split per key tile.
+// Splits of the split-KV prefill: about 1.7 CTAs per SM (rounded down), at
+// most 16 splits and at most one split per key tile.  Every extra split costs
+// an fp32 partial tile per query tile and its share of the combine; on
+// B1 H4 N8192 causal (128 work items on 152 SMs) 2 splits ran at 924 TFLOP/s
+// against 796 for 3 and 640 unsplit, and from 256 work items up the unsplit
+// kernel was fastest.
 int prefill_num_splits(int B, int H, int N, int requested) {
   const long long pairs = (N + kPrefillRowsPerCta - 1) / kPrefillRowsPerCta;
   const int tiles = (N + kPrefillBN - 1) / kPrefillBN;
@@ -163,7 +170,7 @@ int prefill_num_splits(int B, int H, int N, int requested) {
     int sms = sm_count();
     if (sms <= 0) sms = 148;
     const long long base = std::max(1LL, pairs * B * H);
-    s = static_cast<int>((2LL * sms + base - 1) / base);
+    s = static_cast<int>(std::min(16LL, (17LL * sms) / (10LL * base)));
   }
   return std::max(1, std::min({s, 16, std::max(1, tiles)}));
 }
@@ -485,16 +492,22 @@ int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *out, float
   const SplitWs w = split_ws(B, H, N, d, num_splits);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.o_bytes + w.ml_bytes)
     return FA_ERR_WORKSPACE;
+  // one split: the plain kernel writes the result directly
+  if (w.splits == 1) return fa_fwd(q, k, v, out, lse, B, H, Hkv, N, d, scale, causal, stream);
   const long long pairs = (N + kPrefillRowsPerCta - 1) / kPrefillRowsPerCta;
   const long long grid = pairs * B * H * w.splits;
   if (grid > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(N) * H * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
 
-  CUtensorMap tq, tk, tv, to;
+  // The split kernel stores its fp32 partial O tiles, [split][B][N][H][d],
+  // through this map: (split, batch) is the outer coordinate.
+  CUtensorMap tq, tk, tv, to_part;
   int rc = make_map(&tq, q, d, H, N, B, kPrefillBM);
   if (rc == FA_OK) rc = make_map(&tk, k, d, Hkv, N, B, kPrefillBN);
   if (rc == FA_OK) rc = make_map(&tv, v, d, Hkv, N, B, kPrefillBN);
-  if (rc == FA_OK) rc = make_map(&to, out, d, H, N, B, kPrefillBM);
+  if (rc == FA_OK)
+    rc = make_map(&to_part, workspace, d, H, N, static_cast<long long>(w.splits) * B,
+                  kPrefillBM, 4);
   if (rc != FA_OK) return rc;
 
   PrefillParams p{};
@@ -516,7 +529,7 @@ int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *out, float
   p.o_part = static_cast<float *>(workspace);
   p.ml_part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + w.o_bytes);
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_prefill(tq, tk, tv, tv, to, p, d, causal != 0, kKindDenseSplit,
+  cudaError_t e = launch_prefill(tq, tk, tv, tv, to_part, p, d, causal != 0, kKindDenseSplit,
                                  static_cast<int>(grid), st);
   if (e == cudaSuccess) e = launch_prefill_split_combine(p, d, st);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;

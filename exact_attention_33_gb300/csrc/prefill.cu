@@ -139,6 +139,7 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
                    const __grid_constant__ CUtensorMap tm_o, const PrefillParams p) {
   using L = PrefillLayout<D, FP8, QT>;
   using Sh = PrefillShape<QT>;
+  static_assert(!(FP8 && KIND == kKindDenseSplit), "the split-KV layout is bf16 only");
   constexpr int SK = L::kStagesK;
   constexpr int SV = L::kStagesV;
 
@@ -744,7 +745,7 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
     const float m = m_ref;
 
     // ---------------------------------------------------- epilogue
-    if (KIND == kKindDenseSplit) {
+    if constexpr (KIND == kKindDenseSplit) {
       // Partial state of this split: o unnormalised (fp32), m (log2 units),
       // l over the bf16 weights and l over the fp32 exponentials.  A row of
       // a live tile that got no key tile stores the neutral state.
@@ -754,33 +755,58 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
         have = mbar_wait(&o_done[i], 0, abort_flag, p.status);
         have = __all_sync(0xffffffffu, have);
       }
-      if (tile_live && (have || my_end == 0)) {
+      if (tile_live && my_end > 0) {
+        // The fp32 tile goes out through the warpgroup's free Q tile (it
+        // holds half of an fp32 tile), half of the columns at a time, with
+        // one TMA store per 32-column chunk of 128-byte swizzled rows; rows
+        // past N are clipped by the tensor bounds.  All four warps meet at
+        // the barriers (the conditions above are the same for the whole
+        // tile); a warp whose wait gave up writes nothing, and the status
+        // word already marks the call as failed.
         if (have) tc_fence_after();
-        const bool live = qi < len;
-        const size_t prow = (static_cast<size_t>(split) * p.B + b) * p.N + qi;
-        float *orow = p.o_part + (prow * p.H + h) * D;
-        if (have) {
+        uint8_t *stile = sQ + i * L::kTileBytes;
+        constexpr int kHalfChunks = D / 64;
+        static_assert(kHalfChunks * L::kChunkBytes <= L::kTileBytes, "staging tile too small");
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+          for (int cc = 0; have && cc < kHalfChunks; ++cc) {
+            const int c = half * kHalfChunks + cc;  // columns [32 c, 32 c + 32)
             uint32_t o[32];
             tmem_ld32_wait(tO + c * 32, o);
-            if (live) {
+            uint8_t *srow = stile + cc * L::kChunkBytes + row * 128;
+            // 128-byte swizzle: 16-byte unit u of row r sits at u ^ (r % 8)
 #pragma unroll
-              for (int v4 = 0; v4 < 8; ++v4)
-                reinterpret_cast<uint4 *>(orow)[c * 8 + v4] =
-                    make_uint4(o[v4 * 4], o[v4 * 4 + 1], o[v4 * 4 + 2], o[v4 * 4 + 3]);
-            }
+            for (int u = 0; u < 8; ++u)
+              *reinterpret_cast<uint4 *>(srow + ((u ^ (row & 7)) * 16)) =
+                  make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
           }
+          fence_proxy_async_smem();
+          named_bar_sync(1 + i, 128);
+          if (row == 0 && have) {
+#pragma unroll
+            for (int cc = 0; cc < kHalfChunks; ++cc)
+              tma_store_4d(&tm_o, stile + cc * L::kChunkBytes, (half * kHalfChunks + cc) * 32,
+                           h, row0 + i * kPrefillBM, split * p.B + b);
+            tma_store_commit();
+            tma_store_wait_read();
+          }
+          // the second half reuses the staging tile once the copies have read it
+          if (half == 0) named_bar_sync(1 + i, 128);
         }
-        if (live)
-          reinterpret_cast<float4 *>(p.ml_part)[prow * p.H + h] =
-              have ? make_float4(m, l, l_exact, 0.f) : make_float4(-CUDART_INF_F, 0.f, 0.f, 0.f);
       }
-    } else if (ok && my_end > 0) {
-      ok = mbar_wait(&o_done[i], 0, abort_flag, p.status);
-      ok = __all_sync(0xffffffffu, ok);
+      if (tile_live && (have || my_end == 0) && qi < len) {
+        const size_t prow = (static_cast<size_t>(split) * p.B + b) * p.N + qi;
+        reinterpret_cast<float4 *>(p.ml_part)[prow * p.H + h] =
+            have ? make_float4(m, l, l_exact, 0.f) : make_float4(-CUDART_INF_F, 0.f, 0.f, 0.f);
+      }
+    } else if (my_end > 0) {
       if (ok) {
-        tc_fence_after();
+        ok = mbar_wait(&o_done[i], 0, abort_flag, p.status);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      {
+        if (ok) tc_fence_after();
         const bool live = qi < len;
         const float inv_l = (l > 0.f) ? p.v_descale / l : 0.f;
         // A whole bf16 tile goes out through shared memory and one TMA store
@@ -792,9 +818,13 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
         const bool tma_out =
             !FP8 && (KIND == kKindDense || row0 + (i + 1) * kPrefillBM <= len);
         if (tma_out) {
+          // All four warps of the tile meet at the barrier below (my_end and
+          // tma_out are the same for the whole tile); a warp whose wait gave
+          // up writes nothing, and the status word already marks the call as
+          // failed.
           uint8_t *stile = sQ + i * L::kTileBytes;
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; ok && c < D / 32; ++c) {
             uint32_t o[32];
             tmem_ld32_wait(tO + c * 32, o);
             uint8_t *srow = stile + (c >> 1) * L::kChunkBytes + row * 128;
@@ -816,7 +846,7 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
           }
           fence_proxy_async_smem();
           named_bar_sync(1 + i, 128);
-          if (row == 0) {
+          if (row == 0 && ok) {
             const int orow = (KIND == kKindDense ? 0 : seq_start) + row0 + i * kPrefillBM;
 #pragma unroll
             for (int c = 0; c < L::kChunks; ++c)
@@ -833,7 +863,7 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) +
                                                ((out_row * p.H + h) * D) * 2);
 #pragma unroll
-        for (int c = 0; !tma_out && c < D / 32; ++c) {
+        for (int c = 0; ok && !tma_out && c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32_wait(tO + c * 32, o);
           if (live) {
@@ -852,7 +882,7 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
             }
           }
         }
-        if (live && p.lse != nullptr) {
+        if (ok && live && p.lse != nullptr) {
           const float lse = (l_exact > 0.f)
                                 ? (m + __log2f(l_exact)) * 0.69314718055994530942f
                                 : -CUDART_INF_F;

@@ -147,11 +147,14 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *out, const f
  * produces a partial (m, l, o) state and a second kernel merges them with the
  * rescaling of the explainer page's "Show the maths".
  * Arguments and results as fa_fwd, plus:
- *   num_splits : 1..16, or 0 to let the library choose (about two CTAs per
- *                SM); values above the number of 128-key tiles are clamped.
+ *   num_splits : 1..16, or 0 to let the library choose (about 1.7 CTAs per
+ *                SM: 2 splits for 128 work items on 152 SMs, 1 from about
+ *                152 work items up); values above the number of 128-key
+ *                tiles are clamped.
  *   workspace  : >= fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits)
  *                bytes, 256-byte aligned, owned by the caller.
- * Two kernels run in stream order: the split prefill and the combine.
+ * Two kernels run in stream order: the split prefill and the combine.  With
+ * one split the call runs the fa_fwd kernel alone (no partial states).
  */
 size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits);
 int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *out, float *lse, int B,
