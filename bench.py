@@ -66,9 +66,11 @@ NOMINAL_HBM_GBS = 8000.0
 PROFILES = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = {
     "prefill": ["exact_attention_33_gb300/csrc/prefill.cu", "exact_attention_33_gb300/csrc/ptx.cuh",
-                "exact_attention_33_gb300/csrc/fa_internal.h"],
+                "exact_attention_33_gb300/csrc/fa_internal.h",
+                "exact_attention_33_gb300/csrc/checks.cuh"],
     "decode": ["exact_attention_33_gb300/csrc/decode.cu", "exact_attention_33_gb300/csrc/ptx.cuh",
-               "exact_attention_33_gb300/csrc/fa_internal.h"],
+               "exact_attention_33_gb300/csrc/fa_internal.h",
+               "exact_attention_33_gb300/csrc/checks.cuh"],
 }
 
 

@@ -27,6 +27,7 @@ __all__ = [
     "fa_decode_paged", "fa_decode_paged_noalloc", "fa_decode_workspace_size",
     "fa_status_string", "fa_device_status",
     "fa_version", "FA_DEV_TIMEOUT", "FA_DEV_BAD_BLOCK", "FA_DEV_BAD_CTX", "FA_DEV_BAD_SEQLEN",
+    "FA_DEV_BAD_INDEX",
 ]
 
 FA_OK = 0
@@ -34,6 +35,7 @@ FA_DEV_TIMEOUT = 1
 FA_DEV_BAD_BLOCK = 2
 FA_DEV_BAD_CTX = 4
 FA_DEV_BAD_SEQLEN = 8
+FA_DEV_BAD_INDEX = 16   # checked build only
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -47,7 +49,9 @@ class FaError(RuntimeError):
 
 
 def library_path() -> str:
-    return os.path.join(_PKG, "libfa.so")
+    """libfa.so, or the checked build libfa_checked.so when FA_CHECKED=1."""
+    name = "libfa_checked.so" if os.environ.get("FA_CHECKED") == "1" else "libfa.so"
+    return os.path.join(_PKG, name)
 
 
 def load_library() -> ctypes.CDLL:
@@ -62,7 +66,8 @@ def load_library() -> ctypes.CDLL:
         if not os.path.exists(path):
             raise RuntimeError(
                 f"{path} is missing: build it with `python -m exact_attention_33_gb300.build` "
-                "(or __graft_entry__.build()); there is no non-CUDA fallback")
+                "(add --checked for the checked build, or call __graft_entry__.build()); "
+                "there is no non-CUDA fallback")
         lib = ctypes.CDLL(path)
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]

@@ -30,6 +30,7 @@
 
 #include "fa_internal.h"
 #include "ptx.cuh"
+#include "checks.cuh"
 
 namespace fa {
 
@@ -149,9 +150,12 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
   const int h = static_cast<int>(bh % p.H);
   const int b = static_cast<int>(bh / p.H);
   const size_t vec = static_cast<size_t>(gr);  // (b * H + h) * Npad + row
+  // elements of O / dO, and of the workspace vectors, the call owns
+  const size_t n_rows = static_cast<size_t>(p.B) * p.N * p.H;
+  const size_t n_vec = static_cast<size_t>(p.B) * p.H * p.Npad;
   float acc = 0.f;
-  if (row < p.N) {
-    const size_t off = ((static_cast<size_t>(b) * p.N + row) * p.H + h) * D + sub * 8;
+  const size_t off = ((static_cast<size_t>(b) * p.N + row) * p.H + h) * D + sub * 8;
+  if (row < p.N && in_bounds(off, 8, n_rows * D, p.status)) {
     const uint4 o = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.out) + off);
     const uint4 g = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.dout) + off);
     const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
@@ -165,9 +169,10 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
   }
 #pragma unroll
   for (int sft = TPR / 2; sft > 0; sft >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sft);
-  if (sub == 0) {
+  if (sub == 0 && in_bounds(vec, 1, n_vec, p.status)) {
     if (row < p.N) {
-      const float l = p.lse[(static_cast<size_t>(b) * p.H + h) * p.N + row];
+      const float l = checked_load(p.lse, (static_cast<size_t>(b) * p.H + h) * p.N + row,
+                                   n_rows, p.status);
       p.lse2[vec] = (l == -CUDART_INF_F) ? CUDART_INF_F : l * kLog2eF;
       p.dsum[vec] = acc;
     } else {
@@ -335,8 +340,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem + lane_off, tP = tmem + 128 + lane_off, tQ = tmem + 256 + lane_off;
     const size_t vec = (static_cast<size_t>(b) * p.H + h) * p.Npad + min(qi, p.Npad - 1);
-    const float lse2 = p.lse2[vec];
-    const float dsum = p.dsum[vec];
+    const size_t n_vec = static_cast<size_t>(p.B) * p.H * p.Npad;
+    const float lse2 = checked_load(p.lse2, vec, n_vec, p.status);
+    const float dsum = checked_load(p.dsum, vec, n_vec, p.status);
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
@@ -392,13 +398,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (ok) {
       tc_fence_after();
-      uint16_t *dst = static_cast<uint16_t *>(p.dq) +
-                      ((static_cast<size_t>(b) * p.N + qi) * p.H + h) * D;
+      const size_t drow = ((static_cast<size_t>(b) * p.N + qi) * p.H + h) * D;
+      uint16_t *dst = static_cast<uint16_t *>(p.dq) + drow;
+      const bool row_ok =
+          qi >= p.N || in_bounds(drow, D, static_cast<size_t>(p.B) * p.N * p.H * D, p.status);
 #pragma unroll
       for (int c = hf * (D / 64); c < (hf + 1) * (D / 64); ++c) {
         uint32_t o[32];
         tmem_ld32_wait(tQ + c * 32, o);
-        if (qi < p.N) store_row_scaled_bf16(dst + c * 32, o, p.scale);
+        if (qi < p.N && row_ok) store_row_scaled_bf16(dst + c * 32, o, p.scale);
       }
     }
   }
@@ -505,7 +513,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_4d(sq + c * L::kChunkBytes, &tm_q, &qd_full[s], c * 64, hq, i * 128, b);
           tma_load_4d(sd + c * L::kChunkBytes, &tm_do, &qd_full[s], c * 64, hq, i * 128, b);
         }
-        const size_t vec = (static_cast<size_t>(b) * p.H + hq) * p.Npad + i * 128;
+        // (a checked build that finds the 128 entries outside the workspace
+        // copies entries 0..127 instead, so the barrier still gets its bytes)
+        size_t vec = (static_cast<size_t>(b) * p.H + hq) * p.Npad + i * 128;
+        if (!in_bounds(vec, 128, static_cast<size_t>(p.B) * p.H * p.Npad, p.status)) vec = 0;
         bulk_load(sVec + 256 * s, p.lse2 + vec, 512, &qd_full[s]);
         bulk_load(sVec + 256 * s + 128, p.dsum + vec, 512, &qd_full[s]);
         issued = it + 1;
@@ -644,17 +655,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const size_t orow = ((static_cast<size_t>(b) * p.N + kj) * p.Hkv + kvh) * D;
       uint16_t *dv = static_cast<uint16_t *>(p.dv) + orow;
       uint16_t *dk = static_cast<uint16_t *>(p.dk) + orow;
+      const bool row_ok =
+          kj >= p.N || in_bounds(orow, D, static_cast<size_t>(p.B) * p.N * p.Hkv * D, p.status);
 #pragma unroll
       for (int c = hf * (D / 64); c < (hf + 1) * (D / 64); ++c) {
         uint32_t o[32];
         tmem_ld32_wait(tV + c * 32, o);
-        if (kj < p.N) store_row_scaled_bf16(dv + c * 32, o, 1.f);
+        if (kj < p.N && row_ok) store_row_scaled_bf16(dv + c * 32, o, 1.f);
       }
 #pragma unroll
       for (int c = hf * (D / 64); c < (hf + 1) * (D / 64); ++c) {
         uint32_t o[32];
         tmem_ld32_wait(tK + c * 32, o);
-        if (kj < p.N) store_row_scaled_bf16(dk + c * 32, o, p.scale);
+        if (kj < p.N && row_ok) store_row_scaled_bf16(dk + c * 32, o, p.scale);
       }
     }
   }

@@ -31,6 +31,7 @@
 
 #include "fa_internal.h"
 #include "ptx.cuh"
+#include "checks.cuh"
 
 namespace fa {
 
@@ -73,7 +74,7 @@ __global__ void __launch_bounds__(32)
   const int b = blockIdx.z;
   const int lane = threadIdx.x;
 
-  const int ctx = p.ctx_lens[b];
+  const int ctx = checked_load(p.ctx_lens, b, p.batch, p.status);
   if (ctx < 0 || ctx > p.max_ctx_len || ctx > p.max_blocks_per_seq * kDecodeBlock) {
     if (split == 0 && kvh == 0 && lane == 0) raise_status(p.status, FA_DEV_BAD_CTX);
     return;
@@ -89,15 +90,23 @@ __global__ void __launch_bounds__(32)
   int my_blk = 0;
   bool bad = false;
   if (lane < nblk) {
-    my_blk = p.block_table[static_cast<size_t>(b) * p.max_blocks_per_seq + lb0 + lane];
-    bad = (my_blk < 0 || my_blk >= p.num_blocks);
+    const size_t tidx = static_cast<size_t>(b) * p.max_blocks_per_seq + lb0 + lane;
+    if (in_bounds(tidx, 1, static_cast<size_t>(p.batch) * p.max_blocks_per_seq, p.status)) {
+      my_blk = p.block_table[tidx];
+      bad = (my_blk < 0 || my_blk >= p.num_blocks);
+    } else {
+      bad = true;
+    }
   }
+  // partial-state rows of the call: [batch, H, max_splits]
+  const size_t part_rows = static_cast<size_t>(p.batch) * p.H * p.max_splits;
   const size_t part_row = static_cast<size_t>(b) * p.H + static_cast<size_t>(kvh) * G;
   if (__any_sync(0xffffffffu, bad)) {
     if (lane == 0) raise_status(p.status, FA_DEV_BAD_BLOCK);
     // Leave a neutral partial state so that the combine ignores this split.
     for (int g = 0; g < G; ++g) {
       const size_t row = (part_row + g) * p.max_splits + split;
+      if (!in_bounds(row, 1, part_rows, p.status)) continue;
       for (int c = lane; c < D; c += 32) p.o_part[row * D + c] = 0.f;
       if (lane == 0) {
         p.ml_part[row * 2 + 0] = -CUDART_INF_F;
@@ -146,7 +155,8 @@ __global__ void __launch_bounds__(32)
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int n = nt * 8 + grp;
-    const bool valid = n < G;
+    const bool valid =
+        n < G && in_bounds((part_row + n) * D, D, static_cast<size_t>(p.batch) * p.H * D, p.status);
     const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
         static_cast<const uint16_t *>(p.q) + (part_row + (valid ? n : 0)) * D);
 #pragma unroll
@@ -276,6 +286,7 @@ __global__ void __launch_bounds__(32)
         const int g = nt * 8 + 2 * quad + cc;
         if (g < G) {
           const size_t row = (part_row + g) * p.max_splits + split;
+          if (!in_bounds(row, 1, part_rows, p.status)) continue;
           if (grp == 0) {
             p.ml_part[row * 2 + 0] = mcol[nt][cc];
             p.ml_part[row * 2 + 1] = lt;
@@ -322,14 +333,21 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x;
   const int b = gw / p.H;
-  int ctx = p.ctx_lens[b];
+  int ctx = checked_load(p.ctx_lens, b, p.batch, p.status);
   if (ctx < 0 || ctx > p.max_ctx_len || ctx > p.max_blocks_per_seq * kDecodeBlock) ctx = 0;
   const int ns = (ctx + p.split_tokens - 1) / p.split_tokens;
   const size_t row0 = static_cast<size_t>(gw) * p.max_splits;
-  const float2 *ml = reinterpret_cast<const float2 *>(p.ml_part) + row0;
+  const size_t part_rows = static_cast<size_t>(p.batch) * p.H * p.max_splits;
+  // (m, l) of split i of this row (the neutral state if the index fails a
+  // check of the checked build)
+  auto ml = [&](int i) -> float2 {
+    return in_bounds(row0 + i, 1, part_rows, p.status)
+               ? reinterpret_cast<const float2 *>(p.ml_part)[row0 + i]
+               : make_float2(-CUDART_INF_F, 0.f);
+  };
 
   float M = -CUDART_INF_F;
-  for (int i = lane; i < ns; i += 32) M = fmaxf(M, ml[i].x);
+  for (int i = lane; i < ns; i += 32) M = fmaxf(M, ml(i).x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
 
@@ -350,6 +368,11 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
     };
     auto load_o = [&](int i, float (&v)[E]) {
       const float *orow = p.o_part + (row0 + i) * D + lane * E;
+      if (!in_bounds((row0 + i) * D + lane * E, E, part_rows * D, p.status)) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[e] = 0.f;
+        return;
+      }
       if constexpr (E == 4) {
         const float4 x = *reinterpret_cast<const float4 *>(orow);
         v[0] = x.x;
@@ -368,7 +391,7 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
       float v[U][E];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        st[u] = ml[i + u * W];
+        st[u] = ml(i + u * W);
         load_o(i + u * W, v[u]);
       }
 #pragma unroll
@@ -377,7 +400,7 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
     for (; i < ns; i += W) {
       float v[E];
       load_o(i, v);
-      add(ml[i], v);
+      add(ml(i), v);
     }
   }
 #pragma unroll
@@ -397,15 +420,18 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
   }
   const float inv = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
   uint16_t *dst = static_cast<uint16_t *>(p.out) + static_cast<size_t>(gw) * D + lane * E;
-  if (E == 4) {
+  const bool out_ok = in_bounds(static_cast<size_t>(gw) * D + lane * E, E,
+                                static_cast<size_t>(p.batch) * p.H * D, p.status);
+  if (out_ok && E == 4) {
     uint2 w;
     w.x = pack_bf16x2(acc[0] * inv, acc[1 % E] * inv);
     w.y = pack_bf16x2(acc[2 % E] * inv, acc[3 % E] * inv);
     *reinterpret_cast<uint2 *>(dst) = w;
-  } else {
+  } else if (out_ok) {
     *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1 % E] * inv);
   }
-  if (lane == 0 && p.lse != nullptr)
+  if (lane == 0 && p.lse != nullptr &&
+      in_bounds(gw, 1, static_cast<size_t>(p.batch) * p.H, p.status))
     p.lse[gw] = (Lsum > 0.f) ? (M + __log2f(Lsum)) * 0.69314718055994530942f : -CUDART_INF_F;
 }
 

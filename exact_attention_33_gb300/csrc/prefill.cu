@@ -36,6 +36,7 @@
 
 #include "fa_internal.h"
 #include "ptx.cuh"
+#include "checks.cuh"
 
 namespace fa {
 
@@ -91,7 +92,8 @@ __device__ __forceinline__ bool varlen_compact_item(const PrefillParams &p, int 
   if (lin == 0 && threadIdx.x < 32) {
     // A sequence with invalid bounds owns no item here; CTA 0 reports it.
     for (int s = lane; s < p.B; s += 32) {
-      const int a = p.cu_seqlens[s], e = p.cu_seqlens[s + 1];
+      const int a = checked_load(p.cu_seqlens, s, p.B + 1, p.status);
+      const int e = checked_load(p.cu_seqlens, s + 1, p.B + 1, p.status);
       if (a < 0 || e < a || e > p.total_tokens) raise_status(p.status, FA_DEV_BAD_SEQLEN);
     }
   }
@@ -100,7 +102,8 @@ __device__ __forceinline__ bool varlen_compact_item(const PrefillParams &p, int 
     const int s = s0 + lane;
     int np = 0;
     if (s < p.B) {
-      const int a = p.cu_seqlens[s], e = p.cu_seqlens[s + 1];
+      const int a = checked_load(p.cu_seqlens, s, p.B + 1, p.status);
+      const int e = checked_load(p.cu_seqlens, s + 1, p.B + 1, p.status);
       const int n = min(max(e - a, 0), p.total_tokens);
       np = (n + ROWS - 1) / ROWS;
     }
@@ -178,8 +181,8 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
     kv_len = len;
     offset = 0;
   } else {
-    seq_start = p.cu_seqlens[unit];
-    const int seq_end = p.cu_seqlens[unit + 1];
+    seq_start = checked_load(p.cu_seqlens, unit, p.B + 1, p.status);
+    const int seq_end = checked_load(p.cu_seqlens, unit + 1, p.B + 1, p.status);
     if (seq_start < 0 || seq_end < seq_start || seq_end > p.total_tokens) {
       if (pair == 0 && h == 0) raise_status(p.status, FA_DEV_BAD_SEQLEN);
       return;
@@ -193,7 +196,7 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
       kv_len = len;
       offset = 0;
     } else {
-      kv_len = p.ctx_lens[unit];
+      kv_len = checked_load(p.ctx_lens, unit, p.B, p.status);
       if (kv_len < 0 || kv_len > p.max_ctx_len ||
           kv_len > p.max_blocks_per_seq * kDecodeBlock) {
         if (pair == 0 && h == 0) raise_status(p.status, FA_DEV_BAD_CTX);
@@ -346,6 +349,9 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
     auto fetch = [&](int w) -> int {
       const int blk = (kv0 + w) * kBlkPerTile + lane;
       if (w + lane / kBlkPerTile >= n_kv || blk >= total_blk) return -1;
+      if (!in_bounds(static_cast<size_t>(trow - p.block_table) + blk, 1,
+                     static_cast<size_t>(p.B) * p.max_blocks_per_seq, p.status))
+        return -1;
       const int phys = trow[blk];
       if (phys < 0 || phys >= p.num_blocks) {
         raise_status(p.status, FA_DEV_BAD_BLOCK);
@@ -797,7 +803,9 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
       }
       if (tile_live && (have || my_end == 0) && qi < len) {
         const size_t prow = (static_cast<size_t>(split) * p.B + b) * p.N + qi;
-        reinterpret_cast<float4 *>(p.ml_part)[prow * p.H + h] =
+        if (in_bounds(prow * p.H + h, 1,
+                      static_cast<size_t>(p.num_splits) * p.B * p.N * p.H, p.status))
+          reinterpret_cast<float4 *>(p.ml_part)[prow * p.H + h] =
             have ? make_float4(m, l, l_exact, 0.f) : make_float4(-CUDART_INF_F, 0.f, 0.f, 0.f);
       }
     } else if (my_end > 0) {
@@ -862,11 +870,16 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
           out_row = static_cast<size_t>(b) * p.N + qi;
         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) +
                                                ((out_row * p.H + h) * D) * 2);
+        // rows of the output (and of the log-sum-exp) the call owns
+        const size_t out_rows =
+            (KIND == kKindDense) ? static_cast<size_t>(p.B) * p.N : static_cast<size_t>(p.total_tokens);
+        const bool row_ok =
+            !live || tma_out || in_bounds((out_row * p.H + h) * D, D, out_rows * p.H * D, p.status);
 #pragma unroll
         for (int c = 0; ok && !tma_out && c < D / 32; ++c) {
           uint32_t o[32];
-          tmem_ld32_wait(tO + c * 32, o);
-          if (live) {
+          tmem_ld32_wait(tO + c * 32, o);  // warp-wide: every lane loads
+          if (live && row_ok) {
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4) {
               uint4 w;
@@ -882,14 +895,12 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
             }
           }
         }
-        if (ok && live && p.lse != nullptr) {
-          const float lse = (l_exact > 0.f)
-                                ? (m + __log2f(l_exact)) * 0.69314718055994530942f
-                                : -CUDART_INF_F;
-          if (KIND != kKindDense)
-            p.lse[static_cast<size_t>(h) * p.total_tokens + seq_start + qi] = lse;
-          else
-            p.lse[(static_cast<size_t>(b) * p.H + h) * p.N + qi] = lse;
+        const size_t lse_idx = (KIND != kKindDense)
+                                   ? static_cast<size_t>(h) * p.total_tokens + seq_start + qi
+                                   : (static_cast<size_t>(b) * p.H + h) * p.N + qi;
+        if (ok && live && p.lse != nullptr && in_bounds(lse_idx, 1, out_rows * p.H, p.status)) {
+          p.lse[lse_idx] = (l_exact > 0.f) ? (m + __log2f(l_exact)) * 0.69314718055994530942f
+                                           : -CUDART_INF_F;
         }
       }
     }
@@ -919,9 +930,16 @@ __global__ void __launch_bounds__(128) prefill_split_combine_kernel(const Prefil
   const size_t bn = gw / p.H;  // b * N + n
   const int h = static_cast<int>(gw % p.H);
   const size_t stride = static_cast<size_t>(p.B) * p.N * p.H;  // between splits
-  const float4 *ml = reinterpret_cast<const float4 *>(p.ml_part) + gw;
+  const size_t parts = static_cast<size_t>(p.num_splits) * stride;  // partial rows
+  // (m, l, l_exact) of split s for this row (the neutral state if the index
+  // fails a check of the checked build)
+  auto ml = [&](int sp) -> float4 {
+    const size_t idx = sp * stride + gw;
+    return in_bounds(idx, 1, parts, p.status) ? reinterpret_cast<const float4 *>(p.ml_part)[idx]
+                                              : make_float4(-CUDART_INF_F, 0.f, 0.f, 0.f);
+  };
   // M = max over the splits, one split per lane (at most 16 splits)
-  float M = (lane < p.num_splits) ? ml[lane * stride].x : -CUDART_INF_F;
+  float M = (lane < p.num_splits) ? ml(lane).x : -CUDART_INF_F;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   constexpr int E = D / 32;
@@ -942,9 +960,10 @@ __global__ void __launch_bounds__(128) prefill_split_combine_kernel(const Prefil
       for (int e = 0; e < E; ++e) acc[e] = live ? fmaf(w, v[e], acc[e]) : acc[e];
     };
     auto load_o = [&](int sp, float (&v)[E]) {
-      const float *orow = p.o_part + (sp * stride + gw) * D + lane * E;
+      const size_t idx = (sp * stride + gw) * D + lane * E;
+      const bool in = in_bounds(idx, E, parts * D, p.status);
 #pragma unroll
-      for (int e = 0; e < E; ++e) v[e] = orow[e];
+      for (int e = 0; e < E; ++e) v[e] = in ? p.o_part[idx + e] : 0.f;
     };
     constexpr int U = 4;
     int sp = 0;
@@ -953,7 +972,7 @@ __global__ void __launch_bounds__(128) prefill_split_combine_kernel(const Prefil
       float v[U][E];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        st[u] = ml[(sp + u) * stride];
+        st[u] = ml(sp + u);
         load_o(sp + u, v[u]);
       }
 #pragma unroll
@@ -962,19 +981,20 @@ __global__ void __launch_bounds__(128) prefill_split_combine_kernel(const Prefil
     for (; sp < p.num_splits; ++sp) {
       float v[E];
       load_o(sp, v);
-      add(ml[sp * stride], v);
+      add(ml(sp), v);
     }
   }
   const float inv = (Ls > 0.f) ? 1.f / Ls : 0.f;
   uint16_t *dst = static_cast<uint16_t *>(p.out) + gw * D + lane * E;
+  if (in_bounds(gw * D + lane * E, E, rows * D, p.status)) {
 #pragma unroll
-  for (int e = 0; e < E; e += 2)
-    *reinterpret_cast<uint32_t *>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
-  if (lane == 0 && p.lse != nullptr) {
-    const size_t b = bn / p.N, n = bn % p.N;
-    p.lse[(b * p.H + h) * p.N + n] =
-        (Le > 0.f) ? (M + __log2f(Le)) * 0.69314718055994530942f : -CUDART_INF_F;
+    for (int e = 0; e < E; e += 2)
+      *reinterpret_cast<uint32_t *>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
   }
+  const size_t b = bn / p.N, n = bn % p.N;
+  const size_t lse_idx = (b * p.H + h) * p.N + n;
+  if (lane == 0 && p.lse != nullptr && in_bounds(lse_idx, 1, rows, p.status))
+    p.lse[lse_idx] = (Le > 0.f) ? (M + __log2f(Le)) * 0.69314718055994530942f : -CUDART_INF_F;
 }
 
 cudaError_t launch_prefill_split_combine(const PrefillParams &p, int d, cudaStream_t stream) {

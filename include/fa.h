@@ -64,6 +64,7 @@ typedef enum {
 #define FA_DEV_BAD_BLOCK 2u   /* block_table entry outside [0, num_blocks)           */
 #define FA_DEV_BAD_CTX 4u     /* ctx_len < 0 or > max_blocks_per_seq * block_size    */
 #define FA_DEV_BAD_SEQLEN 8u  /* cu_seqlens not non-decreasing / beyond total_tokens */
+#define FA_DEV_BAD_INDEX 16u /* checked build only: a kernel index outside its buffer  */
 
 /*
  * Dense prefill forward (causal or not).
