@@ -143,3 +143,15 @@ def test_decode_binding_checks_caller_buffers(fa):
     o_ref, l_ref = ref_decode(inp)
     compare(host_f64(out), o_ref, lse.cpu().numpy().astype(np.float64), l_ref, "noalloc binding")
     assert_device_clean()
+
+
+def test_decode_quarter_million_token_context(fa):
+    """Contexts of 262,144 tokens (16,384 blocks, 512 key splits, all merged
+    by one combine row) beside single-token, odd-length and empty contexts,
+    on a pool of about 20,000 blocks in random order."""
+    ctx = [262144, 1, 70001, 0]
+    inp = W.decode_inputs(ctx, 8, 2, 128, seed=45, extra_blocks=7)
+    out, lse = run_decode(fa, inp)
+    o_ref, l_ref = ref_decode(inp)
+    compare(out, o_ref, lse, l_ref, "decode 262144-token context")
+    assert_device_clean()

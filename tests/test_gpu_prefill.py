@@ -186,3 +186,26 @@ def test_binding_checks_caller_buffers(fa):
     with pytest.raises(ValueError):   # offsets on the host
         fa.fa_fwd_varlen(q[0], q[0], q[0], torch.tensor([0, 130], dtype=torch.int32), 130)
     assert_device_clean()
+
+
+@pytest.mark.parametrize("d,causal", [(128, True), (64, False)])
+def test_quarter_million_token_sequence_sampled(fa, d, causal):
+    """One head over 262,144 tokens (2048 key tiles, 1024 query-tile pairs,
+    the last rows seeing every key): the longest sequence of the suite.  The
+    oracle evaluates seeded rows plus the first, the middle and the last
+    rows, each over all of its visible keys."""
+    torch = torch_mod()
+    N = 262144
+    inp = W.dense_inputs(1, N, 1, 1, d, seed=90 + d)
+    out, lse = run_dense(fa, inp, causal)
+    rows = np.unique(np.concatenate([
+        [0, 1, 127, 128, N // 2, N - 129, N - 2, N - 1],
+        np.random.default_rng(91).choice(N, 24, replace=False)]))
+    o_ref, l_ref = oracle.attention_one(f64(inp.q[0]), f64(inp.k[0]), f64(inp.v[0]),
+                                        causal=causal, rows=rows)
+    compare(out[0, rows, 0], o_ref[rows, 0], lse[0, 0, rows], l_ref[0, rows],
+            f"N=262144 d{d} causal={causal}")
+    assert np.all(np.isfinite(out))
+    del out, lse
+    torch.cuda.empty_cache()
+    assert_device_clean()
