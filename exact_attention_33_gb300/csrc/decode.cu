@@ -23,7 +23,9 @@
 //
 // decode_combine_kernel: one CTA per (sequence, query head) merges the
 // partial states: M = max m_i, L = sum 2^(m_i - M) l_i,
-// o = sum 2^(m_i - M) o_i / L, lse = (M + log2 L) ln 2.
+// o = sum 2^(m_i - M) o_i / L, lse = (M + log2 L) ln 2.  A row gets 1, 4 or
+// 16 warps by its number of splits (one warp per row and four rows per CTA
+// for large batches of short contexts, 16 for small batches of long ones).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -317,23 +319,40 @@ __global__ void __launch_bounds__(32)
   }
 }
 
-template <int D>
-__global__ void __launch_bounds__(32 * kCombineWarps)
+// Warps per merged row: one for rows of at most kCombineFewSplits splits
+// (four rows per CTA), kCombineWarps up to kCombineManySplits, and
+// kCombineWarpsMany beyond (rows of many short splits: small batches).
+constexpr int kCombineFewSplits = 8;
+constexpr int kCombineManySplits = 64;
+constexpr int kCombineWarpsMany = 16;
+
+template <int W>
+constexpr int combine_cta_warps() { return W < 4 ? 4 : W; }
+
+template <int D, int W>
+__global__ void __launch_bounds__(32 * combine_cta_warps<W>())
     decode_combine_kernel(const DecodeParams p) {
-  // One CTA per (sequence, query head): warp w merges splits w, w + W, ...
-  // (W = kCombineWarps), U of them per memory round trip, and the warps'
-  // sums are added through shared memory.  Lane l owns output elements
-  // [l E, l E + E).
-  constexpr int W = kCombineWarps;
+  // W warps per (sequence, query head) row, R rows per CTA.  The W warps of
+  // a row first find M together (thread t of the row reads the maxima of
+  // splits t, t + 32 W, ...); then warp w of the row merges splits w, w + W,
+  // ..., U of them per memory round trip, and the warps' sums are added
+  // through shared memory.  Lane l owns output elements [l E, l E + E).
+  constexpr int kWarps = combine_cta_warps<W>();
+  constexpr int R = kWarps / W;
   constexpr int E = D / 32;
-  constexpr int U = 4;
-  __shared__ float s_acc[W][D];
-  __shared__ float s_l[W];
+  constexpr int U = 8;
+  __shared__ float s_acc[kWarps][D];
+  __shared__ float s_l[kWarps];
+  __shared__ float s_m[kWarps];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int gw = blockIdx.x;
-  const int b = gw / p.H;
-  int ctx = checked_load(p.ctx_lens, b, p.batch, p.status);
+  const int wr = warp % W;  // warp within the row
+  const int r0 = warp - wr;  // first warp of the row
+  const int gw = blockIdx.x * R + warp / W;
+  // a CTA's last rows may lie past the end; they still meet the barriers
+  const bool row_live = gw < p.batch * p.H;
+  const int b = row_live ? gw / p.H : 0;
+  int ctx = row_live ? checked_load(p.ctx_lens, b, p.batch, p.status) : 0;
   if (ctx < 0 || ctx > p.max_ctx_len || ctx > p.max_blocks_per_seq * kDecodeBlock) ctx = 0;
   const int ns = (ctx + p.split_tokens - 1) / p.split_tokens;
   const size_t row0 = static_cast<size_t>(gw) * p.max_splits;
@@ -347,9 +366,13 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
   };
 
   float M = -CUDART_INF_F;
-  for (int i = lane; i < ns; i += 32) M = fmaxf(M, ml(i).x);
+  for (int i = wr * 32 + lane; i < ns; i += 32 * W) M = fmaxf(M, ml(i).x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) s_m[warp] = M;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < W; ++w) M = fmaxf(M, s_m[r0 + w]);
 
   float acc[E];
 #pragma unroll
@@ -385,7 +408,7 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
         v[1 % E] = x.y;
       }
     };
-    int i = warp;
+    int i = wr;
     for (; i + (U - 1) * W < ns; i += U * W) {
       float2 st[U];
       float v[U][E];
@@ -407,15 +430,15 @@ __global__ void __launch_bounds__(32 * kCombineWarps)
   for (int e = 0; e < E; ++e) s_acc[warp][lane * E + e] = acc[e];
   if (lane == 0) s_l[warp] = Lsum;
   __syncthreads();
-  if (warp != 0) return;
+  if (wr != 0 || !row_live) return;
   Lsum = 0.f;
 #pragma unroll
-  for (int w = 0; w < W; ++w) Lsum += s_l[w];
+  for (int w = 0; w < W; ++w) Lsum += s_l[r0 + w];
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     float t = 0.f;
 #pragma unroll
-    for (int w = 0; w < W; ++w) t += s_acc[w][lane * E + e];
+    for (int w = 0; w < W; ++w) t += s_acc[r0 + w][lane * E + e];
     acc[e] = t;
   }
   const float inv = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
@@ -453,7 +476,14 @@ static cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv,
   kern<<<grid, 32, L::kSmemAlloc, stream>>>(tk, tv, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<D><<<p.batch * p.H, 32 * kCombineWarps, 0, stream>>>(p);
+  const int rows = p.batch * p.H;
+  if (p.max_splits > kCombineManySplits)
+    decode_combine_kernel<D, kCombineWarpsMany>
+        <<<rows, 32 * kCombineWarpsMany, 0, stream>>>(p);
+  else if (p.max_splits > kCombineFewSplits)
+    decode_combine_kernel<D, kCombineWarps><<<rows, 32 * kCombineWarps, 0, stream>>>(p);
+  else
+    decode_combine_kernel<D, 1><<<(rows + 3) / 4, 128, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -155,3 +155,15 @@ def test_decode_quarter_million_token_context(fa):
     o_ref, l_ref = ref_decode(inp)
     compare(out, o_ref, lse, l_ref, "decode 262144-token context")
     assert_device_clean()
+
+
+@pytest.mark.parametrize("ctx", [[5, 40, 17, 1, 90], [700, 3, 1200]])
+def test_decode_combine_row_layouts(fa, ctx):
+    """Odd numbers of (sequence, head) rows (5 x 3 and 3 x 3 heads): short
+    contexts merge one row per warp, four rows per CTA, so the last CTA holds
+    rows past the end; longer ones merge each row with four warps."""
+    inp = W.decode_inputs(ctx, 3, 1, 128, seed=46 + len(ctx))
+    out, lse = run_decode(fa, inp)
+    o_ref, l_ref = ref_decode(inp)
+    compare(out, o_ref, lse, l_ref, f"decode rows {len(ctx)} x 3")
+    assert_device_clean()
