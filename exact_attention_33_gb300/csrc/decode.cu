@@ -37,6 +37,17 @@
 
 namespace fa {
 
+// Programmatic dependent launch of the combine: each split CTA lets the
+// combine grid be launched as soon as it starts (the combine's launch then
+// overlaps the last wave of splits), and the combine waits for the whole
+// split grid, its memory operations included, before reading a partial state.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 template <int D>
 struct DecodeLayout {
   static constexpr int kChunks = D / 64;
@@ -75,6 +86,7 @@ __global__ void __launch_bounds__(32)
   const int kvh = blockIdx.y;
   const int b = blockIdx.z;
   const int lane = threadIdx.x;
+  pdl_launch_dependents();
 
   const int ctx = checked_load(p.ctx_lens, b, p.batch, p.status);
   if (ctx < 0 || ctx > p.max_ctx_len || ctx > p.max_blocks_per_seq * kDecodeBlock) {
@@ -357,6 +369,7 @@ __global__ void __launch_bounds__(32 * combine_cta_warps<W>())
   const int ns = (ctx + p.split_tokens - 1) / p.split_tokens;
   const size_t row0 = static_cast<size_t>(gw) * p.max_splits;
   const size_t part_rows = static_cast<size_t>(p.batch) * p.H * p.max_splits;
+  pdl_wait_primary();  // the split grid's partial states are complete from here on
   // (m, l) of split i of this row (the neutral state if the index fails a
   // check of the checked build)
   auto ml = [&](int i) -> float2 {
@@ -460,6 +473,23 @@ __global__ void __launch_bounds__(32 * combine_cta_warps<W>())
 
 // ------------------------------------------------------------------ launch
 
+// The combine grid, launched as a programmatic dependent of the split grid
+// on the same stream.
+template <int D, int W>
+static cudaError_t launch_combine(const DecodeParams &p, int grid, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(32 * combine_cta_warps<W>());
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, W>, p);
+}
+
 template <int D, int NT>
 static cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv,
                                    const DecodeParams &p, cudaStream_t stream) {
@@ -478,13 +508,9 @@ static cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv,
   if (e != cudaSuccess) return e;
   const int rows = p.batch * p.H;
   if (p.max_splits > kCombineManySplits)
-    decode_combine_kernel<D, kCombineWarpsMany>
-        <<<rows, 32 * kCombineWarpsMany, 0, stream>>>(p);
-  else if (p.max_splits > kCombineFewSplits)
-    decode_combine_kernel<D, kCombineWarps><<<rows, 32 * kCombineWarps, 0, stream>>>(p);
-  else
-    decode_combine_kernel<D, 1><<<(rows + 3) / 4, 128, 0, stream>>>(p);
-  return cudaGetLastError();
+    return launch_combine<D, kCombineWarpsMany>(p, rows, stream);
+  if (p.max_splits > kCombineFewSplits) return launch_combine<D, kCombineWarps>(p, rows, stream);
+  return launch_combine<D, 1>(p, (rows + 3) / 4, stream);
 }
 
 cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
