@@ -37,17 +37,6 @@
 
 namespace fa {
 
-// Programmatic dependent launch of the combine: each split CTA lets the
-// combine grid be launched as soon as it starts (the combine's launch then
-// overlaps the last wave of splits), and the combine waits for the whole
-// split grid, its memory operations included, before reading a partial state.
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait_primary() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
 template <int D>
 struct DecodeLayout {
   static constexpr int kChunks = D / 64;

@@ -145,6 +145,8 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
   static_assert(!(FP8 && KIND == kKindDenseSplit), "the split-KV layout is bf16 only");
   constexpr int SK = L::kStagesK;
   constexpr int SV = L::kStagesV;
+  // the combine of a split launch may be scheduled once every split CTA has started
+  if constexpr (KIND == kKindDenseSplit) pdl_launch_dependents();
 
   // ---------------------------------------------------------- work item
   // One CTA per (sequence, 256-row query pair, head).  CTAs are ordered in
@@ -922,6 +924,7 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
 // lse = (M + log2 sum 2^(m_s - M) l_exact_s) ln 2.
 template <int D>
 __global__ void __launch_bounds__(128) prefill_split_combine_kernel(const PrefillParams p) {
+  pdl_wait_primary();  // the split grid's partial states are complete from here on
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const size_t rows = static_cast<size_t>(p.B) * p.N * p.H;
@@ -999,12 +1002,19 @@ __global__ void __launch_bounds__(128) prefill_split_combine_kernel(const Prefil
 
 cudaError_t launch_prefill_split_combine(const PrefillParams &p, int d, cudaStream_t stream) {
   const size_t rows = static_cast<size_t>(p.B) * p.N * p.H;
-  const unsigned grid = static_cast<unsigned>((rows + 3) / 4);
-  if (d == 64)
-    prefill_split_combine_kernel<64><<<grid, 128, 0, stream>>>(p);
-  else
-    prefill_split_combine_kernel<128><<<grid, 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  // launched as a programmatic dependent of the split grid on the same stream
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (d == 64) return cudaLaunchKernelEx(&cfg, prefill_split_combine_kernel<64>, p);
+  return cudaLaunchKernelEx(&cfg, prefill_split_combine_kernel<128>, p);
 }
 
 // ------------------------------------------------------------------ launch

@@ -170,6 +170,18 @@ __device__ __forceinline__ void tma_store_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Programmatic dependent launch.  A primary grid's CTA lets the dependent
+// grid (launched with programmatic stream serialization) be scheduled once
+// every CTA of the primary has called this or exited; the dependent grid's
+// threads wait in pdl_wait_primary until the whole primary grid has completed
+// and its memory operations are visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Barrier over `count` threads of the CTA (ids 1.. ; id 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
