@@ -146,3 +146,34 @@ def test_fp8_host_validation(lib):
     assert call(d=64) == -2
     assert call(H=3, Hkv=2) == -1
     assert call(N=0) == 0
+
+
+def test_status_bits_match_the_binding():
+    """The FA_DEV_* bits of include/fa.h and the binding's constants agree."""
+    import exact_attention_33_gb300 as fa
+    text = open(HEADER).read()
+    bits = dict((name, int(val)) for name, val in
+                re.findall(r"#define\s+(FA_DEV_[A-Z_]+)\s+(\d+)u", text))
+    assert set(bits) == {"FA_DEV_TIMEOUT", "FA_DEV_BAD_BLOCK", "FA_DEV_BAD_CTX",
+                         "FA_DEV_BAD_SEQLEN", "FA_DEV_BAD_INDEX"}
+    for name, val in bits.items():
+        assert getattr(fa, name) == val, name
+    assert len(set(bits.values())) == len(bits)
+    assert all(v & (v - 1) == 0 for v in bits.values())   # one bit each
+
+
+def test_binding_rejects_host_tensors_before_any_call():
+    """Tensors in host memory are refused by the binding itself (no launch,
+    no device pointer taken)."""
+    torch = pytest.importorskip("torch")
+    import exact_attention_33_gb300 as fa
+    q = torch.zeros((1, 8, 2, 64), dtype=torch.bfloat16)
+    for call in (lambda: fa.fa_fwd(q, q, q),
+                 lambda: fa.fa_fwd_splitkv(q, q, q),
+                 lambda: fa.fa_bwd(q, q, q, q, torch.zeros(1, 2, 8), q),
+                 lambda: fa.fa_fwd_varlen(q[0], q[0], q[0],
+                                          torch.tensor([0, 8], dtype=torch.int32), 8),
+                 lambda: fa.fa_decode_paged(q[0], q, q, torch.zeros((8, 1), dtype=torch.int32),
+                                            torch.ones(8, dtype=torch.int32), 1)):
+        with pytest.raises(ValueError):
+            call()
