@@ -274,8 +274,13 @@ int fa_fwd(const void *q, const void *k, const void *v, void *out, float *lse, i
   if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (B == 0 || N == 0) return FA_OK;
-  const long long pairs = (N + kPrefillRowsPerCta - 1) / kPrefillRowsPerCta;
-  const long long grid = pairs * B * H;
+  // With an even GQA group a CTA holds two query heads of one KV group over
+  // the same 128 rows (both tiles share every K/V stage and key tile);
+  // otherwise two consecutive 128-row tiles of one head.
+  const bool head_pairs = (H / Hkv) % 2 == 0;
+  const int rows = head_pairs ? kPrefillBM : kPrefillRowsPerCta;  // rows per work item
+  const long long pairs = (N + rows - 1) / rows;
+  const long long grid = pairs * B * (head_pairs ? H / 2 : H);
   if (grid > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(N) * H * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
 
@@ -296,14 +301,15 @@ int fa_fwd(const void *q, const void *k, const void *v, void *out, float *lse, i
   p.H = H;
   p.Hkv = Hkv;
   p.group = H / Hkv;
-  p.head_group = prefill_head_group(H);
+  p.head_group = head_pairs ? 2 * prefill_head_group(H / 2) : prefill_head_group(H);
   p.N = N;
   p.max_pairs = static_cast<int>(pairs);
   p.total_tokens = 0;
   p.scale_log2 = scale * kLog2e;
   p.v_descale = 1.f;
   p.causal = causal;
-  cudaError_t e = launch_prefill(tq, tk, tv, tv, to, p, d, causal != 0, kKindDense,
+  cudaError_t e = launch_prefill(tq, tk, tv, tv, to, p, d, causal != 0,
+                                 head_pairs ? kKindDenseHeads : kKindDense,
                                  static_cast<int>(grid), reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -322,19 +328,26 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float 
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (num_seqs == 0 || total_tokens == 0 || max_seqlen == 0) return FA_OK;
   if (max_seqlen > total_tokens) max_seqlen = total_tokens;
-  // Batches of short sequences (under 4096 rows on average) run one query
-  // tile per CTA, two CTAs per SM: their CTAs are short, and the second CTA
-  // hides each one's launch, set-up and epilogue.  Longer sequences keep two
-  // query tiles per CTA, whose shared K/V stages make the key loop faster.
-  const int qtiles = (static_cast<long long>(total_tokens) < 4096LL * num_seqs) ? 1 : 2;
-  const int rows = kPrefillBM * qtiles;
+  // Work layouts of a packed batch.  With an even GQA group a CTA pairs two
+  // query heads of one KV group over the same 128 rows: the two tiles share
+  // every K/V stage and have the same key tiles (3-5% faster than the other
+  // layouts at every length measured).  Otherwise batches of short sequences
+  // (under 4096 rows on average) run one query tile per CTA, two CTAs per SM,
+  // and longer sequences pair two consecutive 128-row tiles of one head.
+  constexpr int kRowsOne = 0, kRowPairs = 1, kHeadPairs = 2;
+  const bool short_seqs = static_cast<long long>(total_tokens) < 4096LL * num_seqs;
+  const int layout = ((H / Hkv) % 2 == 0) ? kHeadPairs : (short_seqs ? kRowsOne : kRowPairs);
+  const int qtiles = layout == kRowsOne ? 1 : 2;
+  const int rows = layout == kRowPairs ? 2 * kPrefillBM : kPrefillBM;  // rows per work item
+  const int slots = layout == kHeadPairs ? H / 2 : H;                 // head slots per row block
   const long long pairs = (max_seqlen + rows - 1) / rows;
-  long long grid = pairs * num_seqs * H;
+  long long grid = pairs * num_seqs * slots;
   // Padding-free order: sum over sequences of ceil(len / rows) is at most
-  // ceil(T / rows) + num_seqs, so that many items per head cover every row.
+  // ceil(T / rows) + num_seqs, so that many items per head slot cover every row.
   const bool compact = num_seqs <= kVarlenCompactMaxSeqs;
   if (compact)
-    grid = std::min(grid, ((total_tokens + rows - 1) / rows + static_cast<long long>(num_seqs)) * H);
+    grid = std::min(grid,
+                    ((total_tokens + rows - 1) / rows + static_cast<long long>(num_seqs)) * slots);
   if (grid > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(total_tokens) * H * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
 
@@ -355,7 +368,8 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float 
   p.H = H;
   p.Hkv = Hkv;
   p.group = H / Hkv;
-  p.head_group = prefill_head_group(H);
+  // heads per CTA-ordering group; a whole number of head pairs for that layout
+  p.head_group = layout == kHeadPairs ? 2 * prefill_head_group(H / 2) : prefill_head_group(H);
   p.N = total_tokens;
   p.max_pairs = static_cast<int>(pairs);
   p.compact = compact ? 1 : 0;
@@ -363,7 +377,8 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float 
   p.scale_log2 = scale * kLog2e;
   p.v_descale = 1.f;
   p.causal = causal;
-  cudaError_t e = launch_prefill(tq, tk, tv, tv, to, p, d, causal != 0, kKindVarlen,
+  cudaError_t e = launch_prefill(tq, tk, tv, tv, to, p, d, causal != 0,
+                                 layout == kHeadPairs ? kKindVarlenHeads : kKindVarlen,
                                  static_cast<int>(grid), reinterpret_cast<cudaStream_t>(stream),
                                  qtiles);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;

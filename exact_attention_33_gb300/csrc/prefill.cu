@@ -84,8 +84,9 @@ struct PrefillLayout {
 // fastest.  A sequence of len rows owns H * ceil(len / 256) items, so the
 // grid needs no item per (sequence, pair) that has no rows.  Every warp
 // finds its item with one pass over cu_seqlens, 32 sequences at a time
-// (all lanes active).  Returns false past the last item.
-template <int ROWS>
+// (all lanes active).  Returns false past the last item.  Items count ROWS
+// query rows by HSTEP heads (h is the first of them).
+template <int ROWS, int HSTEP>
 __device__ __forceinline__ bool varlen_compact_item(const PrefillParams &p, int lin, bool causal,
                                                     int &unit, int &pair, int &h) {
   const int lane = threadIdx.x & 31;
@@ -107,7 +108,7 @@ __device__ __forceinline__ bool varlen_compact_item(const PrefillParams &p, int 
       const int n = min(max(e - a, 0), p.total_tokens);
       np = (n + ROWS - 1) / ROWS;
     }
-    const int mine = np * p.H;  // items of sequence s
+    const int mine = np * (p.H / HSTEP);  // items of sequence s
     int incl = mine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -120,9 +121,9 @@ __device__ __forceinline__ bool varlen_compact_item(const PrefillParams &p, int 
       unit = s0 + l;
       const int lu = lin - base - __shfl_sync(0xffffffffu, incl - mine, l);
       const int nps = __shfl_sync(0xffffffffu, np, l);
-      const int hgs = p.head_group;
+      const int hgs = p.head_group / HSTEP;  // head slots per ordering group
       const int rem = lu % (hgs * nps);
-      h = (lu / (hgs * nps)) * hgs + rem % hgs;
+      h = ((lu / (hgs * nps)) * hgs + rem % hgs) * HSTEP;
       pair = causal ? (nps - 1 - rem / hgs) : rem / hgs;
       return true;
     }
@@ -156,27 +157,37 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
   // pairs with the most key tiles come first in every group.
   // Split-KV layout: the split index varies fastest; each split owns a
   // contiguous slice of the key tiles and writes partial (m, l, o) states.
+  // Head pairs (kKindVarlenHeads): query tile i is head h + i over the same
+  // 128 rows, both heads of one KV group; otherwise tile i covers rows
+  // [row0 + 128 i, row0 + 128 i + 128) of head h.
+  constexpr bool HP = KIND == kKindVarlenHeads || KIND == kKindDenseHeads;
+  constexpr bool DENSE = KIND == kKindDense || KIND == kKindDenseHeads;  // [B, N, H, d] rows
+  static_assert(!HP || QT == 2, "head pairs hold two query tiles");
+  constexpr int kCtaRows = HP ? kPrefillBM : Sh::kRows;  // query rows per work item
+  constexpr int kHeadStep = HP ? 2 : 1;                   // heads per work item
   const int split = (KIND == kKindDenseSplit) ? static_cast<int>(blockIdx.x % p.num_splits) : 0;
   const int lin = (KIND == kKindDenseSplit) ? static_cast<int>(blockIdx.x / p.num_splits)
                                             : static_cast<int>(blockIdx.x);
   int h, unit, pair;  // unit: batch element or sequence
-  if (KIND == kKindVarlen && p.compact) {
-    if (!varlen_compact_item<Sh::kRows>(p, lin, CAUSAL, unit, pair, h)) return;  // past the last item
+  if ((KIND == kKindVarlen || KIND == kKindVarlenHeads) && p.compact) {
+    if (!varlen_compact_item<kCtaRows, kHeadStep>(p, lin, CAUSAL, unit, pair, h))
+      return;  // past the last item
   } else {
-    const int hgs = p.head_group;
+    const int hgs = p.head_group / kHeadStep;  // head slots per ordering group
+    const int slots = p.H / kHeadStep;
     const int h_in = lin % hgs;
     const int t_lin = lin / hgs;
     const int pair_rank = t_lin % p.max_pairs;
     const int grp = t_lin / p.max_pairs;
-    h = (grp % (p.H / hgs)) * hgs + h_in;
-    unit = grp / (p.H / hgs);
+    h = ((grp % (slots / hgs)) * hgs + h_in) * kHeadStep;
+    unit = grp / (slots / hgs);
     pair = CAUSAL ? (p.max_pairs - 1 - pair_rank) : pair_rank;
   }
   // len: query rows of the unit; kv_len: its keys; offset = kv_len - len
   // aligns causal masking to the bottom right (query i sees keys
   // j <= i + offset).
   int b, seq_start, len, kv_len, offset;
-  if (KIND == kKindDense || KIND == kKindDenseSplit) {
+  if (DENSE || KIND == kKindDenseSplit) {
     b = unit;
     seq_start = 0;
     len = p.N;
@@ -194,7 +205,7 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
       raise_status(p.status, FA_DEV_BAD_SEQLEN);  // longer than max_seqlen (the padded order
                                                   // misses its tail)
     b = 0;
-    if (KIND == kKindVarlen) {
+    if (KIND == kKindVarlen || KIND == kKindVarlenHeads) {
       kv_len = len;
       offset = 0;
     } else {
@@ -207,14 +218,17 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
       offset = kv_len - len;
     }
   }
-  const int row0 = pair * Sh::kRows;
+  const int row0 = pair * kCtaRows;
   if (row0 >= len) return;  // no padding work: the whole CTA leaves before any set-up
+  // first query row (within the sequence) and head of query tile i
+  auto tile_row = [&](int i) { return HP ? row0 : row0 + i * kPrefillBM; };
+  auto tile_head = [&](int i) { return HP ? h + i : h; };
 
   const int n_kv_all = (kv_len + kPrefillBN - 1) / kPrefillBN;
   int kv_end[kPrefillQTiles];
 #pragma unroll
   for (int i = 0; i < kPrefillQTiles; ++i) {
-    const int t0 = row0 + i * kPrefillBM;
+    const int t0 = tile_row(i);
     if (i >= QT || t0 >= len) {
       kv_end[i] = 0;
     } else {
@@ -240,7 +254,7 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
     for (int i = 0; i < kPrefillQTiles; ++i) kv_end[i] = max(0, min(kv_end[i], stop) - kv0);
   }
   const int n_kv = max(kv_end[0], kv_end[1]);
-  const bool live1 = QT == 2 && row0 + kPrefillBM < len;  // the second query tile has rows
+  const bool live1 = QT == 2 && tile_row(1) < len;  // the second query tile has rows
 
   // ---------------------------------------------------------- shared memory
   extern __shared__ uint8_t smem_raw[];
@@ -295,11 +309,11 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
     const int nq = live1 ? 2 : 1;
     mbar_arrive_expect_tx(q_full, nq * L::kTileBytes);
     for (int i = 0; i < nq; ++i) {
-      const int qrow = seq_start + row0 + i * kPrefillBM;
+      const int qrow = seq_start + tile_row(i);
 #pragma unroll
       for (int c = 0; c < L::kChunks; ++c)
         tma_load_4d(sQ + i * L::kTileBytes + c * L::kChunkBytes, &tm_q, q_full,
-                    c * L::kChunkElems, h, qrow, b);
+                    c * L::kChunkElems, tile_head(i), qrow, b);
     }
     if (k0_early) {
       mbar_arrive_expect_tx(&k_full[0], L::kTileBytes);
@@ -620,7 +634,8 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem + i * 128 + lane_off;
     const uint32_t tO = tmem + L::kTmemO + i * D + lane_off;
-    const int qi = row0 + i * kPrefillBM + row;  // query row within the sequence
+    const int qi = tile_row(i) + row;  // query row within the sequence
+    const int hi = tile_head(i);       // query head of this tile
     const int my_end = kv_end[i];
     const float sl2 = p.scale_log2;
     const float2 sl2x2 = make_float2(sl2, sl2);
@@ -826,7 +841,7 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
         // partial tile of a packed layout, whose tail rows belong to the next
         // sequence, is written row by row instead.
         const bool tma_out =
-            !FP8 && (KIND == kKindDense || row0 + (i + 1) * kPrefillBM <= len);
+            !FP8 && (DENSE || tile_row(i) + kPrefillBM <= len);
         if (tma_out) {
           // All four warps of the tile meet at the barrier below (my_end and
           // tma_out are the same for the whole tile); a warp whose wait gave
@@ -857,26 +872,26 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
           fence_proxy_async_smem();
           named_bar_sync(1 + i, 128);
           if (row == 0 && ok) {
-            const int orow = (KIND == kKindDense ? 0 : seq_start) + row0 + i * kPrefillBM;
+            const int orow = (DENSE ? 0 : seq_start) + tile_row(i);
 #pragma unroll
             for (int c = 0; c < L::kChunks; ++c)
-              tma_store_4d(&tm_o, stile + c * L::kChunkBytes, c * L::kChunkElems, h, orow, b);
+              tma_store_4d(&tm_o, stile + c * L::kChunkBytes, c * L::kChunkElems, hi, orow, b);
             tma_store_commit();
             tma_store_wait_read();
           }
         }
         size_t out_row;
-        if (KIND != kKindDense)
+        if (!DENSE)
           out_row = static_cast<size_t>(seq_start + qi);
         else
           out_row = static_cast<size_t>(b) * p.N + qi;
         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.out) +
-                                               ((out_row * p.H + h) * D) * 2);
+                                               ((out_row * p.H + hi) * D) * 2);
         // rows of the output (and of the log-sum-exp) the call owns
         const size_t out_rows =
-            (KIND == kKindDense) ? static_cast<size_t>(p.B) * p.N : static_cast<size_t>(p.total_tokens);
+            DENSE ? static_cast<size_t>(p.B) * p.N : static_cast<size_t>(p.total_tokens);
         const bool row_ok =
-            !live || tma_out || in_bounds((out_row * p.H + h) * D, D, out_rows * p.H * D, p.status);
+            !live || tma_out || in_bounds((out_row * p.H + hi) * D, D, out_rows * p.H * D, p.status);
 #pragma unroll
         for (int c = 0; ok && !tma_out && c < D / 32; ++c) {
           uint32_t o[32];
@@ -897,9 +912,9 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
             }
           }
         }
-        const size_t lse_idx = (KIND != kKindDense)
-                                   ? static_cast<size_t>(h) * p.total_tokens + seq_start + qi
-                                   : (static_cast<size_t>(b) * p.H + h) * p.N + qi;
+        const size_t lse_idx = !DENSE
+                                   ? static_cast<size_t>(hi) * p.total_tokens + seq_start + qi
+                                   : (static_cast<size_t>(b) * p.H + hi) * p.N + qi;
         if (ok && live && p.lse != nullptr && in_bounds(lse_idx, 1, out_rows * p.H, p.status)) {
           p.lse[lse_idx] = (l_exact > 0.f) ? (m + __log2f(l_exact)) * 0.69314718055994530942f
                                            : -CUDART_INF_F;
@@ -1073,6 +1088,10 @@ cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const C
       return launch_prefill_k<64, kKindDense>(tq, tk, tv, tv1, to, p, causal, grid, stream);
     if (kind == kKindVarlen)
       return launch_prefill_k<64, kKindVarlen>(tq, tk, tv, tv1, to, p, causal, grid, stream);
+    if (kind == kKindVarlenHeads)
+      return launch_prefill_k<64, kKindVarlenHeads>(tq, tk, tv, tv1, to, p, causal, grid, stream);
+    if (kind == kKindDenseHeads)
+      return launch_prefill_k<64, kKindDenseHeads>(tq, tk, tv, tv1, to, p, causal, grid, stream);
     if (kind == kKindDenseSplit)
       return launch_prefill_k<64, kKindDenseSplit>(tq, tk, tv, tv1, to, p, causal, grid, stream);
     return launch_prefill_k<64, kKindPaged>(tq, tk, tv, tv1, to, p, causal, grid, stream);
@@ -1081,6 +1100,10 @@ cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const C
     return launch_prefill_k<128, kKindDense>(tq, tk, tv, tv1, to, p, causal, grid, stream);
   if (kind == kKindVarlen)
     return launch_prefill_k<128, kKindVarlen>(tq, tk, tv, tv1, to, p, causal, grid, stream);
+  if (kind == kKindVarlenHeads)
+    return launch_prefill_k<128, kKindVarlenHeads>(tq, tk, tv, tv1, to, p, causal, grid, stream);
+  if (kind == kKindDenseHeads)
+    return launch_prefill_k<128, kKindDenseHeads>(tq, tk, tv, tv1, to, p, causal, grid, stream);
   if (kind == kKindDenseSplit)
     return launch_prefill_k<128, kKindDenseSplit>(tq, tk, tv, tv1, to, p, causal, grid, stream);
   return launch_prefill_k<128, kKindPaged>(tq, tk, tv, tv1, to, p, causal, grid, stream);

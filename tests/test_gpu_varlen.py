@@ -32,13 +32,16 @@ def run_varlen(fa, inp, causal):
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_varlen_ragged(fa, d, causal):
+@pytest.mark.parametrize("H,Hkv", [(4, 2), (8, 2), (3, 1)])
+def test_varlen_ragged(fa, d, causal, H, Hkv):
+    """Short sequences: an even GQA group pairs two query heads per CTA (H 4
+    and 8), an odd one runs one query tile per CTA (H 3 over one KV head)."""
     lengths = [1, 5, 128, 129, 300, 0, 700, 256, 2]
-    inp = W.varlen_inputs(lengths, 4, 2, d, seed=30)
+    inp = W.varlen_inputs(lengths, H, Hkv, d, seed=30 + H)
     out, lse = run_varlen(fa, inp, causal)
     o_ref, l_ref = oracle.attention_varlen(f64(inp.q), f64(inp.k), f64(inp.v), inp.cu_seqlens,
                                            causal=causal)
-    compare(out, o_ref, lse, l_ref, f"varlen d{d} causal={causal}")
+    compare(out, o_ref, lse, l_ref, f"varlen H{H}/{Hkv} d{d} causal={causal}")
     assert_device_clean()
 
 
