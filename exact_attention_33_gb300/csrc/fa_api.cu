@@ -574,8 +574,11 @@ int fa_fwd_paged(const void *q, const void *k_pool, const void *v_pool,
   if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (batch == 0 || total_q == 0 || max_seqlen_q == 0) return FA_OK;
   if (max_seqlen_q > total_q) max_seqlen_q = total_q;
-  const long long pairs = (max_seqlen_q + kPrefillRowsPerCta - 1) / kPrefillRowsPerCta;
-  const long long grid = pairs * batch * H;
+  // with an even GQA group, two query heads of one KV group per CTA (as in fa_fwd)
+  const bool head_pairs = (H / Hkv) % 2 == 0;
+  const int rows = head_pairs ? kPrefillBM : kPrefillRowsPerCta;  // query rows per work item
+  const long long pairs = (max_seqlen_q + rows - 1) / rows;
+  const long long grid = pairs * batch * (head_pairs ? H / 2 : H);
   if (grid > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(total_q) * H * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
 
@@ -598,7 +601,7 @@ int fa_fwd_paged(const void *q, const void *k_pool, const void *v_pool,
   p.H = H;
   p.Hkv = Hkv;
   p.group = H / Hkv;
-  p.head_group = prefill_head_group(H);
+  p.head_group = head_pairs ? 2 * prefill_head_group(H / 2) : prefill_head_group(H);
   p.N = total_q;
   p.max_pairs = static_cast<int>(pairs);
   p.total_tokens = total_q;
@@ -610,7 +613,8 @@ int fa_fwd_paged(const void *q, const void *k_pool, const void *v_pool,
   p.max_blocks_per_seq = max_blocks_per_seq;
   p.max_ctx_len = max_ctx_len;
   p.num_blocks = num_blocks;
-  cudaError_t e = launch_prefill(tq, tk, tv, tv1, to, p, d, causal != 0, kKindPaged,
+  cudaError_t e = launch_prefill(tq, tk, tv, tv1, to, p, d, causal != 0,
+                                 head_pairs ? kKindPagedHeads : kKindPaged,
                                  static_cast<int>(grid), reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

@@ -55,6 +55,7 @@ constexpr int kKindDenseSplit = 3;  // dense batch, key tiles split over CTAs
 constexpr int kKindVarlenHeads = 4;  // packed sequences; a CTA's two query tiles are two heads
                                      // of one KV group over the same 128 rows
 constexpr int kKindDenseHeads = 5;   // dense batch, the same head pairs
+constexpr int kKindPagedHeads = 6;   // paged KV cache, the same head pairs
 
 // Packed batches of at most this many sequences use the padding-free order
 // of work items (each CTA finds its item with one pass over cu_seqlens).

@@ -160,7 +160,9 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
   // Head pairs (kKindVarlenHeads): query tile i is head h + i over the same
   // 128 rows, both heads of one KV group; otherwise tile i covers rows
   // [row0 + 128 i, row0 + 128 i + 128) of head h.
-  constexpr bool HP = KIND == kKindVarlenHeads || KIND == kKindDenseHeads;
+  constexpr bool HP =
+      KIND == kKindVarlenHeads || KIND == kKindDenseHeads || KIND == kKindPagedHeads;
+  constexpr bool PAGED = KIND == kKindPaged || KIND == kKindPagedHeads;  // K/V through a block table
   constexpr bool DENSE = KIND == kKindDense || KIND == kKindDenseHeads;  // [B, N, H, d] rows
   static_assert(!HP || QT == 2, "head pairs hold two query tiles");
   constexpr int kCtaRows = HP ? kPrefillBM : Sh::kRows;  // query rows per work item
@@ -280,7 +282,7 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
   uint8_t *sV = smem + L::kV;
   const int kvh = h / p.group;
   // Dense kinds: K(0) is copied with Q, before the block-wide set-up ends.
-  const bool k0_early = (KIND != kKindPaged) && n_kv > 0;
+  const bool k0_early = !PAGED && n_kv > 0;
 
   if (warp == Sh::kTmaWarp && lane == 0) {
     // The producer thread initialises the barriers and starts the Q copies
@@ -305,7 +307,7 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
-    if (KIND == kKindPaged) tma_prefetch_desc(&tm_v1);
+    if (PAGED) tma_prefetch_desc(&tm_v1);
     const int nq = live1 ? 2 : 1;
     mbar_arrive_expect_tx(q_full, nq * L::kTileBytes);
     for (int i = 0; i < nq; ++i) {
@@ -327,7 +329,7 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
     tmem_alloc(tmem_slot, L::kTmemCols);
     tmem_relinquish();
   }
-  if (KIND == kKindPaged) {
+  if (PAGED) {
     // Rows of a V stage that no load fills (keys past the context in the last
     // key tile) must hold finite values: P is 0 there, but 0 * NaN is NaN.
     uint4 *z = reinterpret_cast<uint4 *>(smem + L::kV);
@@ -344,7 +346,7 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
   // One query tile per CTA: this warpgroup (MMA, TMA, two idle warps) hands
   // registers to the softmax warpgroup.
   if constexpr (QT == 1) setmaxnreg_dec<kPrefill1CtlRegs>();
-  if (warp == Sh::kTmaWarp && KIND == kKindPaged) {
+  if (warp == Sh::kTmaWarp && PAGED) {
     // ------------------------------------------------------ TMA producer, paged
     // The warp runs converged: lanes 0..7 look up the 8 physical blocks of a
     // 128-key tile in the block table, lane 0 issues the copies.  A block
@@ -593,7 +595,7 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
         // paged K may still be in flight, so that kind waits for K(j+1)
         // only before the S MMAs that read it.
         if (!mbar_wait_warp(&v_full[sv], (j / SV) & 1, abort_flag, p.status)) break;
-        if (KIND != kKindPaged && SK > 1 && j + 1 < n_kv && !wait_k_next()) break;
+        if (!PAGED && SK > 1 && j + 1 < n_kv && !wait_k_next()) break;
         tc_fence_after();
         if (j < kv_end[0]) {
           if (!mbar_wait_warp(&p_full[0], j & 1, abort_flag, p.status)) break;
@@ -1094,6 +1096,8 @@ cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const C
       return launch_prefill_k<64, kKindDenseHeads>(tq, tk, tv, tv1, to, p, causal, grid, stream);
     if (kind == kKindDenseSplit)
       return launch_prefill_k<64, kKindDenseSplit>(tq, tk, tv, tv1, to, p, causal, grid, stream);
+    if (kind == kKindPagedHeads)
+      return launch_prefill_k<64, kKindPagedHeads>(tq, tk, tv, tv1, to, p, causal, grid, stream);
     return launch_prefill_k<64, kKindPaged>(tq, tk, tv, tv1, to, p, causal, grid, stream);
   }
   if (kind == kKindDense)
@@ -1106,6 +1110,8 @@ cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const C
     return launch_prefill_k<128, kKindDenseHeads>(tq, tk, tv, tv1, to, p, causal, grid, stream);
   if (kind == kKindDenseSplit)
     return launch_prefill_k<128, kKindDenseSplit>(tq, tk, tv, tv1, to, p, causal, grid, stream);
+  if (kind == kKindPagedHeads)
+    return launch_prefill_k<128, kKindPagedHeads>(tq, tk, tv, tv1, to, p, causal, grid, stream);
   return launch_prefill_k<128, kKindPaged>(tq, tk, tv, tv1, to, p, causal, grid, stream);
 }
 

@@ -49,10 +49,12 @@ CASES = [(1, 1), (17, 17), (100, 37), (2048, 300), (5000, 1), (129, 129), (3, 10
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [True, False])
-def test_paged_prefill_ragged(fa, d, causal):
+@pytest.mark.parametrize("H,Hkv", [(8, 2), (3, 1)])
+def test_paged_prefill_ragged(fa, d, causal, H, Hkv):
+    """GQA 8 / 2 pairs two query heads per CTA; 3 / 1 pairs two row tiles."""
     ctx = [c for c, _ in CASES]
     ql = [n for _, n in CASES]
-    inp = W.paged_prefill_inputs(ctx, ql, 8, 2, d, seed=50, extra_blocks=3)
+    inp = W.paged_prefill_inputs(ctx, ql, H, Hkv, d, seed=50 + H, extra_blocks=3)
     out, lse = run(fa, inp, causal)
     o_ref, l_ref = ref(inp, causal)
     compare(out, o_ref, lse, l_ref, f"paged prefill d{d} causal={causal}")
