@@ -203,9 +203,10 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
       return;
     }
     len = seq_end - seq_start;
-    if (len > p.max_pairs * Sh::kRows && pair == 0 && h == 0)
-      raise_status(p.status, FA_DEV_BAD_SEQLEN);  // longer than max_seqlen (the padded order
-                                                  // misses its tail)
+    // Longer than max_seqlen: a grid sized from it cannot cover the sequence.
+    // Any item of head 0 reports it; the sequence's first item, which is one,
+    // is launched whenever the sequences before it respect max_seqlen.
+    if (len > p.max_pairs * kCtaRows && h == 0) raise_status(p.status, FA_DEV_BAD_SEQLEN);
     b = 0;
     if (KIND == kKindVarlen || KIND == kKindVarlenHeads) {
       kv_len = len;

@@ -115,3 +115,25 @@ def test_varlen_bad_cu_seqlens_flagged(fa):
     fa.fa_fwd_varlen(dev_bf16(inp.q), dev_bf16(inp.k), dev_bf16(inp.v), dev_i32(bad), 25)
     torch.cuda.synchronize()
     assert fa.fa_device_status(clear=True) & fa.FA_DEV_BAD_SEQLEN
+
+
+@pytest.mark.parametrize("H,Hkv", [(4, 2), (3, 1)])
+def test_varlen_max_seqlen_too_small_is_flagged(fa, H, Hkv):
+    """A sequence longer than the max_seqlen the caller states (200 rows
+    against 100) cannot be covered by a grid sized from it: the call sets
+    FA_DEV_BAD_SEQLEN, with head pairs (H 4 / 2) and one tile per CTA (3 / 1)
+    alike.  The same batch with the true maximum matches the oracle."""
+    torch = torch_mod()
+    inp = W.varlen_inputs([100, 200], H, Hkv, 64, seed=36 + H)
+    q, k, v, cu = dev_bf16(inp.q), dev_bf16(inp.k), dev_bf16(inp.v), dev_i32(inp.cu_seqlens)
+    fa.fa_device_status(clear=True)
+    fa.fa_fwd_varlen(q, k, v, cu, 100, causal=True)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(clear=True) & fa.FA_DEV_BAD_SEQLEN
+    out, lse = fa.fa_fwd_varlen(q, k, v, cu, 200, causal=True)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.attention_varlen(f64(inp.q), f64(inp.k), f64(inp.v), inp.cu_seqlens,
+                                           causal=True)
+    compare(host_f64(out), o_ref, lse.cpu().numpy().astype(np.float64), l_ref,
+            f"varlen H{H}/{Hkv} true max_seqlen")
+    assert_device_clean()
