@@ -24,10 +24,11 @@ Reported (one JSON line from rank 0):
            sample of the long-context workload
   next     the further rows (chunked prefill over a paged cache, split-KV
            prefill, FP8 prefill, the backward pass), each on its own workload
-  other_configs  the dense d = 64 configuration (B4 H16 N2048), causal and not
+  other_configs  the dense d = 64 configuration (B4 H16 N2048), causal and not, and
+           paged decode steps at small batches (latency and GB/s)
 
-The split-KV and d = 64 workloads fit in L2, so those two are timed launch by
-launch with L2 flushed (a 256 MiB write) before each launch.
+The split-KV, d = 64 and small-batch decode workloads fit in L2 (or nearly), so
+they are timed call by call with L2 flushed (a 256 MiB write) before each call.
 
 ``--impl reference`` times the oracle instead (the slow reference arm).
 Multi-GPU: one process per GPU (torchrun); every rank runs the full step on
@@ -535,6 +536,34 @@ def measure_dense_d64(torch, device, fa, steps, warmup):
     return res
 
 
+def measure_decode_small_batches(torch, device, fa, steps, warmup):
+    """Paged decode at serving batch sizes (32 query / 8 KV heads, d = 128,
+    16-token blocks, equal contexts): the latency of one step, L2 flushed
+    (a 256 MiB write) before each timed call, and its HBM rate."""
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    res = {"workload": "paged GQA decode steps at small batches (L2 flushed before each call)"}
+    for batch, ctx_len in ((1, 4096), (1, 32768), (8, 8192), (16, 32768)):
+        ctx = [ctx_len] * batch
+        inp = W.decode_inputs(ctx, 32, 8, 128, seed=1)
+        q = to_dev(inp.q, torch, device)
+        kp, vp = to_dev(inp.k_pool, torch, device), to_dev(inp.v_pool, torch, device)
+        table = torch.from_numpy(inp.block_table).to(device)
+        cl = torch.from_numpy(inp.ctx_lens).to(device)
+        out = torch.empty_like(q)
+        lse = torch.empty((batch, 32), dtype=torch.float32, device=device)
+        ws = torch.empty(fa.fa_decode_workspace_size(batch, 32, 8, 128, ctx_len),
+                         dtype=torch.uint8, device=device)
+        nbytes = W.decode_bytes(inp.ctx_lens, 32, 8, 128, inp.block_table.shape[1], 16)
+        ms = time_flushed(torch, lambda: fa.fa_decode_paged(q, kp, vp, table, cl, ctx_len,
+                                                            out=out, lse=lse, workspace=ws),
+                          steps, warmup, flush)
+        res[f"batch{batch}_ctx{ctx_len}"] = {"us": ms * 1e3, "gbs": nbytes / (ms / 1e3) / 1e9,
+                                             "bytes": nbytes}
+    if fa.fa_device_status(clear=True) != 0:
+        raise RuntimeError("device status word set during the small-batch decode leg")
+    return res
+
+
 NEXT_LEGS = ("paged_prefill", "splitkv", "fp8_prefill", "backward")
 
 
@@ -729,6 +758,8 @@ def bench_ours(args, rank, world, local):
                                      args.warmup, peaks0["bf16_tflops"])
         other["dense_d64"] = measure_dense_d64(torch, device, fa, min(args.steps, 50),
                                                args.warmup)
+        other["decode_small_batches"] = measure_decode_small_batches(
+            torch, device, fa, min(args.steps, 50), args.warmup)
 
     # ---- numbers (max over ranks of each time)
     K = args.steps
@@ -798,8 +829,8 @@ def bench_ours(args, rank, world, local):
             "decode_batch": args.decode_batch or 64,
             "prefill_flops_per_step": f_pre,
             "decode_bytes_per_step": dbytes,
-            "l2": "step inputs are larger than L2 (no flush needed); the split-KV and "
-                  "d=64 legs, which fit in L2, flush it before each timed launch",
+            "l2": "step inputs are larger than L2 (no flush needed); the split-KV, d=64 "
+                  "and small-batch decode legs flush it before each timed call",
             "parallelism": f"replicas x{world}",
         },
         "decode": None if dbytes is None else {
