@@ -177,3 +177,31 @@ def test_binding_rejects_host_tensors_before_any_call():
                                             torch.ones(8, dtype=torch.int32), 1)):
         with pytest.raises(ValueError):
             call()
+
+
+def test_profile_hash_covers_every_kernel_source():
+    """bench.py uses a committed ncu traffic figure only while the hash of the
+    kernel's sources matches the one in the summary; that hash must cover
+    every local header the kernel file includes, directly or through another
+    header."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    csrc = os.path.join(ROOT, "exact_attention_33_gb300", "csrc")
+
+    def closure(name, seen):
+        if name in seen:
+            return seen
+        seen.add(name)
+        for inc in re.findall(r'#include\s+"([^"]+)"', open(os.path.join(csrc, name)).read()):
+            if os.path.exists(os.path.join(csrc, inc)):
+                closure(inc, seen)
+        return seen
+
+    # The public header gives the kernels only the FA_DEV_* bit values, which
+    # test_status_bits_match_the_binding pins; its prose may change freely.
+    public = {"../../include/fa.h"}
+    for kind, main in (("prefill", "prefill.cu"), ("decode", "decode.cu")):
+        listed = {os.path.basename(p) for p in bench.KERNEL_SOURCES[kind]}
+        missing = closure(main, set()) - listed - public
+        assert not missing, f"{kind} hash misses {sorted(missing)}"
