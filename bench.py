@@ -123,6 +123,7 @@ def measured_peaks():
             p = json.load(f)
         return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
                 "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "sm_mhz_under_load": (p.get("clocks_under_load") or {}).get("sm_mhz_median"),
                 "source": "measured"}
     except Exception:
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
@@ -137,19 +138,31 @@ def source_sha(kind: str) -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kind: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel source (else None)."""
+def profiled_value(kind: str, pattern: str):
+    """A number from the committed ncu summary of the kernel (the first group
+    of ``pattern``), if the summary was taken on the current kernel source
+    (else None)."""
     name = {"prefill": "prefill_long_causal_d128.txt", "decode": "decode_paged_gqa_d128.txt"}[kind]
     path = os.path.join(PROFILES, name)
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m_sha = re.search(r"source_sha:\s*([0-9a-f]+)", text)
-    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_sha or not m_tr or m_sha.group(1) != source_sha(kind):
+    m_val = re.search(pattern, text)
+    if not m_sha or not m_val or m_sha.group(1) != source_sha(kind):
         return None
-    return float(m_tr.group(1))
+    return float(m_val.group(1))
+
+
+def profiled_traffic(kind: str):
+    """DRAM bytes per launch (ncu) of the kernel, or None."""
+    return profiled_value(kind, r"traffic_bytes_per_launch:\s*([0-9.eE+]+)")
+
+
+def profiled_tensor_active(kind: str):
+    """Fraction of elapsed cycles the tensor pipe was active (ncu), or None."""
+    v = profiled_value(kind, r"sm__pipe_tensor_cycles_active \(of elapsed\)\s+([0-9.]+)\s*%")
+    return None if v is None else v / 100.0
 
 
 class ClockSampler:
@@ -261,7 +274,7 @@ def build_step(torch, device, which=("long", "varlen", "decode"), decode_batch=N
         leg["lse"] = torch.empty(dq.shape[:2], dtype=torch.float32, device=device)
         ws = fa.fa_decode_workspace_size(dq.shape[0], dq.shape[1], leg["Hkv"], dq.shape[2],
                                          leg["max_ctx"], 16)
-        leg["ws"] = torch.empty(ws, dtype=torch.uint8, device=device)
+        leg["ws"] = fa.new_workspace(ws, device)
     return legs
 
 
@@ -465,12 +478,14 @@ def measure_backward(torch, device, fa, steps, warmup, peak):
 
 
 L2_FLUSH_BYTES = 256 << 20   # twice the GB300's L2
+SLEEP_CYCLES = 200_000        # ~0.1 ms of device time before each timed call
 
 
 def time_flushed(torch, fn, steps, warmup, flush):
     """Mean device time of fn() over `steps` calls, each timed alone with CUDA
     events on the current stream after `flush` (a buffer larger than L2) has
-    been rewritten, so no call finds its inputs or partial states in L2."""
+    been rewritten, so no call finds its inputs or partial states in L2.  The
+    time is the device's alone: fn() is enqueued before its start event runs."""
     for _ in range(warmup):
         fn()
     stream = torch.cuda.current_stream()
@@ -478,6 +493,9 @@ def time_flushed(torch, fn, steps, warmup, flush):
           for _ in range(steps)]
     for e0, e1 in ev:
         flush.zero_()
+        # a short device-side wait lets the host enqueue fn() before the start
+        # event is reached, so host launch overhead never enters the timing
+        torch.cuda._sleep(SLEEP_CYCLES)
         e0.record(stream)
         fn()
         e1.record(stream)
@@ -496,8 +514,7 @@ def measure_splitkv(torch, device, fa, steps, warmup, peak):
     q, k, v = (to_dev(getattr(inp, n), torch, device) for n in ("q", "k", "v"))
     out = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
-    ws = torch.empty(fa.fa_fwd_splitkv_workspace_size(B, H, N, d, 0), dtype=torch.uint8,
-                     device=device)
+    ws = fa.new_workspace(fa.fa_fwd_splitkv_workspace_size(B, H, N, d, 0), device)
     flops = W.prefill_flops(B, N, H, d, True)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     ms = time_flushed(torch, lambda: fa.fa_fwd_splitkv(q, k, v, causal=True, out=out, lse=lse,
@@ -512,11 +529,11 @@ def measure_splitkv(torch, device, fa, steps, warmup, peak):
             "launches_per_call": 2}
 
 
-def measure_dense_d64(torch, device, fa, steps, warmup):
+def measure_dense_d64(torch, device, fa, steps, warmup, modes=(False, True)):
     """The dense configuration of the workload list (B=4, H=Hkv=16, N=2048,
-    d=64, bf16 N(0,1)), non-causal and causal.  Its inputs fit in L2, so L2
-    is flushed (a 256 MiB write) before every timed launch and only the
-    launch is timed."""
+    d=64, bf16 N(0,1)), non-causal and causal (``modes``: the causal flags
+    to run).  Its inputs fit in L2, so L2 is flushed (a 256 MiB write)
+    before every timed launch and only the launch is timed."""
     cfg = W.WORKLOADS["dense_d64"]
     B, N, H, Hkv, d = cfg["B"], cfg["N"], cfg["H"], cfg["Hkv"], cfg["d"]
     inp = W.dense_inputs(B, N, H, Hkv, d, seed=0)
@@ -525,7 +542,7 @@ def measure_dense_d64(torch, device, fa, steps, warmup):
     lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     res = {"workload": "dense prefill B4 H16 N2048 d64 (L2 flushed before each launch)"}
-    for causal in (False, True):
+    for causal in modes:
         ms = time_flushed(torch, lambda: fa.fa_fwd(q, k, v, causal=causal, out=out, lse=lse),
                           steps, warmup, flush)
         flops = W.prefill_flops(B, N, H, d, causal)
@@ -551,8 +568,7 @@ def measure_decode_small_batches(torch, device, fa, steps, warmup):
         cl = torch.from_numpy(inp.ctx_lens).to(device)
         out = torch.empty_like(q)
         lse = torch.empty((batch, 32), dtype=torch.float32, device=device)
-        ws = torch.empty(fa.fa_decode_workspace_size(batch, 32, 8, 128, ctx_len),
-                         dtype=torch.uint8, device=device)
+        ws = fa.new_workspace(fa.fa_decode_workspace_size(batch, 32, 8, 128, ctx_len), device)
         nbytes = W.decode_bytes(inp.ctx_lens, 32, 8, 128, inp.block_table.shape[1], 16)
         ms = time_flushed(torch, lambda: fa.fa_decode_paged(q, kp, vp, table, cl, ctx_len,
                                                             out=out, lse=lse, workspace=ws),
@@ -565,11 +581,17 @@ def measure_decode_small_batches(torch, device, fa, steps, warmup):
 
 
 NEXT_LEGS = ("paged_prefill", "splitkv", "fp8_prefill", "backward")
+# legs that --profile-leg can run alone (one launch kind each, for ncu captures)
+PROFILE_LEGS = NEXT_LEGS + ("dense_d64", "dense_d64_causal", "decode_small")
 
 
 def run_next_leg(name, torch, device, fa, steps, warmup, peak):
     fn = {"paged_prefill": measure_paged_prefill, "splitkv": measure_splitkv,
-          "fp8_prefill": measure_fp8_prefill, "backward": measure_backward}[name]
+          "fp8_prefill": measure_fp8_prefill, "backward": measure_backward,
+          "dense_d64": lambda t, dv, f, s, w, pk: measure_dense_d64(t, dv, f, s, w, (False,)),
+          "dense_d64_causal": lambda t, dv, f, s, w, pk: measure_dense_d64(t, dv, f, s, w, (True,)),
+          "decode_small": lambda t, dv, f, s, w, pk: measure_decode_small_batches(t, dv, f, s, w),
+          }[name]
     res = fn(torch, device, fa, steps, warmup, peak)
     if fa.fa_device_status(clear=True) != 0:
         raise RuntimeError(f"device status word set during the {name} leg")
@@ -791,7 +813,12 @@ def bench_ours(args, rank, world, local):
         roof = {"bound": "tensor", "kernel": "prefill_kernel<128,causal> (long-context launch)",
                 "achieved": ach, "peak": tensor_peak, "unit": "TFLOP/s",
                 "frac": ach / tensor_peak, "traffic": profiled_traffic("prefill"),
-                "peak_source": peaks["source"] + (" sustained" if timed_s > 2.0 else " burst")}
+                "peak_source": peaks["source"] + (" sustained" if timed_s > 2.0 else " burst"),
+                # clock-independent view: the peak above is cuBLAS at the power-capped
+                # clock of its own measurement; the kernel ran at the sampled clock
+                "tensor_pipe_active_ncu": profiled_tensor_active("prefill"),
+                "peak_measured_at_sm_mhz": peaks.get("sm_mhz_under_load"),
+                "sm_mhz": clk.get("sm_mhz")}
     if "varlen" in order:
         f = legs["varlen"]["flops"]
         leg_info["varlen_causal_prefill"] = {"ms": 1e3 * t["varlen"] / K,
@@ -870,7 +897,7 @@ def main(argv=None):
                     help="skip the separately timed legs (paged prefill, split-KV, FP8, backward)")
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="use only the first B decode sequences (for profiling runs)")
-    ap.add_argument("--profile-leg", choices=NEXT_LEGS, default=None,
+    ap.add_argument("--profile-leg", choices=PROFILE_LEGS, default=None,
                     help="run only this separately timed leg, --steps times (for ncu runs)")
     args = ap.parse_args(argv)
     args.legs = [x for x in args.legs.split(",") if x]

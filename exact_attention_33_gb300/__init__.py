@@ -25,7 +25,8 @@ __all__ = [
     "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_fwd_fp8",
     "fa_bwd", "fa_bwd_workspace_size",
     "fa_decode_paged", "fa_decode_paged_noalloc", "fa_decode_workspace_size",
-    "fa_status_string", "fa_device_status",
+    "fa_status_string", "fa_device_status", "fa_last_device_status", "new_workspace",
+    "FA_WORKSPACE_HEADER_BYTES",
     "fa_version", "FA_DEV_TIMEOUT", "FA_DEV_BAD_BLOCK", "FA_DEV_BAD_CTX", "FA_DEV_BAD_SEQLEN",
     "FA_DEV_BAD_INDEX",
 ]
@@ -36,6 +37,7 @@ FA_DEV_BAD_BLOCK = 2
 FA_DEV_BAD_CTX = 4
 FA_DEV_BAD_SEQLEN = 8
 FA_DEV_BAD_INDEX = 16   # checked build only
+FA_WORKSPACE_HEADER_BYTES = 256   # control block at the start of a decode / split-KV workspace
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -99,6 +101,8 @@ def load_library() -> ctypes.CDLL:
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i]
         lib.fa_device_status.restype = i
+        lib.fa_last_device_status.argtypes = [vp]
+        lib.fa_last_device_status.restype = i
         lib.fa_selftest_wait_timeout.argtypes = [vp, vp]
         lib.fa_selftest_wait_timeout.restype = i
         lib.fa_version.argtypes = []
@@ -134,6 +138,30 @@ def fa_device_status(clear: bool = True) -> int:
     if rc != FA_OK:
         raise FaError("fa_device_status", rc)
     return int(v.value)
+
+
+def fa_last_device_status(workspace) -> int:
+    """FA_DEV_* bits of the last call that finished on ``workspace`` (a
+    decode or split-KV workspace).  Read it after that call has completed
+    (synchronise its stream first); it does not wait for other streams."""
+    torch = _torch()
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda \
+            or workspace.numel() * workspace.element_size() < FA_WORKSPACE_HEADER_BYTES:
+        raise ValueError("workspace must be a CUDA tensor of at least "
+                         f"{FA_WORKSPACE_HEADER_BYTES} bytes")
+    with torch.cuda.device(workspace.device):
+        rc = load_library().fa_last_device_status(_ptr(workspace))
+    if rc < 0:
+        raise FaError("fa_last_device_status", rc)
+    return int(rc)
+
+
+def new_workspace(nbytes: int, device=None):
+    """A decode or split-KV workspace of ``nbytes`` bytes, zero-filled as the
+    library requires before its first call."""
+    torch = _torch()
+    return torch.zeros(max(int(nbytes), FA_WORKSPACE_HEADER_BYTES), dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
 
 
 # ----------------------------------------------------------------- helpers
@@ -186,12 +214,14 @@ def _check_int32(name, t, device, ndim=1, numel=None):
         raise ValueError(f"{name} must hold {numel} values")
 
 
-def _workspace(t, need, device, minimum=1):
+def _workspace(t, need, device, minimum=1, zero=False):
     """The caller's workspace (a 1-D uint8 tensor, its length in bytes), or a
-    new one of at least ``need`` bytes."""
+    new one of at least ``need`` bytes (zero-filled with ``zero``: decode and
+    split-KV workspaces start with a control block that must be zero)."""
     torch = _torch()
     if t is None:
-        return torch.empty(max(need, minimum), dtype=torch.uint8, device=device)
+        alloc = torch.zeros if zero else torch.empty
+        return alloc(max(need, minimum), dtype=torch.uint8, device=device)
     if not isinstance(t, torch.Tensor) or t.device != device or t.dtype != torch.uint8 \
             or t.dim() != 1 or not t.is_contiguous():
         raise ValueError(f"workspace must be a contiguous 1-D uint8 tensor on {device}")
@@ -324,7 +354,7 @@ def fa_fwd_splitkv(q, k, v, causal=False, scale=None, num_splits=0, out=None, ls
     if k.shape != (B, N, Hkv, d) or v.shape != k.shape:
         raise ValueError("k and v must be [B, N, Hkv, d] matching q")
     workspace = _workspace(workspace, fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits),
-                           dev, 256)
+                           dev, 256, zero=True)
     out, lse = _outputs(q.shape, (B, H, N), out, lse, want_lse, dev)
     with torch.cuda.device(dev):
         rc = load_library().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B,
@@ -436,7 +466,8 @@ def fa_decode_paged(q, k_pool, v_pool, block_table, ctx_lens, max_ctx_len, scale
     dev, batch, H, Hkv, d, num_blocks, block_size = _decode_args(q, k_pool, v_pool,
                                                                  block_table, ctx_lens)
     workspace = _workspace(
-        workspace, fa_decode_workspace_size(batch, H, Hkv, d, max_ctx_len, block_size), dev, 256)
+        workspace, fa_decode_workspace_size(batch, H, Hkv, d, max_ctx_len, block_size), dev, 256,
+        zero=True)
     out, lse = _outputs(q.shape, (batch, H), out, lse, want_lse, dev)
     with torch.cuda.device(dev):
         rc = load_library().fa_decode_paged(

@@ -31,6 +31,8 @@
 #include <math_constants.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "fa_internal.h"
 #include "ptx.cuh"
 #include "checks.cuh"
@@ -347,22 +349,28 @@ __global__ void __launch_bounds__(32 * combine_cta_warps<W>())
   __shared__ float s_m[kWarps];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // this kernel's own (checked-build) index errors go to the device word only
+  unsigned int *status = p.dev_status;
   const int wr = warp % W;  // warp within the row
   const int r0 = warp - wr;  // first warp of the row
   const int gw = blockIdx.x * R + warp / W;
   // a CTA's last rows may lie past the end; they still meet the barriers
   const bool row_live = gw < p.batch * p.H;
   const int b = row_live ? gw / p.H : 0;
-  int ctx = row_live ? checked_load(p.ctx_lens, b, p.batch, p.status) : 0;
+  int ctx = row_live ? checked_load(p.ctx_lens, b, p.batch, status) : 0;
   if (ctx < 0 || ctx > p.max_ctx_len || ctx > p.max_blocks_per_seq * kDecodeBlock) ctx = 0;
   const int ns = (ctx + p.split_tokens - 1) / p.split_tokens;
   const size_t row0 = static_cast<size_t>(gw) * p.max_splits;
   const size_t part_rows = static_cast<size_t>(p.batch) * p.H * p.max_splits;
   pdl_wait_primary();  // the split grid's partial states are complete from here on
+  // The split grid has raised all its status bits: one thread reads them
+  // here and publishes them as the call's status when its row is done.
+  const bool publisher = blockIdx.x == 0 && threadIdx.x == 0 && p.call != nullptr;
+  const unsigned int call_bits = publisher ? call_status_bits(p.call) : 0u;
   // (m, l) of split i of this row (the neutral state if the index fails a
   // check of the checked build)
   auto ml = [&](int i) -> float2 {
-    return in_bounds(row0 + i, 1, part_rows, p.status)
+    return in_bounds(row0 + i, 1, part_rows, status)
                ? reinterpret_cast<const float2 *>(p.ml_part)[row0 + i]
                : make_float2(-CUDART_INF_F, 0.f);
   };
@@ -393,7 +401,7 @@ __global__ void __launch_bounds__(32 * combine_cta_warps<W>())
     };
     auto load_o = [&](int i, float (&v)[E]) {
       const float *orow = p.o_part + (row0 + i) * D + lane * E;
-      if (!in_bounds((row0 + i) * D + lane * E, E, part_rows * D, p.status)) {
+      if (!in_bounds((row0 + i) * D + lane * E, E, part_rows * D, status)) {
 #pragma unroll
         for (int e = 0; e < E; ++e) v[e] = 0.f;
         return;
@@ -446,7 +454,7 @@ __global__ void __launch_bounds__(32 * combine_cta_warps<W>())
   const float inv = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
   uint16_t *dst = static_cast<uint16_t *>(p.out) + static_cast<size_t>(gw) * D + lane * E;
   const bool out_ok = in_bounds(static_cast<size_t>(gw) * D + lane * E, E,
-                                static_cast<size_t>(p.batch) * p.H * D, p.status);
+                                static_cast<size_t>(p.batch) * p.H * D, status);
   if (out_ok && E == 4) {
     uint2 w;
     w.x = pack_bf16x2(acc[0] * inv, acc[1 % E] * inv);
@@ -456,8 +464,9 @@ __global__ void __launch_bounds__(32 * combine_cta_warps<W>())
     *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1 % E] * inv);
   }
   if (lane == 0 && p.lse != nullptr &&
-      in_bounds(gw, 1, static_cast<size_t>(p.batch) * p.H, p.status))
+      in_bounds(gw, 1, static_cast<size_t>(p.batch) * p.H, status))
     p.lse[gw] = (Lsum > 0.f) ? (M + __log2f(Lsum)) * 0.69314718055994530942f : -CUDART_INF_F;
+  if (publisher) publish_call_status(p.call, call_bits, p.dev_status);
 }
 
 // ------------------------------------------------------------------ launch
@@ -484,16 +493,21 @@ static cudaError_t launch_decode_t(const CUtensorMap &tk, const CUtensorMap &tv,
                                    const DecodeParams &p, cudaStream_t stream) {
   using L = DecodeLayout<D>;
   auto kern = decode_split_kernel<D, NT>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
+  // The shared-memory attribute is per device: set it once on each device
+  // (one bit per device id; ids past 63 set it on every launch).
+  static std::atomic<unsigned long long> attr_set{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit == 0ull || (attr_set.load(std::memory_order_acquire) & bit) == 0ull) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set.fetch_or(bit, std::memory_order_release);
   }
   dim3 grid(p.max_splits, p.Hkv, p.batch);
   kern<<<grid, 32, L::kSmemAlloc, stream>>>(tk, tv, p);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int rows = p.batch * p.H;
   if (p.max_splits > kCombineManySplits)

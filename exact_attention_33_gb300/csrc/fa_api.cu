@@ -10,6 +10,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstddef>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -35,6 +36,7 @@ cudaError_t launch_prefill_fp8(const CUtensorMap &tq, const CUtensorMap &tk,
                                int grid, cudaStream_t stream);
 cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
                           int d, cudaStream_t stream);
+cudaError_t launch_call_status(CallStatus *call, unsigned int *dev, cudaStream_t stream);
 
 namespace {
 
@@ -138,8 +140,8 @@ int decode_split_tokens(int batch, int Hkv, int max_ctx_len) {
   const long long want = 2LL * 7 * sms;
   int split = kDecodeMaxSplitTokens;
   while (split > 64) {
-    const long long items =
-        static_cast<long long>(batch) * Hkv * ((max_ctx_len + split - 1) / split);
+    const long long items = static_cast<long long>(batch) * Hkv *
+                            ((static_cast<long long>(max_ctx_len) + split - 1) / split);
     if (items >= want) break;
     split >>= 1;
   }
@@ -147,6 +149,9 @@ int decode_split_tokens(int batch, int Hkv, int max_ctx_len) {
 }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Context lengths above this are refused (the split arithmetic stays in int).
+constexpr int kMaxCtxLen = 0x7fffffff - kDecodeMaxSplitTokens;
 
 // Heads per group of the prefill CTA order: the largest divisor of H that is
 // at most 8 (consecutive heads, so GQA heads sharing a KV head stay together).
@@ -180,6 +185,7 @@ struct SplitWs {
   size_t o_bytes, ml_bytes;
 };
 
+// Split-KV workspace: control block, fp32 partial o tiles, (m, l, l_exact).
 SplitWs split_ws(int B, int H, int N, int d, int requested) {
   SplitWs w;
   w.splits = prefill_num_splits(B, H, N, requested);
@@ -189,6 +195,8 @@ SplitWs split_ws(int B, int H, int N, int d, int requested) {
   return w;
 }
 
+size_t split_ws_bytes(const SplitWs &w) { return FA_WORKSPACE_HEADER_BYTES + w.o_bytes + w.ml_bytes; }
+
 struct DecodeWs {
   int split_tokens;
   int max_splits;
@@ -196,10 +204,12 @@ struct DecodeWs {
   size_t ml_bytes;
 };
 
+// Decode workspace: control block, fp32 partial o rows, (m, l) pairs.
 DecodeWs decode_ws(int batch, int H, int Hkv, int d, int max_ctx_len) {
   DecodeWs w;
   w.split_tokens = decode_split_tokens(batch, Hkv, max_ctx_len);
-  w.max_splits = std::max(1, (max_ctx_len + w.split_tokens - 1) / w.split_tokens);
+  w.max_splits = static_cast<int>(std::max(
+      1LL, (static_cast<long long>(max_ctx_len) + w.split_tokens - 1) / w.split_tokens));
   const size_t rows = static_cast<size_t>(batch) * H * w.max_splits;
   w.o_bytes = round_up(rows * d * sizeof(float), 256);
   w.ml_bytes = round_up(rows * 2 * sizeof(float), 256);
@@ -254,6 +264,16 @@ int fa_device_status(unsigned int *status, int clear) {
   return FA_OK;
 }
 
+int fa_last_device_status(const void *workspace) {
+  if (workspace == nullptr || !aligned(workspace, 256)) return FA_ERR_INVALID_ARG;
+  unsigned int v = 0;
+  const void *src = static_cast<const uint8_t *>(workspace) + offsetof(CallStatus, last);
+  cudaError_t e = cudaMemcpyAsync(&v, src, sizeof(v), cudaMemcpyDeviceToHost, cudaStreamPerThread);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cudaStreamPerThread);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  return static_cast<int>(v & 0x7fffffffu);
+}
+
 int fa_selftest_wait_timeout(int *wait_result, fa_stream_t stream) {
   if (wait_result == nullptr) return FA_ERR_INVALID_ARG;
   unsigned int *st = status_ptr();
@@ -263,8 +283,11 @@ int fa_selftest_wait_timeout(int *wait_result, fa_stream_t stream) {
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-int fa_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
-           int Hkv, int N, int d, float scale, int causal, fa_stream_t stream) {
+// Dense prefill; `call` (or null) is the control block of a split-KV
+// workspace whose call runs this kernel alone.
+static int fwd_dense(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                     int H, int Hkv, int N, int d, float scale, int causal, fa_stream_t stream,
+                     CallStatus *call) {
   if (!q || !k || !v || !out) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
     return FA_ERR_INVALID_ARG;
@@ -292,8 +315,10 @@ int fa_fwd(const void *q, const void *k, const void *v, void *out, float *lse, i
   if (rc != FA_OK) return rc;
 
   PrefillParams p{};
-  p.status = status_ptr();
-  if (p.status == nullptr) return FA_ERR_CUDA;
+  p.dev_status = status_ptr();
+  if (p.dev_status == nullptr) return FA_ERR_CUDA;
+  // a split-KV call running this kernel alone raises into its workspace
+  p.status = call != nullptr ? &call->acc : p.dev_status;
   p.out = out;
   p.lse = lse;
   p.cu_seqlens = nullptr;
@@ -311,7 +336,14 @@ int fa_fwd(const void *q, const void *k, const void *v, void *out, float *lse, i
   cudaError_t e = launch_prefill(tq, tk, tv, tv, to, p, d, causal != 0,
                                  head_pairs ? kKindDenseHeads : kKindDense,
                                  static_cast<int>(grid), reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess && call != nullptr)
+    e = launch_call_status(call, p.dev_status, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
+           int Hkv, int N, int d, float scale, int causal, fa_stream_t stream) {
+  return fwd_dense(q, k, v, out, lse, B, H, Hkv, N, d, scale, causal, stream, nullptr);
 }
 
 int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float *lse,
@@ -487,8 +519,7 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *out, const f
 
 size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits) {
   if (B < 0 || H < 1 || N < 0 || num_splits < 0 || (d != 64 && d != 128)) return 0;
-  const SplitWs w = split_ws(B, H, N, d, num_splits);
-  return w.o_bytes + w.ml_bytes;
+  return split_ws_bytes(split_ws(B, H, N, d, num_splits));
 }
 
 int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *out, float *lse, int B,
@@ -505,10 +536,13 @@ int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *out, float
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (B == 0 || N == 0) return FA_OK;
   const SplitWs w = split_ws(B, H, N, d, num_splits);
-  if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.o_bytes + w.ml_bytes)
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < split_ws_bytes(w))
     return FA_ERR_WORKSPACE;
+  CallStatus *call = static_cast<CallStatus *>(workspace);
+  uint8_t *parts = static_cast<uint8_t *>(workspace) + FA_WORKSPACE_HEADER_BYTES;
   // one split: the plain kernel writes the result directly
-  if (w.splits == 1) return fa_fwd(q, k, v, out, lse, B, H, Hkv, N, d, scale, causal, stream);
+  if (w.splits == 1)
+    return fwd_dense(q, k, v, out, lse, B, H, Hkv, N, d, scale, causal, stream, call);
   const long long pairs = (N + kPrefillRowsPerCta - 1) / kPrefillRowsPerCta;
   const long long grid = pairs * B * H * w.splits;
   if (grid > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
@@ -521,7 +555,7 @@ int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *out, float
   if (rc == FA_OK) rc = make_map(&tk, k, d, Hkv, N, B, kPrefillBN);
   if (rc == FA_OK) rc = make_map(&tv, v, d, Hkv, N, B, kPrefillBN);
   if (rc == FA_OK)
-    rc = make_map(&to_part, workspace, d, H, N, static_cast<long long>(w.splits) * B,
+    rc = make_map(&to_part, parts, d, H, N, static_cast<long long>(w.splits) * B,
                   kPrefillBM, 4);
   if (rc != FA_OK) return rc;
 
@@ -541,8 +575,11 @@ int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *out, float
   p.v_descale = 1.f;
   p.causal = causal;
   p.num_splits = w.splits;
-  p.o_part = static_cast<float *>(workspace);
-  p.ml_part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + w.o_bytes);
+  p.dev_status = p.status;
+  p.status = &call->acc;
+  p.call = call;
+  p.o_part = reinterpret_cast<float *>(parts);
+  p.ml_part = reinterpret_cast<float *>(parts + w.o_bytes);
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = launch_prefill(tq, tk, tv, tv, to_part, p, d, causal != 0, kKindDenseSplit,
                                  static_cast<int>(grid), st);
@@ -623,8 +660,9 @@ size_t fa_decode_workspace_size(int batch, int H, int Hkv, int d, int max_ctx_le
                                 int block_size) {
   if (batch < 0 || H < 1 || Hkv < 1 || H % Hkv != 0 || max_ctx_len < 0) return 0;
   if ((d != 64 && d != 128) || block_size != kDecodeBlock) return 0;
+  if (max_ctx_len > kMaxCtxLen) return 0;
   const DecodeWs w = decode_ws(batch, H, Hkv, d, max_ctx_len);
-  return w.o_bytes + w.ml_bytes;
+  return FA_WORKSPACE_HEADER_BYTES + w.o_bytes + w.ml_bytes;
 }
 
 int fa_decode_paged(const void *q, const void *k_pool, const void *v_pool,
@@ -640,6 +678,7 @@ int fa_decode_paged(const void *q, const void *k_pool, const void *v_pool,
   if (batch < 0 || H < 1 || Hkv < 1 || H % Hkv != 0 || num_blocks < 1 ||
       max_blocks_per_seq < 1 || max_ctx_len < 0)
     return FA_ERR_INVALID_ARG;
+  if (max_ctx_len > kMaxCtxLen) return FA_ERR_UNSUPPORTED;
   if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (block_size != kDecodeBlock) return FA_ERR_UNSUPPORTED;
@@ -650,8 +689,11 @@ int fa_decode_paged(const void *q, const void *k_pool, const void *v_pool,
   if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (batch == 0) return FA_OK;
   const DecodeWs w = decode_ws(batch, H, Hkv, d, max_ctx_len);
-  if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.o_bytes + w.ml_bytes)
+  if (!workspace || !aligned(workspace, 256) ||
+      workspace_bytes < FA_WORKSPACE_HEADER_BYTES + w.o_bytes + w.ml_bytes)
     return FA_ERR_WORKSPACE;
+  CallStatus *call = static_cast<CallStatus *>(workspace);
+  uint8_t *parts = static_cast<uint8_t *>(workspace) + FA_WORKSPACE_HEADER_BYTES;
 
   CUtensorMap tk, tv;
   const long long tokens = static_cast<long long>(num_blocks) * block_size;
@@ -660,13 +702,15 @@ int fa_decode_paged(const void *q, const void *k_pool, const void *v_pool,
   if (rc != FA_OK) return rc;
 
   DecodeParams p{};
-  p.status = status_ptr();
-  if (p.status == nullptr) return FA_ERR_CUDA;
+  p.dev_status = status_ptr();
+  if (p.dev_status == nullptr) return FA_ERR_CUDA;
+  p.status = &call->acc;
+  p.call = call;
   p.q = q;
   p.block_table = block_table;
   p.ctx_lens = ctx_lens;
-  p.o_part = static_cast<float *>(workspace);
-  p.ml_part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + w.o_bytes);
+  p.o_part = reinterpret_cast<float *>(parts);
+  p.ml_part = reinterpret_cast<float *>(parts + w.o_bytes);
   p.out = out;
   p.lse = lse;
   p.batch = batch;
@@ -726,10 +770,11 @@ extern "C" int fa_decode_paged_noalloc(const void *q, const void *k_pool, const 
   // the partial states must fit the static array.
   if (batch < 0 || H < 1 || Hkv < 1 || H % Hkv != 0 || max_ctx_len < 0)
     return FA_ERR_INVALID_ARG;
-  if ((d != 64 && d != 128) || block_size != kDecodeBlock) return FA_ERR_UNSUPPORTED;
+  if ((d != 64 && d != 128) || block_size != kDecodeBlock || max_ctx_len > kMaxCtxLen)
+    return FA_ERR_UNSUPPORTED;
   if (batch == 0) return FA_OK;
   const DecodeWs w = decode_ws(batch, H, Hkv, d, max_ctx_len);
-  const size_t need = w.o_bytes + w.ml_bytes;
+  const size_t need = FA_WORKSPACE_HEADER_BYTES + w.o_bytes + w.ml_bytes;
   if (need > FA_DECODE_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
   unsigned char *scratch = noalloc_scratch();
   if (scratch == nullptr) return FA_ERR_CUDA;

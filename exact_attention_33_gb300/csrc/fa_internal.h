@@ -11,6 +11,15 @@ namespace fa {
 // Bound for every on-chip spin-wait (nanoseconds of %globaltimer).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
+// Control block at the start of a decode or split-KV workspace (its first
+// FA_WORKSPACE_HEADER_BYTES bytes).  Zero before the first call that uses
+// the workspace; every call leaves acc at zero again.
+struct CallStatus {
+  unsigned int acc;   // FA_DEV_* bits raised by the call in flight
+  unsigned int last;  // FA_DEV_* bits of the last call that finished
+};
+static_assert(sizeof(CallStatus) <= FA_WORKSPACE_HEADER_BYTES, "workspace header too small");
+
 // ------------------------------------------------------------------ prefill
 
 // Tile shape of the prefill kernel: each CTA owns two 128-row query tiles
@@ -62,7 +71,12 @@ constexpr int kKindPagedHeads = 6;   // paged KV cache, the same head pairs
 constexpr int kVarlenCompactMaxSeqs = 128;
 
 struct PrefillParams {
-  unsigned int *status;   // per-device sticky FA_DEV_* word
+  // FA_DEV_* bits go to `status`: the per-device sticky word, or for a call
+  // with a workspace its accumulator, which the call's last kernel publishes
+  // (into the control block and the per-device word dev_status).
+  unsigned int *status;
+  CallStatus *call;           // control block of the call's workspace, or null
+  unsigned int *dev_status;   // per-device sticky word
   void *out;              // bf16 [rows, H, d] (dense rows = B*N, varlen rows = T)
   float *lse;             // fp32, may be null
   const int32_t *cu_seqlens;  // varlen only
@@ -115,7 +129,9 @@ constexpr int kCombineWarps = 4;
 constexpr int kDecodeMaxSplitTokens = 512;  // one block-table entry per lane of the split warp
 
 struct DecodeParams {
-  unsigned int *status;     // per-device sticky FA_DEV_* word
+  unsigned int *status;       // the workspace's accumulator of FA_DEV_* bits
+  CallStatus *call;           // control block of the call's workspace
+  unsigned int *dev_status;   // per-device sticky word
   const void *q;            // bf16 [batch, H, d]
   const int32_t *block_table;
   const int32_t *ctx_lens;

@@ -943,6 +943,12 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
 template <int D>
 __global__ void __launch_bounds__(128) prefill_split_combine_kernel(const PrefillParams p) {
   pdl_wait_primary();  // the split grid's partial states are complete from here on
+  // The split grid has raised all its status bits: one thread reads them
+  // here and publishes them as the call's status when its row is done.
+  const bool publisher = blockIdx.x == 0 && threadIdx.x == 0 && p.call != nullptr;
+  const unsigned int call_bits = publisher ? call_status_bits(p.call) : 0u;
+  // this kernel's own (checked-build) index errors go to the device word only
+  unsigned int *status = p.call != nullptr ? p.dev_status : p.status;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const size_t rows = static_cast<size_t>(p.B) * p.N * p.H;
@@ -956,7 +962,7 @@ __global__ void __launch_bounds__(128) prefill_split_combine_kernel(const Prefil
   // fails a check of the checked build)
   auto ml = [&](int sp) -> float4 {
     const size_t idx = sp * stride + gw;
-    return in_bounds(idx, 1, parts, p.status) ? reinterpret_cast<const float4 *>(p.ml_part)[idx]
+    return in_bounds(idx, 1, parts, status) ? reinterpret_cast<const float4 *>(p.ml_part)[idx]
                                               : make_float4(-CUDART_INF_F, 0.f, 0.f, 0.f);
   };
   // M = max over the splits, one split per lane (at most 16 splits)
@@ -982,7 +988,7 @@ __global__ void __launch_bounds__(128) prefill_split_combine_kernel(const Prefil
     };
     auto load_o = [&](int sp, float (&v)[E]) {
       const size_t idx = (sp * stride + gw) * D + lane * E;
-      const bool in = in_bounds(idx, E, parts * D, p.status);
+      const bool in = in_bounds(idx, E, parts * D, status);
 #pragma unroll
       for (int e = 0; e < E; ++e) v[e] = in ? p.o_part[idx + e] : 0.f;
     };
@@ -1007,15 +1013,16 @@ __global__ void __launch_bounds__(128) prefill_split_combine_kernel(const Prefil
   }
   const float inv = (Ls > 0.f) ? 1.f / Ls : 0.f;
   uint16_t *dst = static_cast<uint16_t *>(p.out) + gw * D + lane * E;
-  if (in_bounds(gw * D + lane * E, E, rows * D, p.status)) {
+  if (in_bounds(gw * D + lane * E, E, rows * D, status)) {
 #pragma unroll
     for (int e = 0; e < E; e += 2)
       *reinterpret_cast<uint32_t *>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
   }
   const size_t b = bn / p.N, n = bn % p.N;
   const size_t lse_idx = (b * p.H + h) * p.N + n;
-  if (lane == 0 && p.lse != nullptr && in_bounds(lse_idx, 1, rows, p.status))
+  if (lane == 0 && p.lse != nullptr && in_bounds(lse_idx, 1, rows, status))
     p.lse[lse_idx] = (Le > 0.f) ? (M + __log2f(Le)) * 0.69314718055994530942f : -CUDART_INF_F;
+  if (publisher) publish_call_status(p.call, call_bits, p.dev_status);
 }
 
 cudaError_t launch_prefill_split_combine(const PrefillParams &p, int d, cudaStream_t stream) {
@@ -1033,6 +1040,17 @@ cudaError_t launch_prefill_split_combine(const PrefillParams &p, int d, cudaStre
   cfg.numAttrs = 1;
   if (d == 64) return cudaLaunchKernelEx(&cfg, prefill_split_combine_kernel<64>, p);
   return cudaLaunchKernelEx(&cfg, prefill_split_combine_kernel<128>, p);
+}
+
+// Publishes the status of a split-KV call that ran the plain kernel alone
+// (one split), once that kernel has completed.
+__global__ void __launch_bounds__(32) call_status_kernel(CallStatus *call, unsigned int *dev) {
+  if (threadIdx.x == 0) publish_call_status(call, call_status_bits(call), dev);
+}
+
+cudaError_t launch_call_status(CallStatus *call, unsigned int *dev, cudaStream_t stream) {
+  call_status_kernel<<<1, 32, 0, stream>>>(call, dev);
+  return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ launch

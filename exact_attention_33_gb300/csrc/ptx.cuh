@@ -12,9 +12,30 @@
 
 namespace fa {
 
-// Sets FA_DEV_* bits in the per-device sticky status word.
+// Sets FA_DEV_* bits in a status word: the per-device sticky word, or the
+// accumulator of the call's workspace (which the call publishes at its end).
 __device__ __forceinline__ void raise_status(unsigned int *status, unsigned int bits) {
   atomicOr(status, bits);
+}
+
+// The status bits that the earlier kernels of a call raised, read by one
+// thread of the call's last kernel once they have completed (after its
+// grid-dependency wait, or in stream order).
+__device__ __forceinline__ unsigned int call_status_bits(const CallStatus *call) {
+  unsigned int v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(&call->acc) : "memory");
+  return v;
+}
+
+// Publishes `bits` (read by call_status_bits above, by the same thread) as
+// the call's status `last`, clears the accumulator for the next call on the
+// workspace and adds the bits to the per-device word `dev`.  Nothing here
+// needs a round trip, so the thread issues it at the end of its own work.
+__device__ __forceinline__ void publish_call_status(CallStatus *call, unsigned int bits,
+                                                    unsigned int *dev) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(&call->acc), "r"(0u) : "memory");
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(&call->last), "r"(bits) : "memory");
+  if (bits != 0u) atomicOr(dev, bits);
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

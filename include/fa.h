@@ -36,6 +36,19 @@
  *    (an out-of-range block id, a bad context length, a pipeline wait that
  *    ran out of time) set bits of a per-device sticky status word that
  *    fa_device_status() reads; the affected work is skipped, never trapped.
+ *    Calls that take a workspace (fa_decode_paged, fa_fwd_splitkv) record
+ *    their bits in the workspace, where fa_last_device_status() reads them
+ *    without touching other streams' work, and add them to the per-device
+ *    word when they finish.
+ *  - Workspaces: the first FA_WORKSPACE_HEADER_BYTES bytes of a decode or
+ *    split-KV workspace are the call's control block (the bits its kernels
+ *    raise, and the status of the last call that finished).  Zero-fill a
+ *    new workspace once before its first call (cudaMemsetAsync,
+ *    torch.zeros); every call leaves the block ready for the next.  Calls that share a workspace must
+ *    be ordered (one stream, or events); calls on different workspaces are
+ *    independent.
+ *  - The library caches per-device addresses of its own device variables;
+ *    do not keep using it in a process after cudaDeviceReset().
  *  - Supported head sizes: d in {64, 128}.
  */
 #ifndef FA_H_
@@ -58,6 +71,10 @@ typedef enum {
   FA_ERR_CUDA = -3,        /* a CUDA runtime/driver call or a launch failed          */
   FA_ERR_WORKSPACE = -4    /* decode workspace missing, misaligned or too small      */
 } fa_status;
+
+/* Bytes at the start of a decode or split-KV workspace that hold the
+   call's control block (included in the workspace sizes below). */
+#define FA_WORKSPACE_HEADER_BYTES 256u
 
 /* Bits of the per-device sticky status word. */
 #define FA_DEV_TIMEOUT 1u     /* a bounded on-chip pipeline wait gave up             */
@@ -153,9 +170,11 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *out, const f
  *                152 work items up); values above the number of 128-key
  *                tiles are clamped.
  *   workspace  : >= fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits)
- *                bytes, 256-byte aligned, owned by the caller.
+ *                bytes, 256-byte aligned, owned by the caller, zero-filled
+ *                before its first call (the control block).
  * Two kernels run in stream order: the split prefill and the combine.  With
- * one split the call runs the fa_fwd kernel alone (no partial states).
+ * one split the call runs the fa_fwd kernel (no partial states) and a
+ * one-warp kernel that publishes the call's status in the workspace.
  */
 size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits);
 int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *out, float *lse, int B,
@@ -190,10 +209,12 @@ int fa_fwd_paged(const void *q, const void *k_pool, const void *v_pool,
                  float scale, int causal, void *out, float *lse, fa_stream_t stream);
 
 /*
- * Bytes of caller-owned workspace that fa_decode_paged needs for the split
- * partial states (m, l, o) of every (sequence, query head, key split).
- * Returns 0 for invalid arguments.  The split size depends only on these
- * arguments and on the current device's SM count.
+ * Bytes of caller-owned workspace that fa_decode_paged needs: the control
+ * block plus the split partial states (m, l, o) of every (sequence, query
+ * head, key split).  Returns 0 for invalid arguments.  The split size
+ * depends only on these arguments and on the current device's SM count; Hkv
+ * is among them because the number of splits is chosen so that the
+ * (sequence, KV head, split) work items fill the GPU.
  */
 size_t fa_decode_workspace_size(int batch, int H, int Hkv, int d, int max_ctx_len,
                                 int block_size);
@@ -213,7 +234,9 @@ size_t fa_decode_workspace_size(int batch, int H, int Hkv, int d, int max_ctx_le
  *   ctx_lens    : int32 [batch], 0 <= ctx_lens[b] <= max_ctx_len
  *   lse         : [batch, H] fp32, may be NULL
  *   workspace   : >= fa_decode_workspace_size(...) bytes, 256-byte aligned,
- *                 owned by the caller; its contents on entry are ignored.
+ *                 owned by the caller; zero-filled before its first call
+ *                 (the control block, see the conventions above); past the
+ *                 control block its contents on entry are ignored.
  * A sequence with ctx_len 0 gets out = 0 and lse = -inf.  Slots of the last
  * block past ctx_len are never read into the result.  Supported: block_size
  * == 16, H / Hkv <= 16.  Two kernels run in stream order: the split kernel
@@ -244,10 +267,14 @@ int fa_decode_paged(const void *q, const void *k_pool, const void *v_pool,
  *    device (with it current); make that first call before any stream
  *    capture.
  *  - Every call on a device shares the one array and it keeps the last call's
- *    contents; nothing in it needs to start at zero, because each call writes
- *    every partial state before its combine reads it.  Calls whose kernels
- *    overlap on the GPU (other streams, other host threads) race on the array
- *    and must be ordered by the caller.
+ *    contents.  Only its first FA_WORKSPACE_HEADER_BYTES bytes (the control
+ *    block of fa_decode_paged) must start at zero: the array is zero when the
+ *    library is loaded, and every call leaves that block at zero again.  The
+ *    partial states need no clearing, because each call writes every one of
+ *    them before its combine reads it.  Calls whose kernels overlap on the
+ *    GPU (other streams, other host threads) race on the array and must be
+ *    ordered by the caller.  Device-side errors of these calls are read with
+ *    fa_device_status().
  */
 #define FA_DECODE_NOALLOC_SCRATCH_BYTES (32u << 20)
 int fa_decode_paged_noalloc(const void *q, const void *k_pool, const void *v_pool,
@@ -260,9 +287,27 @@ int fa_decode_paged_noalloc(const void *q, const void *k_pool, const void *v_poo
 const char *fa_status_string(int status);
 
 /*
+ * Device-side status of the last call that finished on `workspace` (a
+ * fa_decode_paged or fa_fwd_splitkv workspace): its FA_DEV_* bits (>= 0; 0 =
+ * no device-side error), or a negative fa_status if the read failed.  The
+ * pages state the problem with the caller owning every buffer; this is the
+ * status word of the call's own workspace, so concurrent callers on other
+ * workspaces and streams neither see nor clear each other's errors.
+ * Read it after the call has completed (the caller synchronises its own
+ * stream or event first); the read is a 4-byte device-to-host copy on the
+ * calling thread's per-thread default stream and does not wait for other
+ * streams.  Before any call has finished on a zero-filled workspace it
+ * returns 0.  A call that launches nothing (an empty problem) leaves the
+ * word unchanged.  The index checks of the checked build's combine kernels
+ * report to the per-device word only.
+ */
+int fa_last_device_status(const void *workspace);
+
+/*
  * Read the sticky device status word of the current device into *status
  * (FA_DEV_* bits; 0 = no device-side error since the last clear) and clear
- * it when `clear` != 0.  This call synchronises the device.
+ * it when `clear` != 0.  It gathers the bits of every call on the device,
+ * with or without a workspace.  This call synchronises the device.
  */
 int fa_device_status(unsigned int *status, int clear);
 

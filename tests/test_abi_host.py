@@ -23,15 +23,31 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = re.findall(r"\b(fa_[a-z_]+)\s*\(", text)
+    names = re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)
     return sorted(set(names))
 
 
+# The exported calls, exactly: the three calls of the statement of the
+# problem (dense, packed varlen and paged decode with its workspace size and
+# per-call status), the further prefill layouts and the backward pass, the
+# allocation-free decode, and the status, self-test and version helpers.
+BOUNDARY = sorted([
+    "fa_fwd", "fa_fwd_varlen", "fa_decode_workspace_size", "fa_decode_paged",
+    "fa_last_device_status", "fa_status_string",
+    "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_fwd_paged", "fa_fwd_fp8",
+    "fa_bwd", "fa_bwd_workspace_size", "fa_decode_paged_noalloc",
+    "fa_device_status", "fa_selftest_wait_timeout", "fa_version",
+])
+
+
 def test_header_declares_the_boundary():
-    names = declared_functions()
-    for n in ["fa_fwd", "fa_fwd_varlen", "fa_decode_paged", "fa_decode_workspace_size",
-              "fa_status_string", "fa_device_status", "fa_version"]:
-        assert n in names
+    assert declared_functions() == BOUNDARY
+
+
+def test_binding_exposes_the_boundary():
+    import exact_attention_33_gb300 as fa
+    for name in BOUNDARY:
+        assert callable(getattr(fa, name)), name
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -99,7 +115,12 @@ def test_decode_host_validation(lib):
 def test_workspace_size(lib):
     import exact_attention_33_gb300 as fa
     n = fa.fa_decode_workspace_size(64, 32, 8, 128, 32768, 16)
-    assert n >= 64 * 32 * 128 * 4 and n % 256 == 0
+    assert n >= fa.FA_WORKSPACE_HEADER_BYTES + 64 * 32 * 128 * 4 and n % 256 == 0
+    # the control block comes first in every decode and split-KV workspace
+    assert fa.fa_decode_workspace_size(1, 4, 4, 64, 16, 16) > fa.FA_WORKSPACE_HEADER_BYTES
+    assert fa.fa_fwd_splitkv_workspace_size(1, 4, 1024, 64, 2) > fa.FA_WORKSPACE_HEADER_BYTES
+    # context lengths whose split arithmetic would leave int are refused
+    assert fa.fa_decode_workspace_size(1, 32, 8, 128, 2**31 - 1, 16) == 0
     assert fa.fa_decode_workspace_size(1, 32, 8, 128, 1024, 32) == 0
     assert fa.fa_decode_workspace_size(1, 30, 8, 128, 1024, 16) == 0
 
@@ -146,6 +167,18 @@ def test_fp8_host_validation(lib):
     assert call(d=64) == -2
     assert call(H=3, Hkv=2) == -1
     assert call(N=0) == 0
+
+
+def test_last_device_status_host_validation(lib):
+    import exact_attention_33_gb300  # noqa: F401  (sets argtypes)
+    assert lib.fa_last_device_status(NULL) == -1
+    assert lib.fa_last_device_status(ctypes.c_void_p(0x10010)) == -1   # not 256-byte aligned
+
+
+def test_workspace_header_matches_the_binding():
+    import exact_attention_33_gb300 as fa
+    m = re.search(r"#define\s+FA_WORKSPACE_HEADER_BYTES\s+(\d+)u", open(HEADER).read())
+    assert m and int(m.group(1)) == fa.FA_WORKSPACE_HEADER_BYTES
 
 
 def test_status_bits_match_the_binding():

@@ -49,8 +49,7 @@ def test_decode_graph_replay(fa):
     table, cl = dev_i32(inp.block_table), dev_i32(inp.ctx_lens)
     out = torch.empty_like(q)
     lse = torch.empty((len(ctx), 8), dtype=torch.float32, device="cuda")
-    ws = torch.empty(fa.fa_decode_workspace_size(len(ctx), 8, 2, 128, inp.max_ctx_len),
-                     dtype=torch.uint8, device="cuda")
+    ws = fa.new_workspace(fa.fa_decode_workspace_size(len(ctx), 8, 2, 128, inp.max_ctx_len))
     g = capture(torch, lambda: fa.fa_decode_paged(q, kp, vp, table, cl, inp.max_ctx_len,
                                                   out=out, lse=lse, workspace=ws))
     for seed in (61, 62):   # two replays on new queries
@@ -74,8 +73,7 @@ def test_prefill_graph_replay(fa, split):
     out = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
     if split:
-        ws = torch.empty(fa.fa_fwd_splitkv_workspace_size(B, H, N, d, 3), dtype=torch.uint8,
-                         device="cuda")
+        ws = fa.new_workspace(fa.fa_fwd_splitkv_workspace_size(B, H, N, d, 3))
         fn = lambda: fa.fa_fwd_splitkv(q, k, v, causal=True, num_splits=3, out=out, lse=lse,
                                        workspace=ws)
     else:
