@@ -132,12 +132,16 @@ int sm_count() {
 
 // Keys per split of the decode kernel.  Large splits keep the partial-state
 // traffic small; the split shrinks (down to 64 keys) while the number of
-// (sequence, KV head, split) work items would not fill about two waves of
-// split CTAs (seven resident per SM).
+// (sequence, KV head, split) work items would not fill kDecodeWaveCtas split
+// CTAs per SM (about two waves of seven resident CTAs).
+#ifndef FA_DECODE_WAVE_CTAS
+#define FA_DECODE_WAVE_CTAS 14
+#endif
+constexpr int kDecodeWaveCtas = FA_DECODE_WAVE_CTAS;
 int decode_split_tokens(int batch, int Hkv, int max_ctx_len) {
   int sms = sm_count();
   if (sms <= 0) sms = 148;
-  const long long want = 2LL * 7 * sms;
+  const long long want = static_cast<long long>(kDecodeWaveCtas) * sms;
   int split = kDecodeMaxSplitTokens;
   while (split > 64) {
     const long long items = static_cast<long long>(batch) * Hkv *

@@ -29,10 +29,10 @@ constexpr int kPrefillBM = 128;
 constexpr int kPrefillBN = 128;
 constexpr int kPrefillQTiles = 2;
 constexpr int kPrefillRowsPerCta = kPrefillBM * kPrefillQTiles;
-constexpr int kPrefillThreads = 320;  // 8 softmax warps + 1 MMA warp + 1 TMA warp
+constexpr int kPrefillThreads = 352;  // 8 softmax warps, 1 MMA warp, 2 TMA warps
 
 // The same kernel with one query tile per CTA (packed batches of short
-// sequences): 256 threads, warps 0-3 softmax, 4 MMA, 5 TMA, 6-7 idle, and two
+// sequences): 256 threads, warps 0-3 softmax, 4 MMA, 5 and 6 TMA, 7 idle, and two
 // CTAs per SM, so that one CTA's launch, set-up and epilogue overlap the
 // other's key loop.  Each CTA is built for 128 registers per thread and moves
 // them with setmaxnreg: the softmax warpgroup up to 168, the other down to 88
@@ -52,7 +52,8 @@ struct PrefillShape {
   static constexpr int kThreads = QT == 2 ? kPrefillThreads : 256;
   static constexpr int kSoftmaxWarps = 4 * QT;
   static constexpr int kMmaWarp = kSoftmaxWarps;
-  static constexpr int kTmaWarp = kSoftmaxWarps + 1;
+  static constexpr int kTmaWarp = kSoftmaxWarps + 1;   // Q and K/V copies (K only when paged)
+  static constexpr int kTmaVWarp = kSoftmaxWarps + 2;  // V copies of a paged KV cache
   static constexpr int kMinBlocks = QT == 2 ? 1 : 2;
 };
 

@@ -10,8 +10,11 @@
 // accumulator of the first page (one division at the end).
 //
 // GB300 mapping (one CTA = two 128-row query tiles of one (sequence, head)):
-//   warp 9      TMA producer: Q tiles once, then K/V tiles of 128 keys into a
-//               ring of shared-memory stages (128-byte swizzle).
+//   warp 9      TMA producer: Q tiles once, then K/V tiles of 128 keys into
+//               rings of shared-memory stages (128-byte swizzle).  With a
+//               paged KV cache, whose copies go block by block through the
+//               block table, warp 9 copies the K tiles and warp 10 the V
+//               tiles.
 //   warp 8      MMA issuer (one thread): S_i = Q_i K^T and O_i += P_i V on the
 //               5th-generation tensor cores, fp32 accumulators in TMEM.
 //   warps 0-7   two softmax warpgroups, one per query tile; thread t owns
@@ -44,6 +47,8 @@ namespace fa {
 // grows by more than this many powers of two.
 constexpr float kRescaleLog2 = 8.f;
 
+
+
 template <int D, bool FP8 = false, int QT = 2>
 struct PrefillLayout {
   static constexpr int kElemBytes = FP8 ? 1 : 2;
@@ -63,18 +68,28 @@ struct PrefillLayout {
       (QT == 1) ? ((kTileBytes == 32768) ? 1 : 2) : ((kTileBytes == 32768) ? FA_PREFILL_STAGES_K128 : 5);
   static constexpr int kStagesV =
       (QT == 1) ? ((kTileBytes == 32768) ? 1 : 2) : ((kTileBytes == 32768) ? FA_PREFILL_STAGES_V128 : 5);
+  // Row sums on the tensor cores (d = 64): the P V product also multiplies
+  // P by a block of ones (16 columns of 1.0 beside each V tile, through the
+  // descriptor's leading-byte offset), so column D of O accumulates the sum
+  // of the bf16 weights of each row, rescaled with O.  O then takes D + 16
+  // TMEM columns (2 x (128 + 80) <= 512); at d = 128 there is no room.
+  static constexpr bool kOnes = (D == 64) && !FP8;
+  static constexpr int kOCols = kOnes ? D + 16 : D;  // TMEM columns of O
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + QT * kTileBytes;
   static constexpr int kV = kK + kStagesK * kTileBytes;
-  static constexpr int kBar = kV + kStagesV * kTileBytes;
+  static constexpr int kOnesOff = kV + kStagesV * kTileBytes;  // 128 x 64 bf16 ones (one chunk)
+  static constexpr int kBar = kOnesOff + (kOnes ? kChunkBytes : 0);
   // q_full, k_full[SK], k_empty[SK], v_full[SV], s_full[2], p_full[2],
-  // o_done[2], drain.  A V stage has no release barrier of its own: the
-  // K-stage release that follows the P V products of a key tile frees it.
-  static constexpr int kNumBars = 1 + 2 * kStagesK + kStagesV + 7;
+  // o_done[2], drain, v_empty[SV].  A V stage is released as soon as the
+  // P V products of its key tile are done.
+  static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 7;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kSmemAlloc = kBytes + 1024;     // base is aligned up to 1024 in-kernel
   static constexpr uint32_t kTmemCols = QT * 256;
+  // TMEM columns: S_i at 128 i (P_i over its first columns), O_i at
+  // kTmemO + kOCols i.
   static constexpr int kTmemO = QT * 128;
 };
 
@@ -272,6 +287,8 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
   uint64_t *p_full = s_full + 2;
   uint64_t *o_done = p_full + 2;
   uint64_t *drain = o_done + 2;
+  uint64_t *v_empty = drain + 1;  // V-stage releases
+  constexpr bool ONES = L::kOnes;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
 
@@ -302,6 +319,7 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
       mbar_init(&o_done[i], 1);
     }
     mbar_init(drain, 1);
+    for (int s = 0; s < SV; ++s) mbar_init(&v_empty[s], 1);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -336,8 +354,15 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
     uint4 *z = reinterpret_cast<uint4 *>(smem + L::kV);
     for (int t = threadIdx.x; t < SV * L::kTileBytes / 16; t += Sh::kThreads)
       z[t] = make_uint4(0u, 0u, 0u, 0u);
-    fence_proxy_async_smem();
   }
+  if (ONES) {
+    // the block of ones read beside every V tile (bf16 1.0 = 0x3F80); the
+    // 128-byte swizzle permutes equal values, so no pattern is needed
+    uint4 *o1 = reinterpret_cast<uint4 *>(smem + L::kOnesOff);
+    for (int t = threadIdx.x; t < L::kChunkBytes / 16; t += Sh::kThreads)
+      o1[t] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+  }
+  if (PAGED || ONES) fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -347,7 +372,8 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
   // One query tile per CTA: this warpgroup (MMA, TMA, two idle warps) hands
   // registers to the softmax warpgroup.
   if constexpr (QT == 1) setmaxnreg_dec<kPrefill1CtlRegs>();
-  if (warp == Sh::kTmaWarp && PAGED) {
+  const bool k_producer = warp == Sh::kTmaWarp;  // else the V producer
+  if ((warp == Sh::kTmaWarp || warp == Sh::kTmaVWarp) && PAGED) {
     // ------------------------------------------------------ TMA producer, paged
     // The warp runs converged: lanes 0..7 look up the 8 physical blocks of a
     // 128-key tile in the block table, lane 0 issues the copies.  A block
@@ -418,8 +444,7 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
     };
     auto load_v = [&](int j) -> bool {
       const int sv = j % SV;
-      if (j >= SV && !mbar_wait_warp(&k_empty[(j - SV + 1) % SK], ((j - SV + 1) / SK) & 1,
-                                     abort_flag, p.status))
+      if (j >= SV && !mbar_wait_warp(&v_empty[sv], ((j / SV) - 1) & 1, abort_flag, p.status))
         return false;
       int rows;
       const int phys = lookup(j, rows);
@@ -450,18 +475,17 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
       v_issued = j + 1;
       return true;
     };
-    if (n_kv > 0 && load_k(0)) {
-      for (int j = 0; j < n_kv; ++j) {
-        if (!load_v(j)) break;
-        if (j + 1 < n_kv && !load_k(j + 1)) break;
-      }
-    }
+    for (int j = 0; j < n_kv; ++j)
+      if (!(k_producer ? load_k(j) : load_v(j))) break;
     if (lane == 0) {
-      mbar_drain(q_full, 0, p.status);
-      for (int j = max(0, k_issued - SK); j < k_issued; ++j)
-        mbar_drain(&k_full[j % SK], (j / SK) & 1, p.status);
-      for (int j = max(0, v_issued - SV); j < v_issued; ++j)
-        mbar_drain(&v_full[j % SV], (j / SV) & 1, p.status);
+      if (k_producer) {
+        mbar_drain(q_full, 0, p.status);
+        for (int j = max(0, k_issued - SK); j < k_issued; ++j)
+          mbar_drain(&k_full[j % SK], (j / SK) & 1, p.status);
+      } else {
+        for (int j = max(0, v_issued - SV); j < v_issued; ++j)
+          mbar_drain(&v_full[j % SV], (j / SV) & 1, p.status);
+      }
     }
   } else if (warp == Sh::kTmaWarp) {
     // ------------------------------------------------------ TMA producer
@@ -483,8 +507,7 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
       };
       auto load_v = [&](int j) -> bool {
         const int sv = j % SV;
-        if (j >= SV && !mbar_wait(&k_empty[(j - SV + 1) % SK], ((j - SV + 1) / SK) & 1,
-                                  abort_flag, p.status))
+        if (j >= SV && !mbar_wait(&v_empty[sv], ((j / SV) - 1) & 1, abort_flag, p.status))
           return false;
         mbar_arrive_expect_tx(&v_full[sv], L::kTileBytes);
 #pragma unroll
@@ -518,7 +541,7 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
       constexpr uint32_t kIdescS = FP8 ? idesc_e4m3_f32(kPrefillBM, kPrefillBN, false, false)
                                        : idesc_bf16_f32(kPrefillBM, kPrefillBN, false, false);
       constexpr uint32_t kIdescO = FP8 ? idesc_e4m3_f32(kPrefillBM, D, false, true)
-                                       : idesc_bf16_f32(kPrefillBM, D, false, true);
+                                       : idesc_bf16_f32(kPrefillBM, L::kOCols, false, true);
       const uint32_t q_base = smem_u32(sQ);
       const uint32_t k_base = smem_u32(sK);
       const uint32_t v_base = smem_u32(sV);
@@ -544,10 +567,13 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
         __syncwarp();
       };
       auto issue_o = [&](int i, int st, int j) {
-        const uint32_t d_t = tmem + L::kTmemO + i * D;
+        const uint32_t d_t = tmem + L::kTmemO + i * L::kOCols;
         const uint32_t p_t = tmem + i * 128;
         if (elect_one()) {
-          const uint64_t b0 = sdesc_sw128(v_base + st * L::kTileBytes, L::kChunkBytes, 1024);
+          // N beyond D (the ones block) is read at the leading-byte offset
+          const uint32_t lbo = ONES ? static_cast<uint32_t>(L::kOnesOff - (L::kV + st * L::kTileBytes))
+                                    : static_cast<uint32_t>(L::kChunkBytes);
+          const uint64_t b0 = sdesc_sw128(v_base + st * L::kTileBytes, lbo, 1024);
 #pragma unroll
           for (int kk = 0; kk < kPrefillBN / kKStep; ++kk) {
             // kKStep keys of 128-byte rows; P holds kKStep keys in 8 TMEM columns
@@ -589,7 +615,7 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
           k_next = true;
           return true;
         };
-        // With dense K/V, V(j) and K(j+1) are resident long before P_0(j)
+        // With dense K/V, V(j) and K(j+1) are usually resident before P_0(j)
         // is ready: waiting for them first keeps both waits off the path
         // from P_i(j) to S_i(j+1).  (Their loads never depend on this
         // iteration's releases, so the order cannot deadlock.)  Gathered
@@ -612,15 +638,13 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
           tc_fence_after();
           issue_o(1, sv, j);
         }
+        // the V stage of key tile j is free once its P V products are done
+        mma_commit_elect(&v_empty[sv]);
         if (j + 1 < kv_end[1]) {
           if (!wait_k_next()) break;
           issue_s(1, sk1);
         }
-        // One stage release per key tile, after the products (a commit costs
-        // as much as several MMA issues): it frees the stage of K(j+1) once
-        // S_0(j+1) and S_1(j+1) are done, and, since it also covers the
-        // P V products of this key tile, the stage of V(j).  The producer
-        // waits for V(t)'s stage on the release of key tile t - SV.
+        // the stage of K(j+1) is free once S_0(j+1) and S_1(j+1) are done
         if (j + 1 < n_kv) mma_commit_elect(&k_empty[sk1]);
       }
       // Everything this thread issued must finish before TMEM is released.
@@ -636,7 +660,7 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
     const int row = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem + i * 128 + lane_off;
-    const uint32_t tO = tmem + L::kTmemO + i * D + lane_off;
+    const uint32_t tO = tmem + L::kTmemO + i * L::kOCols + lane_off;
     const int qi = tile_row(i) + row;  // query row within the sequence
     const int hi = tile_head(i);       // query head of this tile
     const int my_end = kv_end[i];
@@ -694,7 +718,8 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
       const float m_use = (m_ref == -CUDART_INF_F) ? 0.f : m_ref;
       const float2 negm = make_float2(-m_use, -m_use);
       // Two row sums: l sums the bf16 values that the P V product multiplies,
-      // so o / l is a weighted mean with consistent weights; l_exact sums the
+      // so o / l is a weighted mean with consistent weights (with the ones
+      // block, the tensor cores form it in column D of O); l_exact sums the
       // fp32 exponentials and gives the log-sum-exp.
       float2 rs0 = make_float2(0.f, 0.f), rs1 = make_float2(0.f, 0.f);
       float2 re0 = make_float2(0.f, 0.f), re1 = make_float2(0.f, 0.f);
@@ -716,8 +741,10 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
             pk[c + 1] = pack_bf16x2(p1.x, p1.y);
             re0 = fadd2(re0, p0);
             re1 = fadd2(re1, p1);
-            add_bf16x2_to(rs0, pk[c]);
-            add_bf16x2_to(rs1, pk[c + 1]);
+            if (!ONES) {
+              add_bf16x2_to(rs0, pk[c]);
+              add_bf16x2_to(rs1, pk[c + 1]);
+            }
           }
           tmem_st32(tS + half * 32, pk);
         }
@@ -747,7 +774,7 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
       }
       const float2 rs = fadd2(rs0, rs1);
       const float2 re = fadd2(re0, re1);
-      l = l * alpha + (rs.x + rs.y);
+      if (!ONES) l = l * alpha + (rs.x + rs.y);
       l_exact = l_exact * alpha + (re.x + re.y);
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
         const float2 a2 = make_float2(alpha, alpha);
@@ -762,6 +789,17 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
             o[t + 1] = __float_as_uint(v.y);
           }
           tmem_st32(tO + c * 32, o);
+        }
+        if (ONES) {  // the row-sum columns follow O
+          uint32_t o[16];
+          tmem_ld16_wait(tO + D, o);
+#pragma unroll
+          for (int t = 0; t < 16; t += 2) {
+            const float2 v = fmul2(make_float2(__uint_as_float(o[t]), __uint_as_float(o[t + 1])), a2);
+            o[t] = __float_as_uint(v.x);
+            o[t + 1] = __float_as_uint(v.y);
+          }
+          tmem_st16(tO + D, o);
         }
       }
       tmem_wait_st();
@@ -780,6 +818,12 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
       if (have) {
         have = mbar_wait(&o_done[i], 0, abort_flag, p.status);
         have = __all_sync(0xffffffffu, have);
+      }
+      if (ONES && have) {  // the sum of the bf16 weights, from column D of O
+        tc_fence_after();
+        uint32_t lr[16];
+        tmem_ld16_wait(tO + D, lr);
+        l = __uint_as_float(lr[0]);
       }
       if (tile_live && my_end > 0) {
         // The fp32 tile goes out through the warpgroup's free Q tile (it
@@ -835,6 +879,11 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
       }
       {
         if (ok) tc_fence_after();
+        if (ONES && ok) {  // the sum of the bf16 weights, from column D of O
+          uint32_t lr[16];
+          tmem_ld16_wait(tO + D, lr);
+          l = __uint_as_float(lr[0]);
+        }
         const bool live = qi < len;
         const float inv_l = (l > 0.f) ? p.v_descale / l : 0.f;
         // A whole bf16 tile goes out through shared memory and one TMA store
