@@ -66,64 +66,44 @@ __device__ __forceinline__ uint32_t keep_tokens(uint32_t x, int tok_lo, int n_va
   return x & (lo | hi);
 }
 
+// One warp's pass over a range of keys: the unnormalised O^T accumulator of
+// the group's query heads (m16n8 accumulator layout: rows are the head
+// dimension, columns the heads), the running maximum of each head (log2
+// units) and each lane's share of the row sums.
 template <int D, int NT>
-__global__ void __launch_bounds__(32)
-    decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
+struct WarpRange {
+  float acc[NT][D / 16][4];
+  float mcol[NT][2], lcol[NT][2];
+};
+
+constexpr int kRangeOk = 0, kRangeBadBlock = 1, kRangeFailed = 2;
+
+// A converged warp streams keys [t0, t1) (at most kDecodeMaxSplitTokens) of
+// sequence b and KV head kvh through its own ring of TMA stages at `smem`
+// (DecodeLayout<D>::kBytes, 1024-byte aligned) and leaves its state in st.
+// Lane i holds the physical id of logical block t0 / 16 + i in my_blk (-1
+// when it could not be read).  Returns kRangeBadBlock (nothing loaded,
+// status raised) when a block id of the range is outside the pool,
+// kRangeFailed when a wait gave up (copies in flight are drained before it
+// returns).
+template <int D, int NT>
+__device__ __forceinline__ int decode_range(const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                                            const DecodeParams &p, int b, int kvh, int t0, int t1,
+                                            int my_blk, uint8_t *smem, WarpRange<D, NT> &st) {
   using L = DecodeLayout<D>;
   constexpr int S = kDecodeStages;
   constexpr int KC = D / 16;  // 16-wide k chunks of the head dimension
-  const int split = blockIdx.x;
-  const int kvh = blockIdx.y;
-  const int b = blockIdx.z;
-  const int lane = threadIdx.x;
-  pdl_launch_dependents();
-
-  const int ctx = checked_load(p.ctx_lens, b, p.batch, p.status);
-  if (ctx < 0 || ctx > p.max_ctx_len || ctx > p.max_blocks_per_seq * kDecodeBlock) {
-    if (split == 0 && kvh == 0 && lane == 0) raise_status(p.status, FA_DEV_BAD_CTX);
-    return;
-  }
-  const int t0 = split * p.split_tokens;
-  if (t0 >= ctx) return;
-  const int t1 = min(ctx, t0 + p.split_tokens);
+  const int lane = threadIdx.x & 31;
   const int nblk = (t1 - t0 + kDecodeBlock - 1) / kDecodeBlock;  // <= 32
-  const int lb0 = t0 / kDecodeBlock;
   const int G = p.group;
 
-  // Physical block ids of this split, one per lane.
-  int my_blk = 0;
-  bool bad = false;
-  if (lane < nblk) {
-    const size_t tidx = static_cast<size_t>(b) * p.max_blocks_per_seq + lb0 + lane;
-    if (in_bounds(tidx, 1, static_cast<size_t>(p.batch) * p.max_blocks_per_seq, p.status)) {
-      my_blk = p.block_table[tidx];
-      bad = (my_blk < 0 || my_blk >= p.num_blocks);
-    } else {
-      bad = true;
-    }
-  }
-  // partial-state rows of the call: [batch, H, max_splits]
-  const size_t part_rows = static_cast<size_t>(p.batch) * p.H * p.max_splits;
+  const bool bad = lane < nblk && (my_blk < 0 || my_blk >= p.num_blocks);
   const size_t part_row = static_cast<size_t>(b) * p.H + static_cast<size_t>(kvh) * G;
   if (__any_sync(0xffffffffu, bad)) {
     if (lane == 0) raise_status(p.status, FA_DEV_BAD_BLOCK);
-    // Leave a neutral partial state so that the combine ignores this split.
-    for (int g = 0; g < G; ++g) {
-      const size_t row = (part_row + g) * p.max_splits + split;
-      if (!in_bounds(row, 1, part_rows, p.status)) continue;
-      for (int c = lane; c < D; c += 32) p.o_part[row * D + c] = 0.f;
-      if (lane == 0) {
-        p.ml_part[row * 2 + 0] = -CUDART_INF_F;
-        p.ml_part[row * 2 + 1] = 0.f;
-      }
-    }
-    return;
+    return kRangeBadBlock;
   }
 
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBar);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc);
 
@@ -171,8 +151,9 @@ __global__ void __launch_bounds__(32)
     }
   }
 
-  float acc[NT][KC][4];
-  float mcol[NT][2], lcol[NT][2];
+  float (&acc)[NT][KC][4] = st.acc;
+  float (&mcol)[NT][2] = st.mcol;
+  float (&lcol)[NT][2] = st.lcol;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -278,34 +259,7 @@ __global__ void __launch_bounds__(32)
     }
   }
 
-  if (ok) {
-    // write the partial state of every query head of the group
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        float lt = lcol[nt][cc];
-        lt += __shfl_xor_sync(0xffffffffu, lt, 4);
-        lt += __shfl_xor_sync(0xffffffffu, lt, 8);
-        lt += __shfl_xor_sync(0xffffffffu, lt, 16);
-        const int g = nt * 8 + 2 * quad + cc;
-        if (g < G) {
-          const size_t row = (part_row + g) * p.max_splits + split;
-          if (!in_bounds(row, 1, part_rows, p.status)) continue;
-          if (grp == 0) {
-            p.ml_part[row * 2 + 0] = mcol[nt][cc];
-            p.ml_part[row * 2 + 1] = lt;
-          }
-          float *orow = p.o_part + row * D;
-#pragma unroll
-          for (int mt = 0; mt < KC; ++mt) {
-            orow[mt * 16 + grp] = acc[nt][mt][cc];
-            orow[mt * 16 + 8 + grp] = acc[nt][mt][2 + cc];
-          }
-        }
-      }
-    }
-  } else {
+  if (ok) return kRangeOk;
     // drain copies still in flight before the CTA releases its shared memory
     if (lane == 0) {
       for (int i = 0; i < min(nblk, S); ++i) {
@@ -319,6 +273,89 @@ __global__ void __launch_bounds__(32)
       }
     }
     __syncwarp();
+  return kRangeFailed;
+}
+
+template <int D, int NT>
+__global__ void __launch_bounds__(32)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
+  constexpr int KC = D / 16;
+  const int split = blockIdx.x;
+  const int kvh = blockIdx.y;
+  const int b = blockIdx.z;
+  const int lane = threadIdx.x;
+  pdl_launch_dependents();
+
+  // The block ids of the whole split are read together with the context
+  // length (one memory round trip instead of two); ids past the context are
+  // not used.
+  const int lb0 = split * (p.split_tokens / kDecodeBlock);
+  int my_blk = -1;
+  if (lane < p.split_tokens / kDecodeBlock && lb0 + lane < p.max_blocks_per_seq) {
+    const size_t tidx = static_cast<size_t>(b) * p.max_blocks_per_seq + lb0 + lane;
+    if (in_bounds(tidx, 1, static_cast<size_t>(p.batch) * p.max_blocks_per_seq, p.status))
+      my_blk = p.block_table[tidx];
+  }
+  const int ctx = checked_load(p.ctx_lens, b, p.batch, p.status);
+  if (ctx < 0 || ctx > p.max_ctx_len || ctx > p.max_blocks_per_seq * kDecodeBlock) {
+    if (split == 0 && kvh == 0 && lane == 0) raise_status(p.status, FA_DEV_BAD_CTX);
+    return;
+  }
+  const int t0 = split * p.split_tokens;
+  if (t0 >= ctx) return;
+  const int t1 = min(ctx, t0 + p.split_tokens);
+  const int G = p.group;
+  // partial-state rows of the call: [batch, H, max_splits]
+  const size_t part_rows = static_cast<size_t>(p.batch) * p.H * p.max_splits;
+  const size_t part_row = static_cast<size_t>(b) * p.H + static_cast<size_t>(kvh) * G;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  WarpRange<D, NT> st;
+  const int rc = decode_range<D, NT>(tm_k, tm_v, p, b, kvh, t0, t1, my_blk, smem, st);
+  if (rc == kRangeBadBlock) {
+    // Leave a neutral partial state so that the combine ignores this split.
+    for (int g = 0; g < G; ++g) {
+      const size_t row = (part_row + g) * p.max_splits + split;
+      if (!in_bounds(row, 1, part_rows, p.status)) continue;
+      for (int c = lane; c < D; c += 32) p.o_part[row * D + c] = 0.f;
+      if (lane == 0) {
+        p.ml_part[row * 2 + 0] = -CUDART_INF_F;
+        p.ml_part[row * 2 + 1] = 0.f;
+      }
+    }
+    return;
+  }
+  if (rc != kRangeOk) return;
+  // write the partial state of every query head of the group
+  const int quad = lane & 3;
+  const int grp = lane >> 2;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      float lt = st.lcol[nt][cc];
+      lt += __shfl_xor_sync(0xffffffffu, lt, 4);
+      lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+      lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+      const int g = nt * 8 + 2 * quad + cc;
+      if (g < G) {
+        const size_t row = (part_row + g) * p.max_splits + split;
+        if (!in_bounds(row, 1, part_rows, p.status)) continue;
+        if (grp == 0) {
+          p.ml_part[row * 2 + 0] = st.mcol[nt][cc];
+          p.ml_part[row * 2 + 1] = lt;
+        }
+        float *orow = p.o_part + row * D;
+#pragma unroll
+        for (int mt = 0; mt < KC; ++mt) {
+          orow[mt * 16 + grp] = st.acc[nt][mt][cc];
+          orow[mt * 16 + 8 + grp] = st.acc[nt][mt][2 + cc];
+        }
+      }
+    }
   }
 }
 
