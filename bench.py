@@ -439,6 +439,44 @@ def measure_fp8_prefill(torch, device, fa, steps, warmup, peak_bf16):
             "launches_per_call": 1}
 
 
+def measure_fp8_varlen(torch, device, fa, steps, warmup, peak_bf16):
+    """FP8 (e4m3) packed varlen causal prefill on the varlen workload (32
+    sequences of U[64, 4096] tokens, GQA 16 / 4, d = 128), quantised per
+    tensor, timed with CUDA events on its own after the main step."""
+    cfg = W.WORKLOADS["varlen_gqa_d128"]
+    lengths = W.varlen_lengths(cfg["num_seqs"], cfg["len_lo"], cfg["len_hi"])
+    T = int(np.sum(lengths))
+    inp = W.fp8_inputs(1, T, cfg["H"], cfg["Hkv"], cfg["d"], seed=0)
+    q, k, v = (torch.from_numpy(getattr(inp, n)[0]).to(device) for n in ("q", "k", "v"))
+    cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)).to(device)
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=device)
+    lse = torch.empty((cfg["H"], T), dtype=torch.float32, device=device)
+    flops = W.varlen_flops(lengths, cfg["H"], cfg["d"], True)
+
+    def run():
+        fa.fa_fwd_varlen_fp8(q, k, v, cu, int(np.max(lengths)), inp.q_descale, inp.k_descale,
+                             inp.v_descale, causal=True, out=out, lse=lse)
+
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    tf = flops / (ms / 1e3) / 1e12
+    peak = 2.0 * peak_bf16
+    return {"workload": "FP8 e4m3 packed varlen causal prefill, 32 seqs U[64,4096], H16/Hkv4, "
+                        "d128, per-tensor descales (N(0,1) quantised)",
+            "ms": ms, "tflops": tf, "frac_of_peak": tf / peak, "peak_tflops": peak,
+            "peak_source": "measured bf16 burst x 2 (nominal fp8/bf16 ratio)", "flops": flops,
+            "launches_per_call": 1}
+
+
 def measure_backward(torch, device, fa, steps, warmup, peak):
     """Backward pass (fa_bwd: dQ, dK, dV) of the long-context causal prefill
     (B=2, H=32, N=8192, d=128, the forward's own workload), timed with CUDA
@@ -580,14 +618,15 @@ def measure_decode_small_batches(torch, device, fa, steps, warmup):
     return res
 
 
-NEXT_LEGS = ("paged_prefill", "splitkv", "fp8_prefill", "backward")
+NEXT_LEGS = ("paged_prefill", "splitkv", "fp8_prefill", "fp8_varlen", "backward")
 # legs that --profile-leg can run alone (one launch kind each, for ncu captures)
 PROFILE_LEGS = NEXT_LEGS + ("dense_d64", "dense_d64_causal", "decode_small")
 
 
 def run_next_leg(name, torch, device, fa, steps, warmup, peak):
     fn = {"paged_prefill": measure_paged_prefill, "splitkv": measure_splitkv,
-          "fp8_prefill": measure_fp8_prefill, "backward": measure_backward,
+          "fp8_prefill": measure_fp8_prefill, "fp8_varlen": measure_fp8_varlen,
+          "backward": measure_backward,
           "dense_d64": lambda t, dv, f, s, w, pk: measure_dense_d64(t, dv, f, s, w, (False,)),
           "dense_d64_causal": lambda t, dv, f, s, w, pk: measure_dense_d64(t, dv, f, s, w, (True,)),
           "decode_small": lambda t, dv, f, s, w, pk: measure_decode_small_batches(t, dv, f, s, w),

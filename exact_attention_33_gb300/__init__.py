@@ -22,7 +22,7 @@ import threading
 
 __all__ = [
     "FaError", "library_path", "load_library", "fa_fwd", "fa_fwd_varlen", "fa_fwd_paged",
-    "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_fwd_fp8",
+    "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_fwd_fp8", "fa_fwd_varlen_fp8",
     "fa_bwd", "fa_bwd_workspace_size",
     "fa_decode_paged", "fa_decode_paged_noalloc", "fa_decode_workspace_size",
     "fa_status_string", "fa_device_status", "fa_last_device_status", "new_workspace",
@@ -78,6 +78,8 @@ def load_library() -> ctypes.CDLL:
         lib.fa_fwd_varlen.restype = i
         lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, f, f, f, i, vp]
         lib.fa_fwd_fp8.restype = i
+        lib.fa_fwd_varlen_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, f, f, f, i, vp]
+        lib.fa_fwd_varlen_fp8.restype = i
         lib.fa_bwd_workspace_size.argtypes = [i, i, i]
         lib.fa_bwd_workspace_size.restype = sz
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
@@ -333,6 +335,43 @@ def fa_fwd_fp8(q, k, v, q_descale, k_descale, v_descale, causal=False, scale=Non
                                        _stream_handle(stream, dev))
     if rc != FA_OK:
         raise FaError("fa_fwd_fp8", rc)
+    return out, lse
+
+
+def _check_fp8(name, t, ndim, dev):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.device != dev \
+            or t.dtype not in (torch.uint8, torch.float8_e4m3fn) or t.dim() != ndim \
+            or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-D uint8/e4m3 CUDA tensor on the "
+                         "device of q")
+
+
+def fa_fwd_varlen_fp8(q, k, v, cu_seqlens, max_seqlen, q_descale, k_descale, v_descale,
+                      causal=False, scale=None, out=None, lse=None, want_lse=True, stream=None):
+    """Packed varlen prefill on e4m3 codes.  q [T,H,d], k/v [T,Hkv,d] uint8
+    CUDA tensors holding e4m3 bits, cu_seqlens int32 [S+1] on the device;
+    per-tensor descales.  Returns (out [T,H,d] bf16, lse [H,T] fp32 or None)."""
+    torch = _torch()
+    dev = q.device if isinstance(q, torch.Tensor) else None
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_fp8(name, t, 3, dev)
+    _check_int32("cu_seqlens", cu_seqlens, dev)
+    if cu_seqlens.numel() < 1:
+        raise ValueError("cu_seqlens must hold num_seqs + 1 offsets")
+    T, H, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (T, Hkv, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [T, Hkv, d] matching q")
+    out, lse = _outputs((T, H, d), (H, T), out, lse, want_lse, dev)
+    with torch.cuda.device(dev):
+        rc = load_library().fa_fwd_varlen_fp8(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens),
+            cu_seqlens.numel() - 1, T, int(max_seqlen), H, Hkv, d, _scale(scale, d),
+            float(q_descale), float(k_descale), float(v_descale), 1 if causal else 0,
+            _stream_handle(stream, dev))
+    if rc != FA_OK:
+        raise FaError("fa_fwd_varlen_fp8", rc)
     return out, lse
 
 

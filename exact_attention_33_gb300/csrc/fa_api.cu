@@ -33,7 +33,7 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUte
                        cudaStream_t stream);
 cudaError_t launch_prefill_fp8(const CUtensorMap &tq, const CUtensorMap &tk,
                                const CUtensorMap &tv, const PrefillParams &p, bool causal,
-                               int grid, cudaStream_t stream);
+                               int grid, cudaStream_t stream, int kind = kKindDense);
 cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
                           int d, cudaStream_t stream);
 cudaError_t launch_call_status(CallStatus *call, unsigned int *dev, cudaStream_t stream);
@@ -350,9 +350,11 @@ int fa_fwd(const void *q, const void *k, const void *v, void *out, float *lse, i
   return fwd_dense(q, k, v, out, lse, B, H, Hkv, N, d, scale, causal, stream, nullptr);
 }
 
-int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float *lse,
-                  const int32_t *cu_seqlens, int num_seqs, int total_tokens, int max_seqlen,
-                  int H, int Hkv, int d, float scale, int causal, fa_stream_t stream) {
+// Packed varlen prefill, bf16 or (fp8) e4m3 codes with per-tensor descales.
+static int fwd_varlen(const void *q, const void *k, const void *v, void *out, float *lse,
+                      const int32_t *cu_seqlens, int num_seqs, int total_tokens, int max_seqlen,
+                      int H, int Hkv, int d, float scale, int causal, fa_stream_t stream, bool fp8,
+                      float q_descale, float k_descale, float v_descale) {
   if (!q || !k || !v || !out || !cu_seqlens) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
     return FA_ERR_INVALID_ARG;
@@ -360,8 +362,10 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float 
   if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0) return FA_ERR_INVALID_ARG;
   if (H < 1 || Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
+  if (!scale_ok(scale) || !scale_ok(q_descale) || !scale_ok(k_descale) || !scale_ok(v_descale))
+    return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (fp8 && d != 128) return FA_ERR_UNSUPPORTED;
   if (num_seqs == 0 || total_tokens == 0 || max_seqlen == 0) return FA_OK;
   if (max_seqlen > total_tokens) max_seqlen = total_tokens;
   // Work layouts of a packed batch.  With an even GQA group a CTA pairs two
@@ -369,9 +373,10 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float 
   // every K/V stage and have the same key tiles (3-5% faster than the other
   // layouts at every length measured).  Otherwise batches of short sequences
   // (under 4096 rows on average) run one query tile per CTA, two CTAs per SM,
-  // and longer sequences pair two consecutive 128-row tiles of one head.
+  // and longer sequences pair two consecutive 128-row tiles of one head (the
+  // fp8 kernel has the two-tile layouts only).
   constexpr int kRowsOne = 0, kRowPairs = 1, kHeadPairs = 2;
-  const bool short_seqs = static_cast<long long>(total_tokens) < 4096LL * num_seqs;
+  const bool short_seqs = !fp8 && static_cast<long long>(total_tokens) < 4096LL * num_seqs;
   const int layout = ((H / Hkv) % 2 == 0) ? kHeadPairs : (short_seqs ? kRowsOne : kRowPairs);
   const int qtiles = layout == kRowsOne ? 1 : 2;
   const int rows = layout == kRowPairs ? 2 * kPrefillBM : kPrefillBM;  // rows per work item
@@ -387,10 +392,11 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float 
   if (grid > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(total_tokens) * H * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
 
+  const int eb = fp8 ? 1 : 2;  // bytes per q, k, v element
   CUtensorMap tq, tk, tv, to;
-  int rc = make_map(&tq, q, d, H, total_tokens, 1, kPrefillBM);
-  if (rc == FA_OK) rc = make_map(&tk, k, d, Hkv, total_tokens, 1, kPrefillBN);
-  if (rc == FA_OK) rc = make_map(&tv, v, d, Hkv, total_tokens, 1, kPrefillBN);
+  int rc = make_map(&tq, q, d, H, total_tokens, 1, kPrefillBM, eb);
+  if (rc == FA_OK) rc = make_map(&tk, k, d, Hkv, total_tokens, 1, kPrefillBN, eb);
+  if (rc == FA_OK) rc = make_map(&tv, v, d, Hkv, total_tokens, 1, kPrefillBN, eb);
   if (rc == FA_OK) rc = make_map(&to, out, d, H, total_tokens, 1, kPrefillBM);
   if (rc != FA_OK) return rc;
 
@@ -410,14 +416,30 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float 
   p.max_pairs = static_cast<int>(pairs);
   p.compact = compact ? 1 : 0;
   p.total_tokens = total_tokens;
-  p.scale_log2 = scale * kLog2e;
-  p.v_descale = 1.f;
+  p.scale_log2 = scale * q_descale * k_descale * kLog2e;
+  p.v_descale = v_descale;
   p.causal = causal;
-  cudaError_t e = launch_prefill(tq, tk, tv, tv, to, p, d, causal != 0,
-                                 layout == kHeadPairs ? kKindVarlenHeads : kKindVarlen,
-                                 static_cast<int>(grid), reinterpret_cast<cudaStream_t>(stream),
-                                 qtiles);
+  const int kind = layout == kHeadPairs ? kKindVarlenHeads : kKindVarlen;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = fp8 ? launch_prefill_fp8(tq, tk, tv, p, causal != 0, static_cast<int>(grid), st, kind)
+                      : launch_prefill(tq, tk, tv, tv, to, p, d, causal != 0, kind,
+                                       static_cast<int>(grid), st, qtiles);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float *lse,
+                  const int32_t *cu_seqlens, int num_seqs, int total_tokens, int max_seqlen,
+                  int H, int Hkv, int d, float scale, int causal, fa_stream_t stream) {
+  return fwd_varlen(q, k, v, out, lse, cu_seqlens, num_seqs, total_tokens, max_seqlen, H, Hkv, d,
+                    scale, causal, stream, false, 1.f, 1.f, 1.f);
+}
+
+int fa_fwd_varlen_fp8(const void *q, const void *k, const void *v, void *out, float *lse,
+                      const int32_t *cu_seqlens, int num_seqs, int total_tokens, int max_seqlen,
+                      int H, int Hkv, int d, float scale, float q_descale, float k_descale,
+                      float v_descale, int causal, fa_stream_t stream) {
+  return fwd_varlen(q, k, v, out, lse, cu_seqlens, num_seqs, total_tokens, max_seqlen, H, Hkv, d,
+                    scale, causal, stream, true, q_descale, k_descale, v_descale);
 }
 
 int fa_fwd_fp8(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,

@@ -1138,12 +1138,24 @@ static cudaError_t launch_prefill_k(const CUtensorMap &tq, const CUtensorMap &tk
                 : launch_prefill_t<D, false, KIND, false, QT>(tq, tk, tv, tv1, to, p, grid, stream);
 }
 
+// FP8 prefill, d = 128: dense batches and packed sequences (row pairs or
+// head pairs); the output leaves by row stores, so no output map is needed.
+template <int KIND>
+static cudaError_t launch_prefill_fp8_k(const CUtensorMap &tq, const CUtensorMap &tk,
+                                        const CUtensorMap &tv, const PrefillParams &p, bool causal,
+                                        int grid, cudaStream_t stream) {
+  return causal ? launch_prefill_t<128, true, KIND, true>(tq, tk, tv, tv, tq, p, grid, stream)
+                : launch_prefill_t<128, false, KIND, true>(tq, tk, tv, tv, tq, p, grid, stream);
+}
+
 cudaError_t launch_prefill_fp8(const CUtensorMap &tq, const CUtensorMap &tk,
                                const CUtensorMap &tv, const PrefillParams &p, bool causal,
-                               int grid, cudaStream_t stream) {
-  return causal
-             ? launch_prefill_t<128, true, kKindDense, true>(tq, tk, tv, tv, tq, p, grid, stream)
-             : launch_prefill_t<128, false, kKindDense, true>(tq, tk, tv, tv, tq, p, grid, stream);
+                               int grid, cudaStream_t stream, int kind) {
+  if (kind == kKindVarlen)
+    return launch_prefill_fp8_k<kKindVarlen>(tq, tk, tv, p, causal, grid, stream);
+  if (kind == kKindVarlenHeads)
+    return launch_prefill_fp8_k<kKindVarlenHeads>(tq, tk, tv, p, causal, grid, stream);
+  return launch_prefill_fp8_k<kKindDense>(tq, tk, tv, p, causal, grid, stream);
 }
 
 cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,

@@ -133,6 +133,21 @@ int fa_fwd_fp8(const void *q, const void *k, const void *v, void *out, float *ls
                float v_descale, int causal, fa_stream_t stream);
 
 /*
+ * Packed variable-length prefill with FP8 (e4m3) inputs: the layouts and
+ * sequence rules of fa_fwd_varlen ("Varlen Is the Quiet Superpower"), the
+ * codes and per-tensor descales of fa_fwd_fp8.
+ *   q          : [total_tokens, H, d]   e4m3 codes (one byte each)
+ *   k, v       : [total_tokens, Hkv, d] e4m3 codes
+ *   out        : [total_tokens, H, d]   bf16;  lse : [H, total_tokens] fp32, may be NULL
+ *   cu_seqlens : int32 DEVICE array [num_seqs + 1] (rules as fa_fwd_varlen)
+ * Supported: d == 128.  Errors as fa_fwd_varlen and fa_fwd_fp8.
+ */
+int fa_fwd_varlen_fp8(const void *q, const void *k, const void *v, void *out, float *lse,
+                      const int32_t *cu_seqlens, int num_seqs, int total_tokens, int max_seqlen,
+                      int H, int Hkv, int d, float scale, float q_descale, float k_descale,
+                      float v_descale, int causal, fa_stream_t stream);
+
+/*
  * Gradient of dense attention (backward pass): given the forward inputs, its
  * output O and log-sum-exp, and the upstream gradient dO, writes
  *   dV = P^T dO,  dQ = scale dS K,  dK = scale dS^T Q,

@@ -35,6 +35,7 @@ BOUNDARY = sorted([
     "fa_fwd", "fa_fwd_varlen", "fa_decode_workspace_size", "fa_decode_paged",
     "fa_last_device_status", "fa_status_string",
     "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_fwd_paged", "fa_fwd_fp8",
+    "fa_fwd_varlen_fp8",
     "fa_bwd", "fa_bwd_workspace_size", "fa_decode_paged_noalloc",
     "fa_device_status", "fa_selftest_wait_timeout", "fa_version",
 ])
@@ -167,6 +168,20 @@ def test_fp8_host_validation(lib):
     assert call(d=64) == -2
     assert call(H=3, Hkv=2) == -1
     assert call(N=0) == 0
+
+
+def test_varlen_fp8_host_validation(lib):
+    import exact_attention_33_gb300  # noqa: F401  (sets argtypes)
+    f = lib.fa_fwd_varlen_fp8
+
+    def call(q=P, cu=P, n=2, T=10, mx=5, H=2, Hkv=1, d=128, descales=(1.0, 1.0, 1.0), causal=1):
+        return f(q, P, P, P, NULL, cu, n, T, mx, H, Hkv, d, 0.1, *descales, causal, NULL)
+    assert call(q=NULL) == -1
+    assert call(cu=NULL) == -1
+    assert call(descales=(1.0, float("nan"), 1.0)) == -1
+    assert call(H=3, Hkv=2) == -1
+    assert call(d=64) == -2
+    assert call(n=0) == 0
 
 
 def test_last_device_status_host_validation(lib):

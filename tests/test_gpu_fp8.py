@@ -182,3 +182,67 @@ def test_fp8_deterministic_and_rejects(fa):
     with pytest.raises(fa.FaError) as e:
         fa.fa_fwd_fp8(q, k, v, 1.0, 0.0, 1.0)
     assert e.value.status == -1
+
+
+# ---------------------------------------------------------------- packed varlen
+
+def varlen_fp8_case(inp, lengths):
+    """The tokens of a B = 1 FP8 input cut into sequences of ``lengths``."""
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    assert cu[-1] == inp.N
+    return cu
+
+
+def run_varlen_fp8(fa, inp, cu, causal):
+    torch = torch_mod()
+    dev_cu = torch.from_numpy(cu).cuda()
+    out, lse = fa.fa_fwd_varlen_fp8(dev_u8(inp.q[0]), dev_u8(inp.k[0]), dev_u8(inp.v[0]), dev_cu,
+                                    int(np.diff(cu).max()), inp.q_descale, inp.k_descale,
+                                    inp.v_descale, causal=causal, scale=inp.scale)
+    torch.cuda.synchronize()
+    return host_f64(out), lse.cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("H,Hkv", [(4, 2), (3, 1)])   # head pairs, and row pairs (odd group)
+def test_fp8_varlen_exact_weights(fa, causal, H, Hkv):
+    """Packed sequences (ragged, one empty, one of a single token) with
+    powers-of-two weights: the bf16 bar applies."""
+    lengths = [300, 1, 0, 129, 640, 77]
+    inp = W.fp8_exact_p_inputs(1, sum(lengths), H, Hkv, 128, seed=31 + H)
+    cu = varlen_fp8_case(inp, lengths)
+    out, lse = run_varlen_fp8(fa, inp, cu, causal)
+    o_ref, l_ref = oracle.attention_varlen(inp.real("q")[0], inp.real("k")[0], inp.real("v")[0],
+                                           cu, scale=inp.scale, causal=causal)
+    compare(out, o_ref, lse, l_ref, f"fp8 varlen exact H{H}/{Hkv} causal={causal}")
+    assert_device_clean()
+
+
+@pytest.mark.parametrize("H,Hkv", [(4, 2), (3, 1)])
+def test_fp8_varlen_random(fa, H, Hkv):
+    """N(0, 1) inputs quantised per tensor, causal: the e4m3 bound of
+    check_bound per sequence and head, and the relative RMS over all."""
+    lengths = [517, 64, 1300, 200]
+    inp = W.fp8_inputs(1, sum(lengths), H, Hkv, 128, seed=55 + H)
+    cu = varlen_fp8_case(inp, lengths)
+    out, lse = run_varlen_fp8(fa, inp, cu, True)
+    q, k, v = inp.real("q")[0], inp.real("k")[0], inp.real("v")[0]
+    o_ref, l_ref = oracle.attention_varlen(q, k, v, cu, causal=True)
+    scale = 1.0 / math.sqrt(128)
+    group = H // Hkv
+    errs, refs = [], []
+    for s in range(len(lengths)):
+        a, e = int(cu[s]), int(cu[s + 1])
+        rows = np.arange(e - a)
+        for h in range(H):
+            g = h // group
+            errs.append(check_bound(out[a:e, h], q[a:e, h], k[a:e, g], v[a:e, g], scale, True,
+                                    o_ref[a:e, h], l_ref[h, a:e], rows, f"fp8 varlen s{s} h{h}"))
+            refs.append(o_ref[a:e, h])
+    lerr = float(np.abs(lse - l_ref).max())
+    assert lerr <= TOL_LSE, f"fp8 varlen: max |lse err| {lerr:.3e}"
+    err = np.concatenate([x.reshape(-1) for x in errs])
+    ref = np.concatenate([x.reshape(-1) for x in refs])
+    rel = math.sqrt(float(np.mean(err ** 2)) / max(float(np.mean(ref ** 2)), 1e-30))
+    assert rel <= REL_RMS_MAX, f"fp8 varlen: relative RMS error {rel:.4f} > {REL_RMS_MAX}"
+    assert_device_clean()
