@@ -567,10 +567,11 @@ def measure_splitkv(torch, device, fa, steps, warmup, peak):
             "launches_per_call": 2}
 
 
-def measure_dense_d64(torch, device, fa, steps, warmup, modes=(False, True)):
+def measure_dense_d64(torch, device, fa, steps, warmup, modes=(False, True), fp8=True):
     """The dense configuration of the workload list (B=4, H=Hkv=16, N=2048,
     d=64, bf16 N(0,1)), non-causal and causal (``modes``: the causal flags
-    to run).  Its inputs fit in L2, so L2 is flushed (a 256 MiB write)
+    to run), and (``fp8``) the same shape on e4m3 inputs quantised per
+    tensor.  Its inputs fit in L2, so L2 is flushed (a 256 MiB write)
     before every timed launch and only the launch is timed."""
     cfg = W.WORKLOADS["dense_d64"]
     B, N, H, Hkv, d = cfg["B"], cfg["N"], cfg["H"], cfg["Hkv"], cfg["d"]
@@ -586,6 +587,17 @@ def measure_dense_d64(torch, device, fa, steps, warmup, modes=(False, True)):
         flops = W.prefill_flops(B, N, H, d, causal)
         res["causal" if causal else "non_causal"] = {"ms": ms, "tflops": flops / (ms / 1e3) / 1e12,
                                                      "flops": flops}
+    if fp8:
+        f8 = W.fp8_inputs(B, N, H, Hkv, d, seed=0)
+        fq, fk, fv = (torch.from_numpy(getattr(f8, n)).to(device) for n in ("q", "k", "v"))
+        for causal in modes:
+            ms = time_flushed(
+                torch, lambda: fa.fa_fwd_fp8(fq, fk, fv, f8.q_descale, f8.k_descale, f8.v_descale,
+                                             causal=causal, out=out, lse=lse),
+                steps, warmup, flush)
+            flops = W.prefill_flops(B, N, H, d, causal)
+            res["fp8_causal" if causal else "fp8_non_causal"] = {
+                "ms": ms, "tflops": flops / (ms / 1e3) / 1e12, "flops": flops}
     if fa.fa_device_status(clear=True) != 0:
         raise RuntimeError("device status word set during the dense d64 leg")
     return res
@@ -627,8 +639,9 @@ def run_next_leg(name, torch, device, fa, steps, warmup, peak):
     fn = {"paged_prefill": measure_paged_prefill, "splitkv": measure_splitkv,
           "fp8_prefill": measure_fp8_prefill, "fp8_varlen": measure_fp8_varlen,
           "backward": measure_backward,
-          "dense_d64": lambda t, dv, f, s, w, pk: measure_dense_d64(t, dv, f, s, w, (False,)),
-          "dense_d64_causal": lambda t, dv, f, s, w, pk: measure_dense_d64(t, dv, f, s, w, (True,)),
+          "dense_d64": lambda t, dv, f, s, w, pk: measure_dense_d64(t, dv, f, s, w, (False,), False),
+          "dense_d64_causal": lambda t, dv, f, s, w, pk: measure_dense_d64(t, dv, f, s, w, (True,),
+                                                                           False),
           "decode_small": lambda t, dv, f, s, w, pk: measure_decode_small_batches(t, dv, f, s, w),
           }[name]
     res = fn(torch, device, fa, steps, warmup, peak)

@@ -33,7 +33,7 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUte
                        cudaStream_t stream);
 cudaError_t launch_prefill_fp8(const CUtensorMap &tq, const CUtensorMap &tk,
                                const CUtensorMap &tv, const PrefillParams &p, bool causal,
-                               int grid, cudaStream_t stream, int kind = kKindDense);
+                               int grid, cudaStream_t stream, int kind, int d);
 cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
                           int d, cudaStream_t stream);
 cudaError_t launch_call_status(CallStatus *call, unsigned int *dev, cudaStream_t stream);
@@ -60,11 +60,12 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 // Tensor [outer][rows][heads][d] (d innermost) of bf16 (or one-byte, or
 // fp32) elements as a 4-D TMA map with dims {d, heads, rows, outer}; each
-// copy moves a box of one 128-byte swizzle row per (head, row): {64, 1,
-// box_rows, 1} bf16 values.  Out-of-range rows read as zero and are not
-// stored.
+// copy moves a box of one swizzled row of swz_bytes per (head, row): {64, 1,
+// box_rows, 1} bf16 values with the 128-byte swizzle, or, for e4m3 rows of
+// d = 64, {64, 1, box_rows, 1} bytes with the 64-byte swizzle.
+// Out-of-range rows read as zero and are not stored.
 int make_map(CUtensorMap *map, const void *base, int d, int heads, long long rows,
-             long long outer, int box_rows, int elem_bytes = 2) {
+             long long outer, int box_rows, int elem_bytes = 2, int swz_bytes = 128) {
   auto fn = encode_fn();
   if (fn == nullptr) return FA_ERR_CUDA;
   const cuuint64_t eb = static_cast<cuuint64_t>(elem_bytes);
@@ -73,18 +74,21 @@ int make_map(CUtensorMap *map, const void *base, int d, int heads, long long row
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * eb,
                                  static_cast<cuuint64_t>(heads) * d * eb,
                                  static_cast<cuuint64_t>(rows) * heads * d * eb};
-  // one 128-byte swizzle row per copy: 64 bf16 or 128 one-byte values
-  const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / elem_bytes), 1,
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(swz_bytes / elem_bytes), 1,
                              static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapDataType dt = elem_bytes == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                  : elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  CUresult r = fn(map, dt, 4, const_cast<void *>(base), dims,
-                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = fn(map, dt, 4, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swz_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
+
+// Swizzled row bytes of the prefill kernels for e4m3 rows of d values.
+int fp8_swz(int d) { return d < 128 ? d : 128; }
 
 // Paged pool [num_blocks * block_size tokens][Hkv][d] as a 3-D map; each copy
 // moves {64, 1, box_rows} (a whole 16-token block, or one token row).
@@ -365,7 +369,6 @@ static int fwd_varlen(const void *q, const void *k, const void *v, void *out, fl
   if (!scale_ok(scale) || !scale_ok(q_descale) || !scale_ok(k_descale) || !scale_ok(v_descale))
     return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (fp8 && d != 128) return FA_ERR_UNSUPPORTED;
   if (num_seqs == 0 || total_tokens == 0 || max_seqlen == 0) return FA_OK;
   if (max_seqlen > total_tokens) max_seqlen = total_tokens;
   // Work layouts of a packed batch.  With an even GQA group a CTA pairs two
@@ -392,11 +395,12 @@ static int fwd_varlen(const void *q, const void *k, const void *v, void *out, fl
   if (grid > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(total_tokens) * H * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
 
-  const int eb = fp8 ? 1 : 2;  // bytes per q, k, v element
+  const int eb = fp8 ? 1 : 2;               // bytes per q, k, v element
+  const int swz = fp8 ? fp8_swz(d) : 128;   // swizzled row bytes
   CUtensorMap tq, tk, tv, to;
-  int rc = make_map(&tq, q, d, H, total_tokens, 1, kPrefillBM, eb);
-  if (rc == FA_OK) rc = make_map(&tk, k, d, Hkv, total_tokens, 1, kPrefillBN, eb);
-  if (rc == FA_OK) rc = make_map(&tv, v, d, Hkv, total_tokens, 1, kPrefillBN, eb);
+  int rc = make_map(&tq, q, d, H, total_tokens, 1, kPrefillBM, eb, swz);
+  if (rc == FA_OK) rc = make_map(&tk, k, d, Hkv, total_tokens, 1, kPrefillBN, eb, swz);
+  if (rc == FA_OK) rc = make_map(&tv, v, d, Hkv, total_tokens, 1, kPrefillBN, eb, swz);
   if (rc == FA_OK) rc = make_map(&to, out, d, H, total_tokens, 1, kPrefillBM);
   if (rc != FA_OK) return rc;
 
@@ -421,7 +425,7 @@ static int fwd_varlen(const void *q, const void *k, const void *v, void *out, fl
   p.causal = causal;
   const int kind = layout == kHeadPairs ? kKindVarlenHeads : kKindVarlen;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = fp8 ? launch_prefill_fp8(tq, tk, tv, p, causal != 0, static_cast<int>(grid), st, kind)
+  cudaError_t e = fp8 ? launch_prefill_fp8(tq, tk, tv, p, causal != 0, static_cast<int>(grid), st, kind, d)
                       : launch_prefill(tq, tk, tv, tv, to, p, d, causal != 0, kind,
                                        static_cast<int>(grid), st, qtiles);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -454,16 +458,16 @@ int fa_fwd_fp8(const void *q, const void *k, const void *v, void *out, float *ls
   if (!scale_ok(scale) || !scale_ok(q_descale) || !scale_ok(k_descale) ||
       !scale_ok(v_descale))
     return FA_ERR_INVALID_ARG;
-  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (B == 0 || N == 0) return FA_OK;
   const long long pairs = (N + kPrefillRowsPerCta - 1) / kPrefillRowsPerCta;
   const long long grid = pairs * B * H;
   if (grid > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(N) * H * d >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
   CUtensorMap tq, tk, tv;
-  int rc = make_map(&tq, q, d, H, N, B, kPrefillBM, 1);
-  if (rc == FA_OK) rc = make_map(&tk, k, d, Hkv, N, B, kPrefillBN, 1);
-  if (rc == FA_OK) rc = make_map(&tv, v, d, Hkv, N, B, kPrefillBN, 1);
+  int rc = make_map(&tq, q, d, H, N, B, kPrefillBM, 1, fp8_swz(d));
+  if (rc == FA_OK) rc = make_map(&tk, k, d, Hkv, N, B, kPrefillBN, 1, fp8_swz(d));
+  if (rc == FA_OK) rc = make_map(&tv, v, d, Hkv, N, B, kPrefillBN, 1, fp8_swz(d));
   if (rc != FA_OK) return rc;
   PrefillParams p{};
   p.status = status_ptr();
@@ -481,7 +485,7 @@ int fa_fwd_fp8(const void *q, const void *k, const void *v, void *out, float *ls
   p.v_descale = v_descale;
   p.causal = causal;
   cudaError_t e = launch_prefill_fp8(tq, tk, tv, p, causal != 0, static_cast<int>(grid),
-                                     reinterpret_cast<cudaStream_t>(stream));
+                                     reinterpret_cast<cudaStream_t>(stream), kKindDense, d);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -52,10 +52,15 @@ constexpr float kRescaleLog2 = 8.f;
 template <int D, bool FP8 = false, int QT = 2>
 struct PrefillLayout {
   static constexpr int kElemBytes = FP8 ? 1 : 2;
-  static constexpr int kChunkElems = 128 / kElemBytes;   // elements per 128-byte swizzle row
-  static constexpr int kChunkBytes = 128 * 128;          // 128 rows x 128 bytes
-  static constexpr int kChunks = D * kElemBytes / 128;
+  // Rows are copied and read in swizzled rows of 128 bytes, or of 64 bytes
+  // when a whole row is that short (e4m3 at d = 64: the 64-byte swizzle).
+  static constexpr int kSwz = (D * kElemBytes < 128) ? D * kElemBytes : 128;
+  static constexpr int kChunkElems = kSwz / kElemBytes;  // elements per swizzled row
+  static constexpr int kChunkBytes = 128 * kSwz;         // 128 rows x one swizzled row
+  static constexpr int kChunks = D * kElemBytes / kSwz;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
+  static constexpr int kSbo = 8 * kSwz;                  // bytes per 8-row core matrix group
+  static_assert(kSwz == 128 || kSwz == 64, "128- or 64-byte rows");
   // K and V have rings of their own: a K stage is released as soon as both
   // S MMAs have read it, a V stage after both P V MMAs.
 #ifndef FA_PREFILL_STAGES_K128
@@ -552,11 +557,13 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
       auto issue_s = [&](int i, int st) {
         const uint32_t d_t = tmem + i * 128;
         if (elect_one()) {
-          const uint64_t a0 = sdesc_sw128(q_base + i * L::kTileBytes, 16, 1024);
-          const uint64_t b0 = sdesc_sw128(k_base + st * L::kTileBytes, 16, 1024);
+          const uint64_t a0 = sdesc_swz<L::kSwz>(q_base + i * L::kTileBytes, 16, L::kSbo);
+          const uint64_t b0 = sdesc_swz<L::kSwz>(k_base + st * L::kTileBytes, 16, L::kSbo);
+          constexpr int kStepsPerRow = L::kSwz / 32;  // 32-byte K-steps in a swizzled row
 #pragma unroll
           for (int kk = 0; kk < D / kKStep; ++kk) {
-            const uint64_t off = static_cast<uint64_t>(((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4);
+            const uint64_t off = static_cast<uint64_t>(
+                ((kk / kStepsPerRow) * L::kChunkBytes + (kk % kStepsPerRow) * 32) >> 4);
             if (FP8)
               mma_ss_f8(d_t, a0 + off, b0 + off, kIdescS, kk > 0 ? 1u : 0u);
             else
@@ -573,11 +580,11 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
           // N beyond D (the ones block) is read at the leading-byte offset
           const uint32_t lbo = ONES ? static_cast<uint32_t>(L::kOnesOff - (L::kV + st * L::kTileBytes))
                                     : static_cast<uint32_t>(L::kChunkBytes);
-          const uint64_t b0 = sdesc_sw128(v_base + st * L::kTileBytes, lbo, 1024);
+          const uint64_t b0 = sdesc_swz<L::kSwz>(v_base + st * L::kTileBytes, lbo, L::kSbo);
 #pragma unroll
           for (int kk = 0; kk < kPrefillBN / kKStep; ++kk) {
-            // kKStep keys of 128-byte rows; P holds kKStep keys in 8 TMEM columns
-            const uint64_t off = static_cast<uint64_t>((kk * kKStep * 128) >> 4);
+            // kKStep keys of swizzled rows; P holds kKStep keys in 8 TMEM columns
+            const uint64_t off = static_cast<uint64_t>((kk * kKStep * L::kSwz) >> 4);
             if (FP8)
               mma_ts_f8(d_t, p_t + kk * 8, b0 + off, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
             else
@@ -1138,24 +1145,32 @@ static cudaError_t launch_prefill_k(const CUtensorMap &tq, const CUtensorMap &tk
                 : launch_prefill_t<D, false, KIND, false, QT>(tq, tk, tv, tv1, to, p, grid, stream);
 }
 
-// FP8 prefill, d = 128: dense batches and packed sequences (row pairs or
-// head pairs); the output leaves by row stores, so no output map is needed.
-template <int KIND>
+// FP8 prefill, d = 64 or 128: dense batches and packed sequences (row pairs
+// or head pairs); the output leaves by row stores, so no output map is needed.
+template <int D, int KIND>
 static cudaError_t launch_prefill_fp8_k(const CUtensorMap &tq, const CUtensorMap &tk,
                                         const CUtensorMap &tv, const PrefillParams &p, bool causal,
                                         int grid, cudaStream_t stream) {
-  return causal ? launch_prefill_t<128, true, KIND, true>(tq, tk, tv, tv, tq, p, grid, stream)
-                : launch_prefill_t<128, false, KIND, true>(tq, tk, tv, tv, tq, p, grid, stream);
+  return causal ? launch_prefill_t<D, true, KIND, true>(tq, tk, tv, tv, tq, p, grid, stream)
+                : launch_prefill_t<D, false, KIND, true>(tq, tk, tv, tv, tq, p, grid, stream);
+}
+
+template <int D>
+static cudaError_t launch_prefill_fp8_d(const CUtensorMap &tq, const CUtensorMap &tk,
+                                        const CUtensorMap &tv, const PrefillParams &p, bool causal,
+                                        int grid, cudaStream_t stream, int kind) {
+  if (kind == kKindVarlen)
+    return launch_prefill_fp8_k<D, kKindVarlen>(tq, tk, tv, p, causal, grid, stream);
+  if (kind == kKindVarlenHeads)
+    return launch_prefill_fp8_k<D, kKindVarlenHeads>(tq, tk, tv, p, causal, grid, stream);
+  return launch_prefill_fp8_k<D, kKindDense>(tq, tk, tv, p, causal, grid, stream);
 }
 
 cudaError_t launch_prefill_fp8(const CUtensorMap &tq, const CUtensorMap &tk,
                                const CUtensorMap &tv, const PrefillParams &p, bool causal,
-                               int grid, cudaStream_t stream, int kind) {
-  if (kind == kKindVarlen)
-    return launch_prefill_fp8_k<kKindVarlen>(tq, tk, tv, p, causal, grid, stream);
-  if (kind == kKindVarlenHeads)
-    return launch_prefill_fp8_k<kKindVarlenHeads>(tq, tk, tv, p, causal, grid, stream);
-  return launch_prefill_fp8_k<kKindDense>(tq, tk, tv, p, causal, grid, stream);
+                               int grid, cudaStream_t stream, int kind, int d) {
+  return d == 64 ? launch_prefill_fp8_d<64>(tq, tk, tv, p, causal, grid, stream, kind)
+                 : launch_prefill_fp8_d<128>(tq, tk, tv, p, causal, grid, stream, kind);
 }
 
 cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,

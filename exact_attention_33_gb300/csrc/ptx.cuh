@@ -261,6 +261,21 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// The same descriptor for rows of SWZ bytes in the matching swizzle: 128
+// (layout type 2, as sdesc_sw128) or 64 (layout type 4).
+template <int SWZ>
+__device__ __forceinline__ uint64_t sdesc_swz(uint32_t saddr, uint32_t lbo_bytes,
+                                              uint32_t sbo_bytes) {
+  static_assert(SWZ == 128 || SWZ == 64, "128- or 64-byte swizzle");
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(SWZ == 128 ? 2 : 4) << 61;
+  return d;
+}
+
 // Instruction descriptor, kind::f16 with bf16 inputs and an fp32 accumulator.
 //   bits 4-5 D type (1 = f32), 7-9 A type (1 = bf16), 10-12 B type (1 = bf16),
 //   bit 15 A is MN-major, bit 16 B is MN-major, bits 17-22 N >> 3,

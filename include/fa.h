@@ -126,7 +126,7 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float 
  * rounded to e4m3 for the P V product, so the output error is bounded by
  * about 2^-4 times the attention-weighted mean of |v| (see the tests).
  *   out : [B, N, H, d] bf16;  lse : [B, H, N] fp32, may be NULL
- * Supported: d == 128.
+ * Supported: d == 64 or 128 (other d: FA_ERR_UNSUPPORTED).
  */
 int fa_fwd_fp8(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
                int Hkv, int N, int d, float scale, float q_descale, float k_descale,
@@ -140,7 +140,7 @@ int fa_fwd_fp8(const void *q, const void *k, const void *v, void *out, float *ls
  *   k, v       : [total_tokens, Hkv, d] e4m3 codes
  *   out        : [total_tokens, H, d]   bf16;  lse : [H, total_tokens] fp32, may be NULL
  *   cu_seqlens : int32 DEVICE array [num_seqs + 1] (rules as fa_fwd_varlen)
- * Supported: d == 128.  Errors as fa_fwd_varlen and fa_fwd_fp8.
+ * Supported: d == 64 or 128.  Errors as fa_fwd_varlen and fa_fwd_fp8.
  */
 int fa_fwd_varlen_fp8(const void *q, const void *k, const void *v, void *out, float *lse,
                       const int32_t *cu_seqlens, int num_seqs, int total_tokens, int max_seqlen,

@@ -165,7 +165,7 @@ def test_fp8_host_validation(lib):
     assert call(q=NULL) == -1
     assert call(descales=(1.0, float("inf"), 1.0)) == -1
     assert call(descales=(1.0, 1.0, -2.0)) == -1
-    assert call(d=64) == -2
+    assert call(d=96) == -2
     assert call(H=3, Hkv=2) == -1
     assert call(N=0) == 0
 
@@ -180,7 +180,7 @@ def test_varlen_fp8_host_validation(lib):
     assert call(cu=NULL) == -1
     assert call(descales=(1.0, float("nan"), 1.0)) == -1
     assert call(H=3, Hkv=2) == -1
-    assert call(d=64) == -2
+    assert call(d=96) == -2
     assert call(n=0) == 0
 
 

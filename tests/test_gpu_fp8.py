@@ -105,28 +105,31 @@ def check_random(out, lse, inp, causal, o_ref, l_ref, what, sample=None):
     return rel
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N,H,Hkv", [(1, 2, 1), (100, 2, 1), (300, 4, 4), (1000, 4, 2),
                                      (2500, 2, 1)])
-def test_fp8_exact_weights(fa, causal, N, H, Hkv):
-    """Powers-of-two weights: the e4m3 P is exact, so the bf16 bar applies."""
-    inp = W.fp8_exact_p_inputs(1, N, H, Hkv, 128, seed=N + H)
+def test_fp8_exact_weights(fa, causal, N, H, Hkv, d):
+    """Powers-of-two weights: the e4m3 P is exact, so the bf16 bar applies.
+    At d = 64 an e4m3 row is 64 bytes (the 64-byte swizzle)."""
+    inp = W.fp8_exact_p_inputs(1, N, H, Hkv, d, seed=N + H + d)
     out, lse = run_fp8(fa, inp, causal)
     o_ref, l_ref = oracle.attention_dense(inp.real("q"), inp.real("k"), inp.real("v"),
                                           scale=inp.scale, causal=causal)
-    compare(out, o_ref, lse, l_ref, f"fp8 exact N{N} H{H}/{Hkv} causal={causal}")
+    compare(out, o_ref, lse, l_ref, f"fp8 exact N{N} H{H}/{Hkv} d{d} causal={causal}")
     assert_device_clean()
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("B,N,H,Hkv", [(1, 200, 2, 1), (2, 777, 4, 2), (1, 1500, 2, 2)])
-def test_fp8_random(fa, causal, B, N, H, Hkv):
-    inp = W.fp8_inputs(B, N, H, Hkv, 128, seed=40 + N)
+def test_fp8_random(fa, causal, B, N, H, Hkv, d):
+    inp = W.fp8_inputs(B, N, H, Hkv, d, seed=40 + N + d)
     out, lse = run_fp8(fa, inp, causal)
     o_ref, l_ref = oracle.attention_dense(inp.real("q"), inp.real("k"), inp.real("v"),
                                           causal=causal)
-    rel = check_random(out, lse, inp, causal, o_ref, l_ref, f"fp8 N{N} causal={causal}")
-    print(f"fp8 N{N} B{B} H{H}/{Hkv} causal={causal}: relative RMS error {rel:.4f}")
+    rel = check_random(out, lse, inp, causal, o_ref, l_ref, f"fp8 N{N} d{d} causal={causal}")
+    print(f"fp8 N{N} B{B} H{H}/{Hkv} d{d} causal={causal}: relative RMS error {rel:.4f}")
     assert_device_clean()
 
 
@@ -175,9 +178,9 @@ def test_fp8_deterministic_and_rejects(fa):
     o2, l2 = fa.fa_fwd_fp8(q, k, v, 1.0, 1.0, 1.0, causal=True)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
-    q64 = torch.zeros((1, 8, 2, 64), dtype=torch.uint8, device="cuda")
+    q96 = torch.zeros((1, 8, 2, 96), dtype=torch.uint8, device="cuda")
     with pytest.raises(fa.FaError) as e:
-        fa.fa_fwd_fp8(q64, q64, q64, 1.0, 1.0, 1.0)
+        fa.fa_fwd_fp8(q96, q96, q96, 1.0, 1.0, 1.0)
     assert e.value.status == -2
     with pytest.raises(fa.FaError) as e:
         fa.fa_fwd_fp8(q, k, v, 1.0, 0.0, 1.0)
@@ -203,32 +206,34 @@ def run_varlen_fp8(fa, inp, cu, causal):
     return host_f64(out), lse.cpu().numpy().astype(np.float64)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("H,Hkv", [(4, 2), (3, 1)])   # head pairs, and row pairs (odd group)
-def test_fp8_varlen_exact_weights(fa, causal, H, Hkv):
+def test_fp8_varlen_exact_weights(fa, causal, H, Hkv, d):
     """Packed sequences (ragged, one empty, one of a single token) with
     powers-of-two weights: the bf16 bar applies."""
     lengths = [300, 1, 0, 129, 640, 77]
-    inp = W.fp8_exact_p_inputs(1, sum(lengths), H, Hkv, 128, seed=31 + H)
+    inp = W.fp8_exact_p_inputs(1, sum(lengths), H, Hkv, d, seed=31 + H + d)
     cu = varlen_fp8_case(inp, lengths)
     out, lse = run_varlen_fp8(fa, inp, cu, causal)
     o_ref, l_ref = oracle.attention_varlen(inp.real("q")[0], inp.real("k")[0], inp.real("v")[0],
                                            cu, scale=inp.scale, causal=causal)
-    compare(out, o_ref, lse, l_ref, f"fp8 varlen exact H{H}/{Hkv} causal={causal}")
+    compare(out, o_ref, lse, l_ref, f"fp8 varlen exact H{H}/{Hkv} d{d} causal={causal}")
     assert_device_clean()
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("H,Hkv", [(4, 2), (3, 1)])
-def test_fp8_varlen_random(fa, H, Hkv):
+def test_fp8_varlen_random(fa, H, Hkv, d):
     """N(0, 1) inputs quantised per tensor, causal: the e4m3 bound of
     check_bound per sequence and head, and the relative RMS over all."""
     lengths = [517, 64, 1300, 200]
-    inp = W.fp8_inputs(1, sum(lengths), H, Hkv, 128, seed=55 + H)
+    inp = W.fp8_inputs(1, sum(lengths), H, Hkv, d, seed=55 + H + d)
     cu = varlen_fp8_case(inp, lengths)
     out, lse = run_varlen_fp8(fa, inp, cu, True)
     q, k, v = inp.real("q")[0], inp.real("k")[0], inp.real("v")[0]
     o_ref, l_ref = oracle.attention_varlen(q, k, v, cu, causal=True)
-    scale = 1.0 / math.sqrt(128)
+    scale = 1.0 / math.sqrt(d)
     group = H // Hkv
     errs, refs = [], []
     for s in range(len(lengths)):
