@@ -341,6 +341,7 @@ static int fwd_dense(const void *q, const void *k, const void *v, void *out, flo
   p.scale_log2 = scale * kLog2e;
   p.v_descale = 1.f;
   p.causal = causal;
+  p.prefetch_ahead = std::max(0, sm_count());  // one CTA per SM
   cudaError_t e = launch_prefill(tq, tk, tv, tv, to, p, d, causal != 0,
                                  head_pairs ? kKindDenseHeads : kKindDense,
                                  static_cast<int>(grid), reinterpret_cast<cudaStream_t>(stream));
@@ -423,6 +424,7 @@ static int fwd_varlen(const void *q, const void *k, const void *v, void *out, fl
   p.scale_log2 = scale * q_descale * k_descale * kLog2e;
   p.v_descale = v_descale;
   p.causal = causal;
+  p.prefetch_ahead = std::max(0, sm_count()) * (qtiles == 1 ? 2 : 1);  // CTAs resident at once
   const int kind = layout == kHeadPairs ? kKindVarlenHeads : kKindVarlen;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = fp8 ? launch_prefill_fp8(tq, tk, tv, p, causal != 0, static_cast<int>(grid), st, kind, d)
@@ -484,6 +486,7 @@ int fa_fwd_fp8(const void *q, const void *k, const void *v, void *out, float *ls
   p.scale_log2 = scale * q_descale * k_descale * kLog2e;
   p.v_descale = v_descale;
   p.causal = causal;
+  p.prefetch_ahead = std::max(0, sm_count());
   cudaError_t e = launch_prefill_fp8(tq, tk, tv, p, causal != 0, static_cast<int>(grid),
                                      reinterpret_cast<cudaStream_t>(stream), kKindDense, d);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;

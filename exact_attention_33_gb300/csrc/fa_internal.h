@@ -91,6 +91,10 @@ struct PrefillParams {
   float scale_log2;       // scale * log2(e) (times the q and k descales for fp8)
   float v_descale;        // multiplies the output (1 for bf16)
   int causal;
+  // dense and packed kinds: each CTA prefetches into L2 the Q tiles of work
+  // item (its own + prefetch_ahead), the one that starts about a wave later
+  // (0: none)
+  int prefetch_ahead;
   // split kind only: partial states
   int num_splits;
   float *o_part;   // fp32 [splits, B, N, H, d]

@@ -190,21 +190,24 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
   const int split = (KIND == kKindDenseSplit) ? static_cast<int>(blockIdx.x % p.num_splits) : 0;
   const int lin = (KIND == kKindDenseSplit) ? static_cast<int>(blockIdx.x / p.num_splits)
                                             : static_cast<int>(blockIdx.x);
-  int h, unit, pair;  // unit: batch element or sequence
-  if ((KIND == kKindVarlen || KIND == kKindVarlenHeads) && p.compact) {
-    if (!varlen_compact_item<kCtaRows, kHeadStep>(p, lin, CAUSAL, unit, pair, h))
-      return;  // past the last item
-  } else {
+  // (unit, pair, h) of work item x; false past the last item.  Collective
+  // over the warp for a compact packed batch.
+  auto decode_item = [&](int x, int &unit_x, int &pair_x, int &h_x) -> bool {
+    if ((KIND == kKindVarlen || KIND == kKindVarlenHeads) && p.compact)
+      return varlen_compact_item<kCtaRows, kHeadStep>(p, x, CAUSAL, unit_x, pair_x, h_x);
     const int hgs = p.head_group / kHeadStep;  // head slots per ordering group
     const int slots = p.H / kHeadStep;
-    const int h_in = lin % hgs;
-    const int t_lin = lin / hgs;
+    const int h_in = x % hgs;
+    const int t_lin = x / hgs;
     const int pair_rank = t_lin % p.max_pairs;
     const int grp = t_lin / p.max_pairs;
-    h = ((grp % (slots / hgs)) * hgs + h_in) * kHeadStep;
-    unit = grp / (slots / hgs);
-    pair = CAUSAL ? (p.max_pairs - 1 - pair_rank) : pair_rank;
-  }
+    h_x = ((grp % (slots / hgs)) * hgs + h_in) * kHeadStep;
+    unit_x = grp / (slots / hgs);
+    pair_x = CAUSAL ? (p.max_pairs - 1 - pair_rank) : pair_rank;
+    return true;
+  };
+  int h, unit, pair;  // unit: batch element or sequence
+  if (!decode_item(lin, unit, pair, h)) return;  // past the last item
   // len: query rows of the unit; kv_len: its keys; offset = kv_len - len
   // aligns causal masking to the bottom right (query i sees keys
   // j <= i + offset).
@@ -494,6 +497,33 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
     }
   } else if (warp == Sh::kTmaWarp) {
     // ------------------------------------------------------ TMA producer
+    // The Q tiles of the work item that starts about a wave after this one
+    // are read from HBM once: prefetch them into L2 now, so that CTA's first
+    // S waits for L2 instead of HBM.
+    if (KIND != kKindDenseSplit && p.prefetch_ahead > 0) {
+      const long long ahead = static_cast<long long>(lin) + p.prefetch_ahead;
+      int unit2 = 0, pair2 = 0, h2 = 0;
+      if (ahead < static_cast<long long>(gridDim.x) &&
+          decode_item(static_cast<int>(ahead), unit2, pair2, h2)) {
+        int start2 = 0, len2 = p.N;
+        if (!DENSE) {
+          start2 = checked_load(p.cu_seqlens, unit2, p.B + 1, p.status);
+          len2 = min(checked_load(p.cu_seqlens, unit2 + 1, p.B + 1, p.status), p.total_tokens) -
+                 start2;
+        }
+        const int r2 = pair2 * kCtaRows;
+        if (lane == 0 && start2 >= 0 && r2 < len2) {
+          for (int i = 0; i < QT; ++i) {
+            const int t2 = HP ? r2 : r2 + i * kPrefillBM;
+            if (t2 >= len2) break;
+#pragma unroll
+            for (int c = 0; c < L::kChunks; ++c)
+              tma_prefetch_4d(&tm_q, c * L::kChunkElems, HP ? h2 + i : h2, start2 + t2,
+                              DENSE ? unit2 : 0);
+          }
+        }
+      }
+    }
     if (lane == 0) {
       // Issue order K(0) (already issued with Q), then V(j), K(j+1) for
       // every j: a V load never waits behind a K stage that frees later.

@@ -172,6 +172,15 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, u
       : "memory");
 }
 
+// Prefetch of a 4-D tile into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *map, int c0, int c1, int c2,
+                                                int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+
 // 4-D tiled bulk tensor store from shared memory (bulk-group completion).
 __device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, const void *src, int c0,
                                              int c1, int c2, int c3) {
