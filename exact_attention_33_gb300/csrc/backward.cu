@@ -133,8 +133,9 @@ __device__ __forceinline__ void store_row_scaled_bf16(void *dst_row, const uint3
 
 // ------------------------------------------------------------------ preprocess
 // D / 8 threads per (b, row, h), 16 bytes each: D = sum_c dO * O (fp32 from
-// bf16) and the forward log-sum-exp in log2 units (+inf for rows past N or
-// rows without a visible key, so that every weight recomputed from it is 0).
+// bf16) and the forward log-sum-exp in log2 units, both stored negated (the
+// consumers add them); -lse is -inf for rows past N or rows without a visible
+// key, so that every weight recomputed from it is 0.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) {
   constexpr int TPR = D / 8;  // threads per row
@@ -173,11 +174,11 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
     if (row < p.N) {
       const float l = checked_load(p.lse, (static_cast<size_t>(b) * p.H + h) * p.N + row,
                                    n_rows, p.status);
-      p.lse2[vec] = (l == -CUDART_INF_F) ? CUDART_INF_F : l * kLog2eF;
-      p.dsum[vec] = acc;
+      p.nlse2[vec] = (l == -CUDART_INF_F) ? -CUDART_INF_F : -(l * kLog2eF);
+      p.ndsum[vec] = -acc;
     } else {
-      p.lse2[vec] = CUDART_INF_F;
-      p.dsum[vec] = 0.f;
+      p.nlse2[vec] = -CUDART_INF_F;
+      p.ndsum[vec] = 0.f;
     }
   }
 }
@@ -341,9 +342,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tS = tmem + lane_off, tP = tmem + 128 + lane_off, tQ = tmem + 256 + lane_off;
     const size_t vec = (static_cast<size_t>(b) * p.H + h) * p.Npad + min(qi, p.Npad - 1);
     const size_t n_vec = static_cast<size_t>(p.B) * p.H * p.Npad;
-    const float lse2 = checked_load(p.lse2, vec, n_vec, p.status);
-    const float dsum = checked_load(p.dsum, vec, n_vec, p.status);
+    const float nlse2 = checked_load(p.nlse2, vec, n_vec, p.status);  // -lse (log2 units)
+    const float ndsum = checked_load(p.ndsum, vec, n_vec, p.status);  // -D
     const float sl2 = p.scale_log2;
+    const float2 sl2x2 = make_float2(sl2, sl2);
+    const float2 nl2 = make_float2(nlse2, nlse2), nd2 = make_float2(ndsum, ndsum);
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       ok = mbar_wait(s_full, j & 1, abort_flag, p.status);
@@ -354,17 +357,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int nvis = min(128, (CAUSAL ? min(p.N, qi + 1) : p.N) - j * 128);
       // P = exp(S * scale - lse) of this half's 64 keys, kept as bf16 pairs
       // (the values the dQ product uses through dS)
+      // (packed pairs; the mask is applied only in chunks that reach past nvis)
       uint32_t pp[32];
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int c = 2 * hf + cc;
         uint32_t sv[32];
         tmem_ld32_wait(tS + c * 32, sv);
+        const bool part = c * 32 + 32 > nvis;
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float w0 = (c * 32 + e < nvis) ? ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse2)) : 0.f;
-          const float w1 =
-              (c * 32 + e + 1 < nvis) ? ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -lse2)) : 0.f;
+          const float2 x =
+              ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sl2x2, nl2);
+          float w0 = ex2(x.x), w1 = ex2(x.y);
+          if (part) {
+            w0 = (c * 32 + e < nvis) ? w0 : 0.f;
+            w1 = (c * 32 + e + 1 < nvis) ? w1 : 0.f;
+          }
           pp[cc * 16 + (e >> 1)] = pack_bf16x2(w0, w1);
         }
       }
@@ -383,8 +392,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const float2 w = bf16x2_to_float2(pp[cc * 16 + (e >> 1)]);
-          pk[e >> 1] = pack_bf16x2(w.x * (__uint_as_float(dp[e]) - dsum),
-                                   w.y * (__uint_as_float(dp[e + 1]) - dsum));
+          const float2 r = fmul2(
+              w, fadd2(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd2));
+          pk[e >> 1] = pack_bf16x2(r.x, r.y);
         }
         tmem_st16(tP + hf * 64 + cc * 16, pk);
       }
@@ -454,7 +464,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t *sK = smem + L::kA;
   uint8_t *sV = smem + L::kB;
   uint8_t *sR = smem + L::kR0;  // stage s: Q at 2s, dO at 2s + 1
-  float *sVec = reinterpret_cast<float *>(smem + L::kVec);  // stage s: lse2 at 256s, D at 256s+128
+  float *sVec = reinterpret_cast<float *>(smem + L::kVec);  // stage s: -lse2 at 256s, -D at 256s+128
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -517,8 +527,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // copies entries 0..127 instead, so the barrier still gets its bytes)
         size_t vec = (static_cast<size_t>(b) * p.H + hq) * p.Npad + i * 128;
         if (!in_bounds(vec, 128, static_cast<size_t>(p.B) * p.H * p.Npad, p.status)) vec = 0;
-        bulk_load(sVec + 256 * s, p.lse2 + vec, 512, &qd_full[s]);
-        bulk_load(sVec + 256 * s + 128, p.dsum + vec, 512, &qd_full[s]);
+        bulk_load(sVec + 256 * s, p.nlse2 + vec, 512, &qd_full[s]);
+        bulk_load(sVec + 256 * s + 128, p.ndsum + vec, 512, &qd_full[s]);
         issued = it + 1;
       }
       mbar_drain(in_full, 0, p.status);
@@ -576,6 +586,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tS = tmem + lane_off, tP = tmem + 128 + lane_off;
     const uint32_t tV = tmem + 256 + lane_off, tK = tmem + 256 + D + lane_off;
     const float sl2 = p.scale_log2;
+    const float2 sl2x2 = make_float2(sl2, sl2);
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int s = it % ST;
@@ -587,27 +598,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const float *vl = sVec + 256 * s;  // log-sum-exp (log2 units) of the 128 queries
-      const float *vd = vl + 128;        // D of the 128 queries
+      const float *vl = sVec + 256 * s;  // -log-sum-exp (log2 units) of the 128 queries
+      const float *vd = vl + 128;        // -D of the 128 queries
       // queries [qfirst, 128) of this tile see the key (causal); earlier
-      // ones do not.  Queries past N carry lse2 = +inf, so their weight is 0.
+      // ones do not.  Queries past N carry -lse2 = -inf, so their weight is 0.
       const int qfirst = CAUSAL ? max(0, kj - i * 128) : 0;
       // P^T = exp(S^T * scale - lse[q]) of this half's 64 queries as bf16
-      // pairs, stored over S^T
+      // pairs, stored over S^T (packed pairs; the mask is applied only in
+      // chunks that start before qfirst)
       uint32_t pp[32];
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int c = 2 * hf + cc;
         uint32_t sv[32];
         tmem_ld32_wait(tS + c * 32, sv);
+        const bool part = c * 32 < qfirst;
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           const int q0 = c * 32 + e;
           const float4 l4 = *reinterpret_cast<const float4 *>(vl + q0);
-          const float w0 = (q0 >= qfirst) ? ex2(fmaf(__uint_as_float(sv[e]), sl2, -l4.x)) : 0.f;
-          const float w1 = (q0 + 1 >= qfirst) ? ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -l4.y)) : 0.f;
-          const float w2 = (q0 + 2 >= qfirst) ? ex2(fmaf(__uint_as_float(sv[e + 2]), sl2, -l4.z)) : 0.f;
-          const float w3 = (q0 + 3 >= qfirst) ? ex2(fmaf(__uint_as_float(sv[e + 3]), sl2, -l4.w)) : 0.f;
+          const float2 x0 = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                  sl2x2, make_float2(l4.x, l4.y));
+          const float2 x1 = ffma2(make_float2(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])),
+                                  sl2x2, make_float2(l4.z, l4.w));
+          float w0 = ex2(x0.x), w1 = ex2(x0.y), w2 = ex2(x1.x), w3 = ex2(x1.y);
+          if (part) {
+            w0 = (q0 >= qfirst) ? w0 : 0.f;
+            w1 = (q0 + 1 >= qfirst) ? w1 : 0.f;
+            w2 = (q0 + 2 >= qfirst) ? w2 : 0.f;
+            w3 = (q0 + 3 >= qfirst) ? w3 : 0.f;
+          }
           pp[cc * 16 + (e >> 1)] = pack_bf16x2(w0, w1);
           pp[cc * 16 + (e >> 1) + 1] = pack_bf16x2(w2, w3);
         }
@@ -635,10 +655,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const float4 d4 = *reinterpret_cast<const float4 *>(vd + q0);
           const float2 wa = bf16x2_to_float2(pp[cc * 16 + (e >> 1)]);
           const float2 wb = bf16x2_to_float2(pp[cc * 16 + (e >> 1) + 1]);
-          pd[e >> 1] = pack_bf16x2(wa.x * (__uint_as_float(dp[e]) - d4.x),
-                                   wa.y * (__uint_as_float(dp[e + 1]) - d4.y));
-          pd[(e >> 1) + 1] = pack_bf16x2(wb.x * (__uint_as_float(dp[e + 2]) - d4.z),
-                                         wb.y * (__uint_as_float(dp[e + 3]) - d4.w));
+          const float2 ra = fmul2(
+              wa, fadd2(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
+                        make_float2(d4.x, d4.y)));
+          const float2 rb = fmul2(
+              wb, fadd2(make_float2(__uint_as_float(dp[e + 2]), __uint_as_float(dp[e + 3])),
+                        make_float2(d4.z, d4.w)));
+          pd[e >> 1] = pack_bf16x2(ra.x, ra.y);
+          pd[(e >> 1) + 1] = pack_bf16x2(rb.x, rb.y);
         }
         tmem_st16(tP + hf * 64 + cc * 16, pd);
       }

@@ -533,8 +533,8 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *out, const f
   p.lse = lse;
   p.n_tiles = static_cast<int>(n_tiles);
   p.Npad = p.n_tiles * 128;
-  p.lse2 = static_cast<float *>(workspace);
-  p.dsum = p.lse2 + static_cast<size_t>(B) * H * p.Npad;
+  p.nlse2 = static_cast<float *>(workspace);
+  p.ndsum = p.nlse2 + static_cast<size_t>(B) * H * p.Npad;
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;

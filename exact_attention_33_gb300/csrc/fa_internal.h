@@ -116,8 +116,8 @@ struct BwdParams {
   const void *out;        // forward output O, bf16 [B, N, H, d]
   const void *dout;       // upstream gradient dO, bf16 [B, N, H, d]
   const float *lse;       // forward log-sum-exp, fp32 [B, H, N] (natural log)
-  float *lse2;            // workspace: lse in log2 units, [B, H, Npad]
-  float *dsum;            // workspace: D = rowsum(dO * O), [B, H, Npad]
+  float *nlse2;           // workspace: -lse in log2 units, [B, H, Npad]
+  float *ndsum;           // workspace: -D = -rowsum(dO * O), [B, H, Npad]
   void *dq, *dk, *dv;     // bf16, layouts of q, k, v
   int B, H, Hkv, group, N;
   int Npad;               // N rounded up to 128
