@@ -28,7 +28,7 @@ __all__ = [
     "fa_status_string", "fa_device_status", "fa_last_device_status", "new_workspace",
     "FA_WORKSPACE_HEADER_BYTES",
     "fa_version", "FA_DEV_TIMEOUT", "FA_DEV_BAD_BLOCK", "FA_DEV_BAD_CTX", "FA_DEV_BAD_SEQLEN",
-    "FA_DEV_BAD_INDEX",
+    "FA_DEV_BAD_INDEX", "FA_DEV_SMEM_ALIGN",
 ]
 
 FA_OK = 0
@@ -37,6 +37,7 @@ FA_DEV_BAD_BLOCK = 2
 FA_DEV_BAD_CTX = 4
 FA_DEV_BAD_SEQLEN = 8
 FA_DEV_BAD_INDEX = 16   # checked build only
+FA_DEV_SMEM_ALIGN = 32  # a kernel found its shared memory not 1 KiB aligned
 FA_WORKSPACE_HEADER_BYTES = 256   # control block at the start of a decode / split-KV workspace
 
 _PKG = os.path.dirname(os.path.abspath(__file__))

@@ -43,18 +43,30 @@ struct BwdLayout {
   static constexpr int kChunkBytes = 128 * 128;  // 128 rows x one 128-byte swizzle row
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
-  static constexpr int kStages = 2;
-  // dK/dV kernel: K, V, then a ring of (Q, dO) tile pairs plus the
-  // per-stage log-sum-exp and D vectors (128 floats each).
+  // dK/dV kernel: K, V, then a ring of Q tiles (with their log-sum-exp
+  // vectors) and a ring of dO tiles (with their D vectors), 128 floats per
+  // vector.  Both are released once dK is done (dO's vector is read by the
+  // elementwise warps until then); Q gets the deeper ring, because S^T of
+  // the next query tile needs it right after dV, a product earlier than
+  // dP^T needs dO.
+  static constexpr int kStagesQ = 3;
+  static constexpr int kStagesO = 2;
   static constexpr int kA = 0;                          // K
   static constexpr int kB = kA + kTileBytes;            // V
-  static constexpr int kR0 = kB + kTileBytes;           // ring of tile pairs
-  static constexpr int kVec = kR0 + 2 * kStages * kTileBytes;
-  static constexpr int kBar = kVec + kStages * 2 * 512;
-  static constexpr int kNumBars = 2 + 2 * kStages + 8;
+  static constexpr int kQ = kB + kTileBytes;            // Q ring
+  static constexpr int kDO = kQ + kStagesQ * kTileBytes;  // dO ring
+  static constexpr int kVecQ = kDO + kStagesO * kTileBytes;  // -lse2 per Q stage
+  static constexpr int kVecO = kVecQ + kStagesQ * 512;       // -D per dO stage
+  static constexpr int kBar = kVecO + kStagesO * 512;
+  static constexpr int kNumBars = 1 + 2 * kStagesQ + 2 * kStagesO + 6;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
-  static constexpr int kSmemAlloc = kBytes + 1024;
+  // Room to align the base up to 1 KiB, as much as the 227 KiB limit leaves
+  // at d = 128 (the dynamic shared memory of a kernel without static
+  // shared memory starts 1 KiB aligned; the kernel checks).
+  static constexpr int kSlack = (kBytes + 1024 <= 232448) ? 1024 : 232448 - kBytes;
+  static constexpr int kSmemAlloc = kBytes + kSlack;
+  static_assert(kSlack >= 0, "dK/dV shared memory exceeds 227 KiB");
 };
 
 // Shared memory of the dQ kernel: Q and dO of the query tile, then separate
@@ -437,7 +449,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const BwdParams p) {
   using L = BwdLayout<D>;
-  constexpr int ST = L::kStages;
+  constexpr int SQ = L::kStagesQ;
+  constexpr int SO = L::kStagesO;
   // heaviest key tiles first (causal: tile 0 sees every query tile)
   const int kvh = static_cast<int>(blockIdx.x % p.Hkv);
   const int rest = static_cast<int>(blockIdx.x / p.Hkv);
@@ -449,11 +462,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  if (smem - smem_raw > L::kSlack) {
+    // the layout does not fit: report it, touch nothing (the whole CTA leaves)
+    if (threadIdx.x == 0) raise_status(p.status, FA_DEV_SMEM_ALIGN);
+    return;
+  }
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBar);
   uint64_t *in_full = bars;          // K and V of this key tile
-  uint64_t *qd_full = bars + 1;      // [ST] Q, dO, lse2, D
-  uint64_t *qd_empty = qd_full + ST;
-  uint64_t *s_full = qd_empty + ST;
+  uint64_t *q_full = bars + 1;       // [SQ] Q and its -lse2 vector
+  uint64_t *q_empty = q_full + SQ;
+  uint64_t *o_full = q_empty + SQ;   // [SO] dO and its -D vector
+  uint64_t *o_empty = o_full + SO;
+  uint64_t *s_full = o_empty + SO;
   uint64_t *dp_full = s_full + 1;
   uint64_t *pt_full = dp_full + 1;  // P^T (bf16) is in TMEM
   uint64_t *p_full = pt_full + 1;   // dS^T (bf16) is in TMEM
@@ -463,16 +483,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
   uint8_t *sK = smem + L::kA;
   uint8_t *sV = smem + L::kB;
-  uint8_t *sR = smem + L::kR0;  // stage s: Q at 2s, dO at 2s + 1
-  float *sVec = reinterpret_cast<float *>(smem + L::kVec);  // stage s: -lse2 at 256s, -D at 256s+128
+  uint8_t *sQr = smem + L::kQ;    // Q ring
+  uint8_t *sOr = smem + L::kDO;   // dO ring
+  float *sVq = reinterpret_cast<float *>(smem + L::kVecQ);  // Q stage s: -lse2 at 128 s
+  float *sVo = reinterpret_cast<float *>(smem + L::kVecO);  // dO stage s: -D at 128 s
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   if (warp == 9 && lane == 0) {
     mbar_init(in_full, 1);
-    for (int s = 0; s < ST; ++s) {
-      mbar_init(&qd_full[s], 1);
-      mbar_init(&qd_empty[s], 1);
+    for (int s = 0; s < SQ; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
+    for (int s = 0; s < SO; ++s) {
+      mbar_init(&o_full[s], 1);
+      mbar_init(&o_empty[s], 1);
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
@@ -508,32 +534,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_4d(sK + c * L::kChunkBytes, &tm_k, in_full, c * 64, kvh, jt * 128, b);
         tma_load_4d(sV + c * L::kChunkBytes, &tm_v, in_full, c * 64, kvh, jt * 128, b);
       }
-      int issued = 0;
+      // Q(it) then dO(it) for every it; each waits for its own ring
+      int q_issued = 0, o_issued = 0;
       for (int it = 0; it < n_it; ++it) {
-        const int s = it % ST;
-        if (it >= ST && !mbar_wait(&qd_empty[s], ((it / ST) - 1) & 1, abort_flag, p.status))
-          break;
         const int hq = kvh * p.group + it % p.group;
         const int i = i0 + it / p.group;
-        mbar_arrive_expect_tx(&qd_full[s], 2 * L::kTileBytes + 2 * 512);
-        uint8_t *sq = sR + (2 * s) * L::kTileBytes;
-        uint8_t *sd = sq + L::kTileBytes;
-#pragma unroll
-        for (int c = 0; c < L::kChunks; ++c) {
-          tma_load_4d(sq + c * L::kChunkBytes, &tm_q, &qd_full[s], c * 64, hq, i * 128, b);
-          tma_load_4d(sd + c * L::kChunkBytes, &tm_do, &qd_full[s], c * 64, hq, i * 128, b);
-        }
         // (a checked build that finds the 128 entries outside the workspace
         // copies entries 0..127 instead, so the barrier still gets its bytes)
         size_t vec = (static_cast<size_t>(b) * p.H + hq) * p.Npad + i * 128;
         if (!in_bounds(vec, 128, static_cast<size_t>(p.B) * p.H * p.Npad, p.status)) vec = 0;
-        bulk_load(sVec + 256 * s, p.nlse2 + vec, 512, &qd_full[s]);
-        bulk_load(sVec + 256 * s + 128, p.ndsum + vec, 512, &qd_full[s]);
-        issued = it + 1;
+        const int sq = it % SQ, so = it % SO;
+        if (it >= SQ && !mbar_wait(&q_empty[sq], ((it / SQ) - 1) & 1, abort_flag, p.status))
+          break;
+        mbar_arrive_expect_tx(&q_full[sq], L::kTileBytes + 512);
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_4d(sQr + sq * L::kTileBytes + c * L::kChunkBytes, &tm_q, &q_full[sq], c * 64, hq,
+                      i * 128, b);
+        bulk_load(sVq + 128 * sq, p.nlse2 + vec, 512, &q_full[sq]);
+        q_issued = it + 1;
+        if (it >= SO && !mbar_wait(&o_empty[so], ((it / SO) - 1) & 1, abort_flag, p.status))
+          break;
+        mbar_arrive_expect_tx(&o_full[so], L::kTileBytes + 512);
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_4d(sOr + so * L::kTileBytes + c * L::kChunkBytes, &tm_do, &o_full[so], c * 64,
+                      hq, i * 128, b);
+        bulk_load(sVo + 128 * so, p.ndsum + vec, 512, &o_full[so]);
+        o_issued = it + 1;
       }
       mbar_drain(in_full, 0, p.status);
-      for (int it = max(0, issued - ST); it < issued; ++it)
-        mbar_drain(&qd_full[it % ST], (it / ST) & 1, p.status);
+      for (int it = max(0, q_issued - SQ); it < q_issued; ++it)
+        mbar_drain(&q_full[it % SQ], (it / SQ) & 1, p.status);
+      for (int it = max(0, o_issued - SO); it < o_issued; ++it)
+        mbar_drain(&o_full[it % SO], (it / SO) & 1, p.status);
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
@@ -543,23 +577,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // overwrites P^T only after dV has read it); dK += dS^T Q once dS^T
     // (over dP^T) is in TMEM; then dP^T of the next iteration.
     const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV);
-    auto q_at = [&](int it) { return smem_u32(sR + (2 * (it % ST)) * L::kTileBytes); };
+    auto q_at = [&](int it) { return smem_u32(sQr + (it % SQ) * L::kTileBytes); };
+    auto do_at = [&](int it) { return smem_u32(sOr + (it % SO) * L::kTileBytes); };
     bool ok = mbar_wait_warp(in_full, 0, abort_flag, p.status) &&
-              mbar_wait_warp(&qd_full[0], 0, abort_flag, p.status);
+              mbar_wait_warp(&q_full[0], 0, abort_flag, p.status) &&
+              mbar_wait_warp(&o_full[0], 0, abort_flag, p.status);
     if (ok) {
       tc_fence_after();
       mma_tile_ss<D>(tmem, k_base, q_at(0));
       mma_commit_elect(s_full);
-      mma_tile_ss<D>(tmem + 128, v_base, q_at(0) + L::kTileBytes);
+      mma_tile_ss<D>(tmem + 128, v_base, do_at(0));
       mma_commit_elect(dp_full);
     }
     for (int it = 0; ok && it < n_it; ++it) {
-      const uint32_t q_base = q_at(it);
       if (!mbar_wait_warp(pt_full, it & 1, abort_flag, p.status)) break;
       tc_fence_after();
-      mma_tile_ts<D>(tmem + 256, tmem, q_base + L::kTileBytes, it > 0);
+      mma_tile_ts<D>(tmem + 256, tmem, do_at(it), it > 0);
       if (it + 1 < n_it) {
-        if (!mbar_wait_warp(&qd_full[(it + 1) % ST], ((it + 1) / ST) & 1, abort_flag, p.status))
+        if (!mbar_wait_warp(&q_full[(it + 1) % SQ], ((it + 1) / SQ) & 1, abort_flag, p.status))
           break;
         tc_fence_after();
         mma_tile_ss<D>(tmem, k_base, q_at(it + 1));
@@ -567,10 +602,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (!mbar_wait_warp(p_full, it & 1, abort_flag, p.status)) break;
       tc_fence_after();
-      mma_tile_ts<D>(tmem + 256 + D, tmem + 128, q_base, it > 0);
-      mma_commit_elect(&qd_empty[it % ST]);
+      mma_tile_ts<D>(tmem + 256 + D, tmem + 128, q_at(it), it > 0);
+      // Q(it) was last read by dK(it); the dO stage is released here too,
+      // because the elementwise warps read its -D vector until dS^T(it) is
+      // handed over (which dK(it) waited for)
+      mma_commit_elect(&q_empty[it % SQ]);
+      mma_commit_elect(&o_empty[it % SO]);
       if (it + 1 < n_it) {
-        mma_tile_ss<D>(tmem + 128, v_base, q_at(it + 1) + L::kTileBytes);
+        if (!mbar_wait_warp(&o_full[(it + 1) % SO], ((it + 1) / SO) & 1, abort_flag, p.status))
+          break;
+        tc_fence_after();
+        mma_tile_ss<D>(tmem + 128, v_base, do_at(it + 1));
         mma_commit_elect(dp_full);
       }
     }
@@ -589,17 +631,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float2 sl2x2 = make_float2(sl2, sl2);
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
-      const int s = it % ST;
       const int i = i0 + it / p.group;
-      // the stage's vectors arrived with its tiles (async copies): observe
-      // that barrier too before reading them
-      ok = mbar_wait(&qd_full[s], (it / ST) & 1, abort_flag, p.status) &&
+      // the stages' vectors arrived with their tiles (async copies): observe
+      // those barriers too before reading them
+      ok = mbar_wait(&q_full[it % SQ], (it / SQ) & 1, abort_flag, p.status) &&
            mbar_wait(s_full, it & 1, abort_flag, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const float *vl = sVec + 256 * s;  // -log-sum-exp (log2 units) of the 128 queries
-      const float *vd = vl + 128;        // -D of the 128 queries
+      const float *vl = sVq + 128 * (it % SQ);  // -log-sum-exp (log2 units) of the 128 queries
+      const float *vd = sVo + 128 * (it % SO);  // -D of the 128 queries (read after o_full)
       // queries [qfirst, 128) of this tile see the key (causal); earlier
       // ones do not.  Queries past N carry -lse2 = -inf, so their weight is 0.
       const int qfirst = CAUSAL ? max(0, kj - i * 128) : 0;
@@ -639,7 +680,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(pt_full);
-      ok = mbar_wait(dp_full, it & 1, abort_flag, p.status);
+      ok = mbar_wait(&o_full[it % SO], (it / SO) & 1, abort_flag, p.status) &&
+           mbar_wait(dp_full, it & 1, abort_flag, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();

@@ -82,6 +82,7 @@ typedef enum {
 #define FA_DEV_BAD_CTX 4u     /* ctx_len < 0 or > max_blocks_per_seq * block_size    */
 #define FA_DEV_BAD_SEQLEN 8u  /* cu_seqlens not non-decreasing / beyond total_tokens */
 #define FA_DEV_BAD_INDEX 16u /* checked build only: a kernel index outside its buffer  */
+#define FA_DEV_SMEM_ALIGN 32u /* a kernel found its shared memory not 1 KiB aligned    */
 
 /*
  * Dense prefill forward (causal or not).
