@@ -203,7 +203,7 @@ def test_status_bits_match_the_binding():
     bits = dict((name, int(val)) for name, val in
                 re.findall(r"#define\s+(FA_DEV_[A-Z_]+)\s+(\d+)u", text))
     assert set(bits) == {"FA_DEV_TIMEOUT", "FA_DEV_BAD_BLOCK", "FA_DEV_BAD_CTX",
-                         "FA_DEV_BAD_SEQLEN", "FA_DEV_BAD_INDEX"}
+                         "FA_DEV_BAD_SEQLEN", "FA_DEV_BAD_INDEX", "FA_DEV_SMEM_ALIGN"}
     for name, val in bits.items():
         assert getattr(fa, name) == val, name
     assert len(set(bits.values())) == len(bits)
