@@ -306,28 +306,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
-    // S lives in TMEM [0,128), dP in [128,256), dQ in [256, 256 + d).  Per
-    // key tile j: dP_j; then S_{j+1} as soon as the elementwise warps have
-    // read S_j (s_read), so it runs while they finish tile j; then
-    // dQ += dS_j K_j once dS_j (bf16, written over dP_j) is in TMEM.  dP_{j+1}
-    // is issued after dQ_j by this thread, so it overwrites dS_j only after
-    // dQ_j has read it.
+    // S lives in TMEM [0,128), dQ in [256, 256 + d), and dP in two buffers,
+    // [128,256) for even key tiles and [384,512) for odd ones.  Per key tile
+    // j: S_{j+1} as soon as the elementwise warps have read S_j (s_read),
+    // then dP_{j+1} into the other buffer, so both run while they finish
+    // tile j; then dQ += dS_j K_j once dS_j (bf16, written over dP_j) is in
+    // TMEM.  dP_{j+2} takes dS_j's buffer only after dQ_j, issued before it
+    // by this thread, has read it.
     const uint32_t q_base = smem_u32(sQ), do_base = smem_u32(sDO);
     const uint32_t k_ring = smem_u32(sK), v_ring = smem_u32(sV);
+    auto issue_dp = [&](int j) -> bool {
+      const int sv = j % SV;
+      if (!mbar_wait_warp(&v_full[sv], (j / SV) & 1, abort_flag, p.status)) return false;
+      tc_fence_after();
+      mma_tile_ss<D>(tmem + ((j & 1) ? 384 : 128), do_base, v_ring + sv * L::kTileBytes);
+      mma_commit_elect(dp_full);
+      mma_commit_elect(&v_empty[sv]);
+      return true;
+    };
     bool ok = mbar_wait_warp(in_full, 0, abort_flag, p.status) &&
               mbar_wait_warp(&k_full[0], 0, abort_flag, p.status);
     if (ok) {
       tc_fence_after();
       mma_tile_ss<D>(tmem, q_base, k_ring);
       mma_commit_elect(s_full);
+      ok = issue_dp(0);
     }
     for (int j = 0; ok && j < n_kv; ++j) {
-      const int sk = j % SK, sv = j % SV;
-      if (!mbar_wait_warp(&v_full[sv], (j / SV) & 1, abort_flag, p.status)) break;
-      tc_fence_after();
-      mma_tile_ss<D>(tmem + 128, do_base, v_ring + sv * L::kTileBytes);
-      mma_commit_elect(dp_full);
-      mma_commit_elect(&v_empty[sv]);
+      const int sk = j % SK;
       if (j + 1 < n_kv) {
         const int sk1 = (j + 1) % SK;
         ok = mbar_wait_warp(s_read, j & 1, abort_flag, p.status) &&
@@ -336,10 +342,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         mma_tile_ss<D>(tmem, q_base, k_ring + sk1 * L::kTileBytes);
         mma_commit_elect(s_full);
+        if (!issue_dp(j + 1)) break;
       }
       if (!mbar_wait_warp(p_full, j & 1, abort_flag, p.status)) break;
       tc_fence_after();
-      mma_tile_ts<D>(tmem + 256, tmem + 128, k_ring + sk * L::kTileBytes, j > 0);
+      mma_tile_ts<D>(tmem + 256, tmem + ((j & 1) ? 384 : 128), k_ring + sk * L::kTileBytes, j > 0);
       mma_commit_elect(&k_empty[sk]);
     }
     mma_commit_elect(dq_done);
@@ -351,7 +358,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int row = quad * 32 + lane;
     const int qi = t * 128 + row;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t tS = tmem + lane_off, tP = tmem + 128 + lane_off, tQ = tmem + 256 + lane_off;
+    const uint32_t tS = tmem + lane_off, tQ = tmem + 256 + lane_off;
     const size_t vec = (static_cast<size_t>(b) * p.H + h) * p.Npad + min(qi, p.Npad - 1);
     const size_t n_vec = static_cast<size_t>(p.B) * p.H * p.Npad;
     const float nlse2 = checked_load(p.nlse2, vec, n_vec, p.status);  // -lse (log2 units)
@@ -395,7 +402,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      // dS = P (dP - D), written over this half's dP columns
+      // dS = P (dP - D), written over this half's dP columns (dP_j in the
+      // buffer of key tile j's parity)
+      const uint32_t tP = tmem + ((j & 1) ? 384 : 128) + lane_off;
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int c = 2 * hf + cc;
