@@ -725,6 +725,10 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
       uint32_t sr[128];
       tmem_ld128_wait(tS, sr);
       const int nvis = limit - (kv0 + j) * kPrefillBN;
+      // keys past the last one any row of this warp sees (the causal
+      // diagonal): at d = 64, where the softmax bounds the key loop, their
+      // 64-key halves of P are zero without exponentials
+      const int nvis_w = (D == 64) ? __reduce_max_sync(0xffffffffu, nvis) : kPrefillBN;
       if (__any_sync(0xffffffffu, nvis < kPrefillBN)) {
 #pragma unroll
         for (int c = 0; c < 128; ++c)
@@ -765,6 +769,12 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t pk[32];
+          if (D == 64 && half * 64 >= nvis_w) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) pk[c] = 0u;
+            tmem_st32(tS + half * 32, pk);
+            continue;
+          }
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
             const int e = half * 64 + 2 * c;
