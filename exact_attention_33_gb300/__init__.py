@@ -23,7 +23,7 @@ import threading
 __all__ = [
     "FaError", "library_path", "load_library", "fa_fwd", "fa_fwd_varlen", "fa_fwd_paged",
     "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_fwd_fp8", "fa_fwd_varlen_fp8",
-    "fa_bwd", "fa_bwd_workspace_size",
+    "fa_bwd", "fa_bwd_varlen", "fa_bwd_workspace_size",
     "fa_decode_paged", "fa_decode_paged_noalloc", "fa_decode_workspace_size",
     "fa_status_string", "fa_device_status", "fa_last_device_status", "new_workspace",
     "FA_WORKSPACE_HEADER_BYTES",
@@ -85,6 +85,9 @@ def load_library() -> ctypes.CDLL:
         lib.fa_bwd_workspace_size.restype = sz
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
         lib.fa_bwd.restype = i
+        lib.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f,
+                                      i, vp, sz, vp]
+        lib.fa_bwd_varlen.restype = i
         lib.fa_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i]
         lib.fa_fwd_splitkv_workspace_size.restype = sz
         lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]
@@ -309,6 +312,46 @@ def fa_bwd(q, k, v, out, lse, dout, causal=False, scale=None, dq=None, dk=None, 
                                    workspace.numel(), _stream_handle(stream, dev))
     if rc != FA_OK:
         raise FaError("fa_bwd", rc)
+    return dq, dk, dv
+
+
+def fa_bwd_varlen(q, k, v, out, lse, dout, cu_seqlens, max_seqlen, causal=False, scale=None,
+                  dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Gradient of a packed varlen batch.  q, out, dout [T,H,d]; k, v [T,Hkv,d]
+    bf16 CUDA tensors; lse [H,T] fp32 from fa_fwd_varlen; cu_seqlens int32
+    [S+1] on the device.  Returns (dq, dk, dv); rows outside every sequence
+    are left as they were."""
+    torch = _torch()
+    _check_bf16_cuda("q", q, 3)
+    dev = q.device
+    for name, t in (("k", k), ("v", v), ("out", out), ("dout", dout)):
+        _check_bf16_cuda(name, t, 3, dev)
+    _check_int32("cu_seqlens", cu_seqlens, dev)
+    if cu_seqlens.numel() < 1:
+        raise ValueError("cu_seqlens must hold num_seqs + 1 offsets")
+    T, H, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (T, Hkv, d) or v.shape != k.shape or out.shape != q.shape \
+            or dout.shape != q.shape:
+        raise ValueError("shapes must be q/out/dout [T,H,d], k/v [T,Hkv,d]")
+    _check_tensor("lse", lse, (H, T), torch.float32, dev)
+    grads = []
+    for name, g, like in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        if g is None:
+            g = torch.empty_like(like)
+        else:
+            _check_tensor(name, g, like.shape, torch.bfloat16, dev)
+        grads.append(g)
+    dq, dk, dv = grads
+    S = cu_seqlens.numel() - 1
+    workspace = _workspace(workspace, fa_bwd_workspace_size(S, H, min(int(max_seqlen), T)), dev)
+    with torch.cuda.device(dev):
+        rc = load_library().fa_bwd_varlen(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+            _ptr(dv), _ptr(cu_seqlens), S, T, int(max_seqlen), H, Hkv, d, _scale(scale, d),
+            1 if causal else 0, _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
+    if rc != FA_OK:
+        raise FaError("fa_bwd_varlen", rc)
     return dq, dk, dv
 
 

@@ -141,6 +141,30 @@ __device__ __forceinline__ void store_row_scaled_bf16(void *dst_row, const uint3
   }
 }
 
+// First row and length of sequence b: in a packed batch from cu_seqlens
+// (a sequence with invalid bounds, or longer than N, is reported and gets
+// length 0, so nothing of it is computed or written); in a dense batch the
+// rows of batch element b (row coordinates are then per element).
+template <bool VARLEN>
+__device__ __forceinline__ void bwd_seq(const BwdParams &p, int b, int &start, int &len,
+                                        bool report) {
+  if constexpr (VARLEN) {
+    const int a = checked_load(p.cu_seqlens, b, p.B + 1, p.status);
+    const int e = checked_load(p.cu_seqlens, b + 1, p.B + 1, p.status);
+    if (a < 0 || e < a || e > p.total_tokens || e - a > p.N) {
+      if (report) raise_status(p.status, FA_DEV_BAD_SEQLEN);
+      start = 0;
+      len = 0;
+      return;
+    }
+    start = a;
+    len = e - a;
+  } else {
+    start = 0;
+    len = p.N;
+  }
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ preprocess
@@ -148,7 +172,7 @@ __device__ __forceinline__ void store_row_scaled_bf16(void *dst_row, const uint3
 // bf16) and the forward log-sum-exp in log2 units, both stored negated (the
 // consumers add them); -lse is -inf for rows past N or rows without a visible
 // key, so that every weight recomputed from it is 0.
-template <int D>
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) {
   constexpr int TPR = D / 8;  // threads per row
   const int sub = threadIdx.x % TPR;
@@ -164,11 +188,18 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
   const int b = static_cast<int>(bh / p.H);
   const size_t vec = static_cast<size_t>(gr);  // (b * H + h) * Npad + row
   // elements of O / dO, and of the workspace vectors, the call owns
-  const size_t n_rows = static_cast<size_t>(p.B) * p.N * p.H;
+  const size_t n_rows =
+      VARLEN ? static_cast<size_t>(p.total_tokens) * p.H : static_cast<size_t>(p.B) * p.N * p.H;
   const size_t n_vec = static_cast<size_t>(p.B) * p.H * p.Npad;
+  int start, len;
+  bwd_seq<VARLEN>(p, b, start, len, row == 0 && h == 0 && sub == 0);
+  // the row's place in O / dO and in the log-sum-exp
+  const size_t grow = VARLEN ? static_cast<size_t>(start) + row : static_cast<size_t>(b) * p.N + row;
+  const size_t lidx = VARLEN ? static_cast<size_t>(h) * p.total_tokens + start + row
+                             : (static_cast<size_t>(b) * p.H + h) * p.N + row;
   float acc = 0.f;
-  const size_t off = ((static_cast<size_t>(b) * p.N + row) * p.H + h) * D + sub * 8;
-  if (row < p.N && in_bounds(off, 8, n_rows * D, p.status)) {
+  const size_t off = (grow * p.H + h) * D + sub * 8;
+  if (row < len && in_bounds(off, 8, n_rows * D, p.status)) {
     const uint4 o = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.out) + off);
     const uint4 g = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.dout) + off);
     const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
@@ -183,9 +214,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
 #pragma unroll
   for (int sft = TPR / 2; sft > 0; sft >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sft);
   if (sub == 0 && in_bounds(vec, 1, n_vec, p.status)) {
-    if (row < p.N) {
-      const float l = checked_load(p.lse, (static_cast<size_t>(b) * p.H + h) * p.N + row,
-                                   n_rows, p.status);
+    if (row < len) {
+      const float l = checked_load(p.lse, lidx, n_rows, p.status);
       p.nlse2[vec] = (l == -CUDART_INF_F) ? -CUDART_INF_F : -(l * kLog2eF);
       p.ndsum[vec] = -acc;
     } else {
@@ -196,7 +226,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
 }
 
 // ------------------------------------------------------------------------- dQ
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -211,7 +241,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int b = rest / p.n_tiles;
   const int t = CAUSAL ? (p.n_tiles - 1 - t_rank) : t_rank;
   const int kvh = h / p.group;
-  const int n_kv = CAUSAL ? (t + 1) : p.n_tiles;
+  // the sequence's rows: a packed batch's tiles past its end leave at once
+  int start, len;
+  bwd_seq<VARLEN>(p, b, start, len, t_rank == 0 && h == 0 && threadIdx.x == 0);
+  const int n_tiles = VARLEN ? (len + 127) / 128 : p.n_tiles;
+  if (t >= n_tiles) return;
+  const int row0 = VARLEN ? start : 0;  // first row of the sequence in the tensor maps
+  const int bc = VARLEN ? 0 : b;        // the maps' outer coordinate
+  const int n_kv = CAUSAL ? (t + 1) : n_tiles;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -276,8 +313,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive_expect_tx(in_full, 2 * L::kTileBytes);
 #pragma unroll
       for (int c = 0; c < L::kChunks; ++c) {
-        tma_load_4d(sQ + c * L::kChunkBytes, &tm_q, in_full, c * 64, h, t * 128, b);
-        tma_load_4d(sDO + c * L::kChunkBytes, &tm_do, in_full, c * 64, h, t * 128, b);
+        tma_load_4d(sQ + c * L::kChunkBytes, &tm_q, in_full, c * 64, h, row0 + t * 128, bc);
+        tma_load_4d(sDO + c * L::kChunkBytes, &tm_do, in_full, c * 64, h, row0 + t * 128, bc);
       }
       // K(j) then V(j) for every j; each waits for its own ring
       int k_issued = 0, v_issued = 0;
@@ -288,14 +325,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c)
           tma_load_4d(sK + sk * L::kTileBytes + c * L::kChunkBytes, &tm_k, &k_full[sk], c * 64,
-                      kvh, j * 128, b);
+                      kvh, row0 + j * 128, bc);
         k_issued = j + 1;
         if (j >= SV && !mbar_wait(&v_empty[sv], ((j / SV) - 1) & 1, abort_flag, p.status)) break;
         mbar_arrive_expect_tx(&v_full[sv], L::kTileBytes);
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c)
           tma_load_4d(sV + sv * L::kTileBytes + c * L::kChunkBytes, &tm_v, &v_full[sv], c * 64,
-                      kvh, j * 128, b);
+                      kvh, row0 + j * 128, bc);
         v_issued = j + 1;
       }
       mbar_drain(in_full, 0, p.status);
@@ -372,8 +409,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      // keys [0, nvis) of this tile are visible to the row
-      const int nvis = min(128, (CAUSAL ? min(p.N, qi + 1) : p.N) - j * 128);
+      // keys [0, nvis) of this tile are visible to the row (keys past the
+      // sequence, of the next sequence in a packed batch, are not)
+      const int nvis = min(128, (CAUSAL ? min(len, qi + 1) : len) - j * 128);
       // P = exp(S * scale - lse) of this half's 64 keys, kept as bf16 pairs
       // (the values the dQ product uses through dS)
       // (packed pairs; the mask is applied only in chunks that reach past nvis)
@@ -429,15 +467,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (ok) {
       tc_fence_after();
-      const size_t drow = ((static_cast<size_t>(b) * p.N + qi) * p.H + h) * D;
+      const size_t grow = VARLEN ? static_cast<size_t>(start) + qi : static_cast<size_t>(b) * p.N + qi;
+      const size_t drow = (grow * p.H + h) * D;
+      const size_t rows = VARLEN ? static_cast<size_t>(p.total_tokens) : static_cast<size_t>(p.B) * p.N;
       uint16_t *dst = static_cast<uint16_t *>(p.dq) + drow;
-      const bool row_ok =
-          qi >= p.N || in_bounds(drow, D, static_cast<size_t>(p.B) * p.N * p.H * D, p.status);
+      const bool row_ok = qi >= len || in_bounds(drow, D, rows * p.H * D, p.status);
 #pragma unroll
       for (int c = hf * (D / 64); c < (hf + 1) * (D / 64); ++c) {
         uint32_t o[32];
         tmem_ld32_wait(tQ + c * 32, o);
-        if (qi < p.N && row_ok) store_row_scaled_bf16(dst + c * 32, o, p.scale);
+        if (qi < len && row_ok) store_row_scaled_bf16(dst + c * 32, o, p.scale);
       }
     }
   }
@@ -451,7 +490,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ----------------------------------------------------------------------- dK dV
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_do,
@@ -465,8 +504,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int rest = static_cast<int>(blockIdx.x / p.Hkv);
   const int jt = rest % p.n_tiles;
   const int b = rest / p.n_tiles;
+  // the sequence's rows: a packed batch's key tiles past its end leave at once
+  int start, len;
+  bwd_seq<VARLEN>(p, b, start, len, jt == 0 && kvh == 0 && threadIdx.x == 0);
+  const int n_tiles = VARLEN ? (len + 127) / 128 : p.n_tiles;
+  if (jt >= n_tiles) return;
+  const int row0 = VARLEN ? start : 0;  // first row of the sequence in the tensor maps
+  const int bc = VARLEN ? 0 : b;        // the maps' outer coordinate
   const int i0 = CAUSAL ? jt : 0;  // first query tile that sees a key of this tile
-  const int n_it = (p.n_tiles - i0) * p.group;
+  const int n_it = (n_tiles - i0) * p.group;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -540,8 +586,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive_expect_tx(in_full, 2 * L::kTileBytes);
 #pragma unroll
       for (int c = 0; c < L::kChunks; ++c) {
-        tma_load_4d(sK + c * L::kChunkBytes, &tm_k, in_full, c * 64, kvh, jt * 128, b);
-        tma_load_4d(sV + c * L::kChunkBytes, &tm_v, in_full, c * 64, kvh, jt * 128, b);
+        tma_load_4d(sK + c * L::kChunkBytes, &tm_k, in_full, c * 64, kvh, row0 + jt * 128, bc);
+        tma_load_4d(sV + c * L::kChunkBytes, &tm_v, in_full, c * 64, kvh, row0 + jt * 128, bc);
       }
       // Q(it) then dO(it) for every it; each waits for its own ring
       int q_issued = 0, o_issued = 0;
@@ -559,7 +605,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c)
           tma_load_4d(sQr + sq * L::kTileBytes + c * L::kChunkBytes, &tm_q, &q_full[sq], c * 64, hq,
-                      i * 128, b);
+                      row0 + i * 128, bc);
         bulk_load(sVq + 128 * sq, p.nlse2 + vec, 512, &q_full[sq]);
         q_issued = it + 1;
         if (it >= SO && !mbar_wait(&o_empty[so], ((it / SO) - 1) & 1, abort_flag, p.status))
@@ -568,7 +614,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c)
           tma_load_4d(sOr + so * L::kTileBytes + c * L::kChunkBytes, &tm_do, &o_full[so], c * 64,
-                      hq, i * 128, b);
+                      hq, row0 + i * 128, bc);
         bulk_load(sVo + 128 * so, p.ndsum + vec, 512, &o_full[so]);
         o_issued = it + 1;
       }
@@ -727,22 +773,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (ok) {
       tc_fence_after();
-      const size_t orow = ((static_cast<size_t>(b) * p.N + kj) * p.Hkv + kvh) * D;
+      // key rows past the sequence (the next sequence's, in a packed batch)
+      // are not written
+      const size_t grow = VARLEN ? static_cast<size_t>(start) + kj : static_cast<size_t>(b) * p.N + kj;
+      const size_t orow = (grow * p.Hkv + kvh) * D;
+      const size_t rows = VARLEN ? static_cast<size_t>(p.total_tokens) : static_cast<size_t>(p.B) * p.N;
       uint16_t *dv = static_cast<uint16_t *>(p.dv) + orow;
       uint16_t *dk = static_cast<uint16_t *>(p.dk) + orow;
-      const bool row_ok =
-          kj >= p.N || in_bounds(orow, D, static_cast<size_t>(p.B) * p.N * p.Hkv * D, p.status);
+      const bool row_ok = kj >= len || in_bounds(orow, D, rows * p.Hkv * D, p.status);
 #pragma unroll
       for (int c = hf * (D / 64); c < (hf + 1) * (D / 64); ++c) {
         uint32_t o[32];
         tmem_ld32_wait(tV + c * 32, o);
-        if (kj < p.N && row_ok) store_row_scaled_bf16(dv + c * 32, o, 1.f);
+        if (kj < len && row_ok) store_row_scaled_bf16(dv + c * 32, o, 1.f);
       }
 #pragma unroll
       for (int c = hf * (D / 64); c < (hf + 1) * (D / 64); ++c) {
         uint32_t o[32];
         tmem_ld32_wait(tK + c * 32, o);
-        if (kj < p.N && row_ok) store_row_scaled_bf16(dk + c * 32, o, p.scale);
+        if (kj < len && row_ok) store_row_scaled_bf16(dk + c * 32, o, p.scale);
       }
     }
   }
@@ -757,19 +806,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 // ------------------------------------------------------------------- launch
 
-template <int D>
+template <int D, bool VARLEN>
 static cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tdo,
                                 const CUtensorMap &tk, const CUtensorMap &tv, const BwdParams &p,
                                 bool causal, cudaStream_t stream) {
   using L = BwdLayout<D>;
   const long long pre_rows = static_cast<long long>(p.B) * p.Npad * p.H;
   const long long rows_per_block = 256 / (D / 8);
-  bwd_preprocess_kernel<D><<<static_cast<unsigned>((pre_rows + rows_per_block - 1) / rows_per_block),
-                             256, 0, stream>>>(p);
+  bwd_preprocess_kernel<D, VARLEN>
+      <<<static_cast<unsigned>((pre_rows + rows_per_block - 1) / rows_per_block), 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  auto dq = causal ? bwd_dq_kernel<D, true> : bwd_dq_kernel<D, false>;
-  auto dkdv = causal ? bwd_dkdv_kernel<D, true> : bwd_dkdv_kernel<D, false>;
+  auto dq = causal ? bwd_dq_kernel<D, true, VARLEN> : bwd_dq_kernel<D, false, VARLEN>;
+  auto dkdv = causal ? bwd_dkdv_kernel<D, true, VARLEN> : bwd_dkdv_kernel<D, false, VARLEN>;
   e = cudaFuncSetAttribute(dq, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            BwdDqLayout<D>::kSmemAlloc);
   if (e != cudaSuccess) return e;
@@ -787,8 +836,11 @@ static cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tdo,
 cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUtensorMap &tk,
                        const CUtensorMap &tv, const BwdParams &p, int d, bool causal,
                        cudaStream_t stream) {
-  return d == 64 ? launch_bwd_d<64>(tq, tdo, tk, tv, p, causal, stream)
-                 : launch_bwd_d<128>(tq, tdo, tk, tv, p, causal, stream);
+  if (p.cu_seqlens != nullptr)
+    return d == 64 ? launch_bwd_d<64, true>(tq, tdo, tk, tv, p, causal, stream)
+                   : launch_bwd_d<128, true>(tq, tdo, tk, tv, p, causal, stream);
+  return d == 64 ? launch_bwd_d<64, false>(tq, tdo, tk, tv, p, causal, stream)
+                 : launch_bwd_d<128, false>(tq, tdo, tk, tv, p, causal, stream);
 }
 
 }  // namespace fa

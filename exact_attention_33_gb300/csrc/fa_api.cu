@@ -550,6 +550,67 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *out, const f
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *out, const float *lse,
+                  const void *dout, void *dq, void *dk, void *dv, const int32_t *cu_seqlens,
+                  int num_seqs, int total_tokens, int max_seqlen, int H, int Hkv, int d,
+                  float scale, int causal, void *workspace, size_t workspace_bytes,
+                  fa_stream_t stream) {
+  if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !cu_seqlens)
+    return FA_ERR_INVALID_ARG;
+  for (const void *ptr : {q, k, v, out, dout, static_cast<const void *>(dq),
+                          static_cast<const void *>(dk), static_cast<const void *>(dv)})
+    if (!aligned(ptr, 16)) return FA_ERR_INVALID_ARG;
+  if (!aligned(lse, 4) || !aligned(cu_seqlens, 4)) return FA_ERR_INVALID_ARG;
+  if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0) return FA_ERR_INVALID_ARG;
+  if (H < 1 || Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (num_seqs == 0 || total_tokens == 0 || max_seqlen == 0) return FA_OK;
+  const int n_max = std::min(max_seqlen, total_tokens);
+  const size_t need = fa_bwd_workspace_size(num_seqs, H, n_max);
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
+    return FA_ERR_WORKSPACE;
+  const long long n_tiles = (n_max + 127) / 128;
+  if (n_tiles * num_seqs * H > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(total_tokens) * H * d * 2 >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
+
+  // the packed tensors as one batch element of total_tokens rows; each CTA
+  // offsets its row coordinates by its sequence's first row
+  CUtensorMap tq, tdo, tk, tv;
+  int rc = make_map(&tq, q, d, H, total_tokens, 1, 128);
+  if (rc == FA_OK) rc = make_map(&tdo, dout, d, H, total_tokens, 1, 128);
+  if (rc == FA_OK) rc = make_map(&tk, k, d, Hkv, total_tokens, 1, 128);
+  if (rc == FA_OK) rc = make_map(&tv, v, d, Hkv, total_tokens, 1, 128);
+  if (rc != FA_OK) return rc;
+
+  BwdParams p{};
+  p.status = status_ptr();
+  if (p.status == nullptr) return FA_ERR_CUDA;
+  p.out = out;
+  p.dout = dout;
+  p.lse = lse;
+  p.n_tiles = static_cast<int>(n_tiles);
+  p.Npad = p.n_tiles * 128;
+  p.nlse2 = static_cast<float *>(workspace);
+  p.ndsum = p.nlse2 + static_cast<size_t>(num_seqs) * H * p.Npad;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.B = num_seqs;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.group = H / Hkv;
+  p.N = n_max;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.cu_seqlens = cu_seqlens;
+  p.total_tokens = total_tokens;
+  cudaError_t e = launch_bwd(tq, tdo, tk, tv, p, d, causal != 0,
+                             reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits) {
   if (B < 0 || H < 1 || N < 0 || num_splits < 0 || (d != 64 && d != 128)) return 0;
   return split_ws_bytes(split_ws(B, H, N, d, num_splits));

@@ -113,17 +113,19 @@ constexpr int kBwdThreads = 320;  // 8 elementwise warps + 1 MMA warp + 1 TMA wa
 
 struct BwdParams {
   unsigned int *status;   // per-device sticky FA_DEV_* word
-  const void *out;        // forward output O, bf16 [B, N, H, d]
-  const void *dout;       // upstream gradient dO, bf16 [B, N, H, d]
-  const float *lse;       // forward log-sum-exp, fp32 [B, H, N] (natural log)
+  const void *out;        // forward output O, bf16 [B, N, H, d] (packed: [T, H, d])
+  const void *dout;       // upstream gradient dO, layout of out
+  const float *lse;       // forward log-sum-exp, fp32 [B, H, N] (packed: [H, T]) (natural log)
   float *nlse2;           // workspace: -lse in log2 units, [B, H, Npad]
   float *ndsum;           // workspace: -D = -rowsum(dO * O), [B, H, Npad]
   void *dq, *dk, *dv;     // bf16, layouts of q, k, v
-  int B, H, Hkv, group, N;
+  int B, H, Hkv, group, N;  // packed batches: B sequences of at most N (max_seqlen) rows
   int Npad;               // N rounded up to 128
   int n_tiles;            // Npad / 128
   float scale;            // softmax scale
   float scale_log2;       // scale * log2(e)
+  const int32_t *cu_seqlens;  // packed batches only: sequence b is rows [cu[b], cu[b + 1])
+  int total_tokens;           // packed batches only: T
 };
 
 // ------------------------------------------------------------------- decode

@@ -174,6 +174,34 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *out, const f
            float scale, int causal, void *workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
+ * Gradient of a packed batch of variable-length sequences: the fa_bwd
+ * products applied to each sequence of an fa_fwd_varlen call on its own rows
+ * (its keys are the only ones its queries see; causal masking by position
+ * inside the sequence).  The same definition as fa_bwd (chain rule through
+ * "S12 FlashAttention"'s softmax), with the packing of fa_fwd_varlen.
+ *   q, out, dout, dq : [total_tokens, H, d] bf16
+ *   k, v, dk, dv     : [total_tokens, Hkv, d] bf16
+ *   lse              : [H, total_tokens] fp32, as written by fa_fwd_varlen
+ *   cu_seqlens       : int32 DEVICE array [num_seqs + 1]; sequence s is rows
+ *                      [cu_seqlens[s], cu_seqlens[s + 1]).  A sequence whose
+ *                      bounds are decreasing, outside [0, total_tokens] or
+ *                      longer than max_seqlen raises FA_DEV_BAD_SEQLEN and its
+ *                      rows of dq, dk and dv are not written; rows that belong
+ *                      to no sequence are not written either.
+ *   max_seqlen       : upper bound on every sequence's length
+ *   workspace        : >= fa_bwd_workspace_size(num_seqs, H, max_seqlen)
+ *                      bytes, 256-byte aligned, owned by the caller;
+ *                      overwritten
+ * Supported: d in {64, 128}.  All buffers device memory; asynchronous on
+ * `stream`.  Errors as fa_bwd.
+ */
+int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *out, const float *lse,
+                  const void *dout, void *dq, void *dk, void *dv, const int32_t *cu_seqlens,
+                  int num_seqs, int total_tokens, int max_seqlen, int H, int Hkv, int d,
+                  float scale, int causal, void *workspace, size_t workspace_bytes,
+                  fa_stream_t stream);
+
+/*
  * Dense prefill with the key tiles of every query tile split over several
  * CTAs, for batches whose B * H * ceil(N / 256) work items cannot fill the
  * GPU (long single sequences).  "S12 FlashAttention", "What this unlocks

@@ -25,7 +25,8 @@ Pinned in ``tests/oracle_pins.py`` by central finite differences of the
 scalar <O, dO> on tiny inputs (independent of these formulas), and by the
 invariants sum_j dV_j = sum_i dO_i (rows of P sum to 1) and, without a
 mask, sum_j dK_j = 0 (softmax is unchanged when every key moves by the same
-vector).
+vector).  The packed (varlen) form is pinned by finite differences through
+the packed forward oracle ``oracle.attention.attention_varlen``.
 """
 
 from __future__ import annotations
@@ -34,7 +35,7 @@ import math
 
 import numpy as np
 
-__all__ = ["attention_backward_one", "attention_backward_dense"]
+__all__ = ["attention_backward_one", "attention_backward_dense", "attention_backward_varlen"]
 
 
 def attention_backward_one(q, k, v, do, scale=None, causal=False):
@@ -87,3 +88,21 @@ def attention_backward_dense(q, k, v, do, scale=None, causal=False):
     outs = [attention_backward_one(q[b], k[b], v[b], do[b], scale=scale, causal=causal)
             for b in range(np.asarray(q).shape[0])]
     return tuple(np.stack([o[i] for o in outs]) for i in range(3))
+
+
+def attention_backward_varlen(q, k, v, do, cu_seqlens, scale=None, causal=False):
+    """Packed variable-length batch (the explainer article's "Varlen" section):
+    q, do [T, H, d]; k, v [T, Hkv, d]; sequence s owns rows [cu[s], cu[s+1])
+    and sees only its own keys, so its gradients are those of the sequence on
+    its own.  Rows outside every sequence get zero gradients."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for s in range(len(cu) - 1):
+        a, e = int(cu[s]), int(cu[s + 1])
+        dq[a:e], dk[a:e], dv[a:e] = attention_backward_one(q[a:e], k[a:e], v[a:e], do[a:e],
+                                                           scale=scale, causal=causal)
+    return dq, dk, dv

@@ -539,5 +539,37 @@ def pin_backward_dense_layout(fwd, bwd):
             np.testing.assert_allclose(x, y, atol=0)
 
 
+def pin_backward_varlen_finite_differences(fwd, bwd):
+    """The packed gradient against central differences of <O, dO> through the
+    packed forward oracle (sequences of 3, 0, 1 and 4 rows, GQA, both masks):
+    a row slice taken from the wrong sequence, or a key seen across a
+    sequence boundary, moves the loss where the analytic gradient says it
+    does not."""
+    rng = np.random.default_rng(53)
+    cu = np.array([0, 3, 3, 4, 8])
+    t = int(cu[-1])
+    eps = 1e-6
+    scale = 0.8
+    for causal in (False, True):
+        q, k, v = rand(rng, t, 2, 3), rand(rng, t, 1, 3), rand(rng, t, 1, 3)
+        do = rand(rng, t, 2, 3)
+        dq, dk, dv = bwd.attention_backward_varlen(q, k, v, do, cu, scale=scale, causal=causal)
+
+        def loss(args):
+            o, _ = fwd.attention_varlen(args["q"], args["k"], args["v"], cu, scale=scale,
+                                        causal=causal)
+            return float((o * do).sum())
+
+        for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+            num = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += eps
+                xm[idx] -= eps
+                num[idx] = (loss({"q": q, "k": k, "v": v, name: xp})
+                            - loss({"q": q, "k": k, "v": v, name: xm})) / (2 * eps)
+            np.testing.assert_allclose(g, num, rtol=1e-6, atol=1e-8, err_msg=f"varlen d{name}")
+
+
 BACKWARD_PINS = [pin_backward_finite_differences, pin_backward_invariants,
-                 pin_backward_dense_layout]
+                 pin_backward_dense_layout, pin_backward_varlen_finite_differences]

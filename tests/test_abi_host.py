@@ -36,7 +36,7 @@ BOUNDARY = sorted([
     "fa_last_device_status", "fa_status_string",
     "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_fwd_paged", "fa_fwd_fp8",
     "fa_fwd_varlen_fp8",
-    "fa_bwd", "fa_bwd_workspace_size", "fa_decode_paged_noalloc",
+    "fa_bwd", "fa_bwd_varlen", "fa_bwd_workspace_size", "fa_decode_paged_noalloc",
     "fa_device_status", "fa_selftest_wait_timeout", "fa_version",
 ])
 

@@ -18,7 +18,7 @@ import pytest
 
 import oracle
 from exact_attention_33_gb300 import workloads as W
-from gpu_helpers import assert_device_clean, dev_bf16, host_f64, torch_mod
+from gpu_helpers import assert_device_clean, dev_bf16, dev_i32, host_f64, torch_mod
 
 pytestmark = pytest.mark.gpu
 
@@ -159,4 +159,103 @@ def test_backward_full_size_sampled(fa):
                 check_grad("dk", host_f64(dk[b, keys, h]), dk_ref, what),
                 check_grad("dv", host_f64(dv[b, keys, h]), dv_ref, what)]
         print(f"{what}: relative RMS errors dq {errs[0]:.2e} dk {errs[1]:.2e} dv {errs[2]:.2e}")
+    assert_device_clean()
+
+
+# ------------------------------------------------------------- packed batches
+def run_varlen(fa, lengths, H, Hkv, d, causal, seed, pad_rows=0):
+    """fa_bwd_varlen on a packed batch against the packed gradient oracle,
+    one sequence at a time (each sequence's gradients at the tolerance of
+    its own scale).  ``pad_rows`` extra rows after the last sequence belong
+    to no sequence: their gradients keep the value they had before the call."""
+    torch = torch_mod()
+    inp = W.varlen_inputs(lengths, H, Hkv, d, seed=seed)
+    T = inp.total_tokens
+    cu = inp.cu_seqlens
+    max_len = int(max(lengths))
+    do_bits = W.normal_bf16_bits((T, H, d), seed, 3)
+    pad = lambda bits, h: np.concatenate([bits, W.normal_bf16_bits((pad_rows, h, d), seed, 9)])
+    q, k, v = dev_bf16(pad(inp.q, H)), dev_bf16(pad(inp.k, Hkv)), dev_bf16(pad(inp.v, Hkv))
+    do = dev_bf16(pad(do_bits, H))
+    cu_d = dev_i32(cu)
+    out, lse = fa.fa_fwd_varlen(q, k, v, cu_d, max_len, causal=causal)
+    sentinel = 7.0
+    dq = torch.full_like(q, sentinel)
+    dk = torch.full_like(k, sentinel)
+    dv = torch.full_like(v, sentinel)
+    fa.fa_bwd_varlen(q, k, v, out, lse, do, cu_d, max_len, causal=causal, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    rq, rk, rv = oracle.attention_backward_varlen(f64(inp.q), f64(inp.k), f64(inp.v),
+                                                  f64(do_bits), cu, causal=causal)
+    gq, gk, gv = host_f64(dq), host_f64(dk), host_f64(dv)
+    worst = 0.0
+    for s in range(len(lengths)):
+        a, e = int(cu[s]), int(cu[s + 1])
+        if e == a:
+            continue
+        what = f"seq {s} of {list(lengths)} H{H}/{Hkv} d{d} causal={causal}"
+        for n, g, r in (("dq", gq, rq), ("dk", gk, rk), ("dv", gv, rv)):
+            worst = max(worst, check_grad(n, g[a:e], r[a:e], what))
+    if pad_rows:
+        for n, g in (("dq", gq), ("dk", gk), ("dv", gv)):
+            assert np.all(g[T:] == sentinel), f"{n}: a row outside every sequence was written"
+    print(f"{list(lengths)} H{H}/{Hkv} d{d} causal={causal}: worst relative RMS {worst:.2e}")
+    assert_device_clean()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("lengths,H,Hkv", [([1, 130, 0, 257, 64], 4, 2),
+                                           ([300, 5, 128], 3, 1),
+                                           ([129], 2, 2)])
+def test_backward_varlen(fa, d, causal, lengths, H, Hkv):
+    run_varlen(fa, lengths, H, Hkv, d, causal, seed=200 + sum(lengths))
+
+
+def test_backward_varlen_rows_outside_sequences(fa):
+    run_varlen(fa, [70, 190], 2, 1, 128, True, seed=211, pad_rows=37)
+
+
+def test_backward_varlen_many_tiles(fa):
+    """Sequences of 1000 to 2100 rows (8 to 17 tiles each way)."""
+    run_varlen(fa, [1000, 2100, 1537], 4, 1, 128, True, seed=212)
+
+
+def test_backward_varlen_matches_dense(fa):
+    """Equal lengths packed back to back give the dense call's gradients bit
+    for bit (the same tiles in the same order)."""
+    torch = torch_mod()
+    B, N, H, Hkv, d = 3, 200, 4, 2, 64
+    inp = W.dense_inputs(B, N, H, Hkv, d, seed=213)
+    do_bits = W.normal_bf16_bits((B, N, H, d), 213, 3)
+    q, k, v, do = dev_bf16(inp.q), dev_bf16(inp.k), dev_bf16(inp.v), dev_bf16(do_bits)
+    out, lse = fa.fa_fwd(q, k, v, causal=True)
+    dense = fa.fa_bwd(q, k, v, out, lse, do, causal=True)
+    cu = dev_i32(np.arange(B + 1) * N)
+    flat = lambda t: t.reshape(B * N, t.shape[2], d)
+    packed = fa.fa_bwd_varlen(flat(q), flat(k), flat(v), flat(out),
+                              lse.permute(1, 0, 2).reshape(H, B * N).contiguous(), flat(do), cu, N,
+                              causal=True)
+    torch.cuda.synchronize()
+    for x, y in zip(dense, packed):
+        assert torch.equal(flat(x), y)
+    assert_device_clean()
+
+
+def test_backward_varlen_bad_cu_seqlens_flagged(fa):
+    torch = torch_mod()
+    inp = W.varlen_inputs([10, 20], 2, 2, 64, seed=214)
+    q, k, v = dev_bf16(inp.q), dev_bf16(inp.k), dev_bf16(inp.v)
+    cu = dev_i32(inp.cu_seqlens)
+    out, lse = fa.fa_fwd_varlen(q, k, v, cu, 20)
+    torch.cuda.synchronize()
+    fa.fa_device_status(clear=True)
+    for bad, max_len in (([0, 25, 20], 25), ([0, 10, 30], 15)):   # decreasing; too long
+        fa.fa_bwd_varlen(q, k, v, out, lse, q, dev_i32(np.array(bad, dtype=np.int32)), max_len)
+        torch.cuda.synchronize()
+        assert fa.fa_device_status(clear=True) & fa.FA_DEV_BAD_SEQLEN
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fa.FaError) as e:
+        fa.fa_bwd_varlen(q, k, v, out, lse, q, cu, 20, workspace=small)
+    assert e.value.status == -4
     assert_device_clean()

@@ -171,3 +171,38 @@ def test_backward_mistake_is_caught(monkeypatch, mistake):
         except (AssertionError, ValueError, IndexError):
             failures += 1
     assert failures > 0
+
+
+def mutant_backward_varlen(mistake):
+    one = grad_mod.attention_backward_one
+
+    def attention_backward_varlen(q, k, v, do, cu_seqlens, scale=None, causal=False):
+        q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
+        cu = np.asarray(cu_seqlens, dtype=np.int64)
+        if mistake == "one_sequence":  # keys seen across sequence boundaries
+            return one(q, k, v, do, scale=scale, causal=causal)
+        dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+        for s in range(len(cu) - 1):
+            a, e = int(cu[s]), int(cu[s + 1])
+            if mistake == "keys_from_start":  # every sequence reads the first keys
+                r = one(q[a:e], k[:e - a], v[:e - a], do[a:e], scale=scale, causal=causal)
+            else:  # "last_row_dropped"
+                r = one(q[a:max(a, e - 1)], k[a:e], v[a:e], do[a:max(a, e - 1)], scale=scale,
+                        causal=causal)
+                r = (np.concatenate([r[0], np.zeros((e - a - r[0].shape[0],) + q.shape[1:])]),
+                     r[1], r[2])
+            dq[a:e], dk[a:e], dv[a:e] = r
+        return dq, dk, dv
+    return attention_backward_varlen
+
+
+@pytest.mark.parametrize("mistake", ["one_sequence", "keys_from_start", "last_row_dropped"])
+def test_backward_varlen_mistake_is_caught(monkeypatch, mistake):
+    monkeypatch.setattr(grad_mod, "attention_backward_varlen", mutant_backward_varlen(mistake))
+    failures = 0
+    for pin in BACKWARD_PINS:
+        try:
+            pin(ora_mod, grad_mod)
+        except (AssertionError, ValueError, IndexError):
+            failures += 1
+    assert failures > 0
