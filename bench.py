@@ -515,6 +515,48 @@ def measure_backward(torch, device, fa, steps, warmup, peak):
             "launches_per_call": 3}
 
 
+def measure_backward_varlen(torch, device, fa, steps, warmup, peak):
+    """Backward pass of a packed varlen batch (fa_bwd_varlen) on the varlen
+    workload (32 sequences of U[64, 4096] tokens, GQA 16 / 4, d = 128,
+    causal), timed with CUDA events on its own.  Work: 2.5 times the
+    forward's causal products of each sequence, as for the dense backward."""
+    cfg = W.WORKLOADS["varlen_gqa_d128"]
+    lengths = W.varlen_lengths(cfg["num_seqs"], cfg["len_lo"], cfg["len_hi"])
+    H, Hkv, d = cfg["H"], cfg["Hkv"], cfg["d"]
+    inp = W.varlen_inputs(lengths, H, Hkv, d, seed=0)
+    T = inp.total_tokens
+    q, k, v = (to_dev(getattr(inp, n), torch, device) for n in ("q", "k", "v"))
+    do = to_dev(W.normal_bf16_bits((T, H, d), 0, 3), torch, device)
+    cu = torch.from_numpy(inp.cu_seqlens.astype(np.int32)).to(device)
+    max_len = int(np.max(lengths))
+    out, lse = fa.fa_fwd_varlen(q, k, v, cu, max_len, causal=True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_bwd_workspace_size(len(lengths), H, max_len), dtype=torch.uint8,
+                     device=device)
+    flops = 2.5 * W.varlen_flops(lengths, H, d, True)
+
+    def run():
+        fa.fa_bwd_varlen(q, k, v, out, lse, do, cu, max_len, causal=True, dq=dq, dk=dk, dv=dv,
+                         workspace=ws)
+
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    tf = flops / (ms / 1e3) / 1e12
+    return {"workload": "backward of the packed varlen causal prefill: 32 seqs U[64,4096], "
+                        "H16/Hkv4, d128 (dQ, dK, dV from O, lse, dO)",
+            "ms": ms, "tflops": tf, "frac_of_peak": tf / peak, "flops": flops,
+            "launches_per_call": 3}
+
+
 L2_FLUSH_BYTES = 256 << 20   # twice the GB300's L2
 SLEEP_CYCLES = 200_000        # ~0.1 ms of device time before each timed call
 
@@ -630,7 +672,8 @@ def measure_decode_small_batches(torch, device, fa, steps, warmup):
     return res
 
 
-NEXT_LEGS = ("paged_prefill", "splitkv", "fp8_prefill", "fp8_varlen", "backward")
+NEXT_LEGS = ("paged_prefill", "splitkv", "fp8_prefill", "fp8_varlen", "backward",
+             "backward_varlen")
 # legs that --profile-leg can run alone (one launch kind each, for ncu captures)
 PROFILE_LEGS = NEXT_LEGS + ("dense_d64", "dense_d64_causal", "decode_small")
 
@@ -638,7 +681,7 @@ PROFILE_LEGS = NEXT_LEGS + ("dense_d64", "dense_d64_causal", "decode_small")
 def run_next_leg(name, torch, device, fa, steps, warmup, peak):
     fn = {"paged_prefill": measure_paged_prefill, "splitkv": measure_splitkv,
           "fp8_prefill": measure_fp8_prefill, "fp8_varlen": measure_fp8_varlen,
-          "backward": measure_backward,
+          "backward": measure_backward, "backward_varlen": measure_backward_varlen,
           "dense_d64": lambda t, dv, f, s, w, pk: measure_dense_d64(t, dv, f, s, w, (False,), False),
           "dense_d64_causal": lambda t, dv, f, s, w, pk: measure_dense_d64(t, dv, f, s, w, (True,),
                                                                            False),
@@ -828,7 +871,7 @@ def bench_ours(args, rank, world, local):
         peaks0 = measured_peaks()
         for name in NEXT_LEGS:
             nxt[name] = run_next_leg(name, torch, device, fa,
-                                     min(args.steps, 20 if name == "backward" else 50),
+                                     min(args.steps, 20 if name.startswith("backward") else 50),
                                      args.warmup, peaks0["bf16_tflops"])
         other["dense_d64"] = measure_dense_d64(torch, device, fa, min(args.steps, 50),
                                                args.warmup)

@@ -23,6 +23,8 @@
 // The bf16 operands the elementwise warps write (P, dS) land in the columns
 // each half has already read: keys 0-63 in columns [0, 32), keys 64-127 in
 // [64, 96) of the region, so the TMEM-sourced MMAs read them at that split.
+#include <algorithm>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -84,10 +86,13 @@ struct BwdDqLayout {
   static constexpr int kK = kDO + kTileBytes;
   static constexpr int kV = kK + kStagesK * kTileBytes;
   static constexpr int kBar = kV + kStagesV * kTileBytes;
-  static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 6;
+  static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 9;
   static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kItem = kMisc + 16;  // the work item slot
+  static constexpr int kVec = kItem + 32;   // the item's -lse2 and -D vectors (128 floats each)
+  static constexpr int kBytes = kVec + 1024;
   static constexpr int kSmemAlloc = kBytes + 1024;
+  static_assert(kSmemAlloc <= 232448, "dQ shared memory exceeds 227 KiB");
 };
 
 // S-like MMA (both operands K-major over d): D[tmem] = A[128 x d] B[128 x d]^T.
@@ -165,6 +170,131 @@ __device__ __forceinline__ void bwd_seq(const BwdParams &p, int b, int &start, i
   }
 }
 
+// Longest-first order of the 128-row tiles of a packed batch of at most
+// kBwdOrderMaxSeqs sequences, so that the heaviest CTAs start first and the
+// last wave holds the lightest ones.  Levels L = n_tiles .. 1 in turn:
+//  - causal: level L holds, for every sequence of at least L tiles (in
+//    sequence order), the tile whose work is L tiles: query tile L - 1 (it
+//    sees L key tiles) or key tile n_b - L (L query tiles see it);
+//  - non-causal: level L holds every tile of the sequences of exactly L tiles
+//    (each tile's work is the sequence's n_b tiles).
+// Returns the sequence of work item `item` and sets `tile`, or returns -1 past
+// the last item.  Run by whole warps (every lane gets the answer); a sequence
+// with invalid bounds has no tiles (the preprocess reports it).
+template <bool CAUSAL, bool KEY_TILES>
+__device__ __forceinline__ int longest_first_item(const BwdParams &p, int item, int &tile) {
+  const int lane = threadIdx.x & 31;
+  int nt[kBwdOrderMaxSeqs / 32];  // tiles of sequence lane + 32 k
+#pragma unroll
+  for (int k = 0; k < kBwdOrderMaxSeqs / 32; ++k) {
+    const int b = lane + 32 * k;
+    nt[k] = 0;
+    if (b < p.B) {
+      const int a = checked_load(p.cu_seqlens, b, p.B + 1, p.status);
+      const int e = checked_load(p.cu_seqlens, b + 1, p.B + 1, p.status);
+      if (a >= 0 && e >= a && e <= p.total_tokens && e - a <= p.N) nt[k] = (e - a + 127) / 128;
+    }
+  }
+  // items at levels >= L (non-increasing in L)
+  auto above = [&](int L) {
+    int c = 0;
+#pragma unroll
+    for (int k = 0; k < kBwdOrderMaxSeqs / 32; ++k)
+      c += CAUSAL ? max(0, nt[k] - L + 1) : (nt[k] >= L ? nt[k] : 0);
+#pragma unroll
+    for (int sft = 16; sft > 0; sft >>= 1) c += __shfl_xor_sync(0xffffffffu, c, sft);
+    return c;
+  };
+  if (item >= above(1)) return -1;
+  int lo = 1, hi = p.n_tiles;  // the level of `item`: the largest L with above(L) > item
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (above(mid) > item)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int L = lo;
+  int o = item - (L < p.n_tiles ? above(L + 1) : 0);  // place in the level
+  int idx = o;                                          // member of the level
+  if (!CAUSAL) {
+    idx = o / L;
+    tile = o % L;
+  }
+#pragma unroll
+  for (int k = 0; k < kBwdOrderMaxSeqs / 32; ++k) {
+    const bool in = CAUSAL ? nt[k] >= L : nt[k] == L;
+    const unsigned m = __ballot_sync(0xffffffffu, in);
+    const int cnt = __popc(m);
+    if (idx < cnt) {
+      const bool hit = in && __popc(m & ((1u << lane) - 1u)) == idx;
+      const int src = __ffs(__ballot_sync(0xffffffffu, hit)) - 1;
+      const int n_b = __shfl_sync(0xffffffffu, nt[k], src);
+      if (CAUSAL) tile = KEY_TILES ? n_b - L : L - 1;
+      return src + 32 * k;
+    }
+    idx -= cnt;
+  }
+  return -1;  // not reached: the level holds idx + 1 members
+}
+
+// A work item of a persistent backward CTA: one 128-row tile of one
+// sequence (batch element) and one head, handed from the producer warp to
+// the others through shared memory.
+struct BwdItem {
+  int b;      // sequence
+  int tile;   // query tile (dQ) or key tile (dK / dV)
+  int h;      // query head (dQ) or KV head (dK / dV)
+  int start;  // the sequence's first row in a packed batch (0 when dense)
+  int len;    // its rows
+  int valid;  // 0: no work left
+};
+static_assert(sizeof(BwdItem) <= 32, "work item slot");
+
+// Claims the next work item from the call's counter (lane 0 takes an index,
+// the whole warp decodes it) and returns it, or an item with valid = 0 once
+// none are left.  Heads run fastest.  Tiles run heaviest first: for the
+// query tiles of a causal pass the last tile first, for key tiles the first;
+// a dense batch takes sequence by sequence, a packed batch its tiles
+// longest-first; a packed batch of more sequences than that order covers
+// takes sequence by sequence and claims again past a sequence's last tile.
+// Run by whole warps.
+template <bool CAUSAL, bool VARLEN, bool KEY_TILES>
+__device__ BwdItem claim_item(const BwdParams &p, unsigned int *counter, int heads) {
+  BwdItem it{};
+  const long long total = static_cast<long long>(p.B) * p.n_tiles * heads;
+  for (;;) {
+    unsigned int w = 0;
+    if ((threadIdx.x & 31) == 0) w = atomicAdd(counter, 1u);
+    w = __shfl_sync(0xffffffffu, w, 0);
+    if (w >= total) return it;
+    const int h = static_cast<int>(w % heads);
+    const int r = static_cast<int>(w / heads);
+    int b, rank, t;
+    if (VARLEN && p.longest_first) {
+      b = longest_first_item<CAUSAL, KEY_TILES>(p, r, t);
+      if (b < 0) return it;
+    } else {
+      // sequence by sequence (the items in flight share the sequence's K and
+      // V, or Q and dO, in L2)
+      b = r / p.n_tiles;
+      rank = r % p.n_tiles;
+      t = (CAUSAL && !KEY_TILES) ? p.n_tiles - 1 - rank : rank;
+    }
+    int start, len;
+    bwd_seq<VARLEN>(p, b, start, len, false);
+    if (t < (len + 127) / 128) {
+      it.b = b;
+      it.tile = t;
+      it.h = h;
+      it.start = start;
+      it.len = len;
+      it.valid = 1;
+      return it;
+    }
+  }
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ preprocess
@@ -178,6 +308,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
   const int sub = threadIdx.x % TPR;
   const long long gr = static_cast<long long>(blockIdx.x) * (256 / TPR) + threadIdx.x / TPR;
   const long long total = static_cast<long long>(p.B) * p.Npad * p.H;
+  // the work counters of the dQ and dK / dV kernels, which run after this one
+  if (blockIdx.x == 0 && threadIdx.x < 2) p.work[threadIdx.x] = 0u;
   if (gr >= total) return;  // whole row groups leave together (TPR divides 32)
   // Row groups run over the rows of one (b, h) first, so that the lse reads
   // and the D / lse2 writes of a warp are contiguous; each row's O and dO
@@ -226,6 +358,13 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
 }
 
 // ------------------------------------------------------------------------- dQ
+// Persistent: one CTA per SM takes (query tile, head) work items from the
+// call's counter until none are left, so that one item's first products and
+// copies overlap the previous item's dQ epilogue and no CTA launch or set-up
+// sits between items.  The producer warp claims and decodes each item and
+// hands it to the other warps through shared memory (slot, published by the
+// Q / dO barrier); every barrier of the key-tile pipeline counts key tiles
+// over all of the CTA's items.
 template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -234,27 +373,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   using L = BwdDqLayout<D>;
   constexpr int SK = L::kStagesK;
   constexpr int SV = L::kStagesV;
-  // heaviest query tiles first (causal), heads fastest
-  const int h = static_cast<int>(blockIdx.x % p.H);
-  const int rest = static_cast<int>(blockIdx.x / p.H);
-  const int t_rank = rest % p.n_tiles;
-  const int b = rest / p.n_tiles;
-  const int t = CAUSAL ? (p.n_tiles - 1 - t_rank) : t_rank;
-  const int kvh = h / p.group;
-  // the sequence's rows: a packed batch's tiles past its end leave at once
-  int start, len;
-  bwd_seq<VARLEN>(p, b, start, len, t_rank == 0 && h == 0 && threadIdx.x == 0);
-  const int n_tiles = VARLEN ? (len + 127) / 128 : p.n_tiles;
-  if (t >= n_tiles) return;
-  const int row0 = VARLEN ? start : 0;  // first row of the sequence in the tensor maps
-  const int bc = VARLEN ? 0 : b;        // the maps' outer coordinate
-  const int n_kv = CAUSAL ? (t + 1) : n_tiles;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBar);
-  uint64_t *in_full = bars;        // Q and dO
+  uint64_t *in_full = bars;        // Q and dO of the item (and its slot)
   uint64_t *k_full = bars + 1;     // [SK]
   uint64_t *k_empty = k_full + SK;
   uint64_t *v_full = k_empty + SK;  // [SV]
@@ -263,10 +387,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t *s_read = s_full + 1;    // the elementwise warps have read S_j
   uint64_t *dp_full = s_read + 1;
   uint64_t *p_full = dp_full + 1;   // dS_j (bf16) is in TMEM
-  uint64_t *dq_done = p_full + 1;
+  uint64_t *dq_done = p_full + 1;   // the item's dQ is complete in TMEM
   uint64_t *drain = dq_done + 1;
+  uint64_t *qdo_empty = drain + 1;  // the item's last products that read Q and dO are done
+  uint64_t *dq_free = qdo_empty + 1;  // the elementwise warps have read the item's dQ
+  uint64_t *taken = dq_free + 1;    // the MMA and elementwise warps have read the slot
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
+  volatile BwdItem *slot = reinterpret_cast<volatile BwdItem *>(smem + L::kItem);
+  float *sVec = reinterpret_cast<float *>(smem + L::kVec);  // -lse2 [0, 128), -D [128, 256)
   uint8_t *sQ = smem + L::kQ;
   uint8_t *sDO = smem + L::kDO;
   uint8_t *sK = smem + L::kK;
@@ -290,6 +419,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(p_full, 256);
     mbar_init(dq_done, 1);
     mbar_init(drain, 1);
+    mbar_init(qdo_empty, 1);
+    mbar_init(dq_free, 256);
+    mbar_init(taken, 9);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -303,181 +435,283 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // reads the slot of item m (and, for row `row` >= 0, its entries of the
+  // item's vectors) once its barrier phase is complete, then tells the
+  // producer (one arrival per warp)
+  auto take = [&](int m, BwdItem &it, int row, float &nlse2, float &ndsum) -> bool {
+    bool ok = mbar_wait(in_full, m & 1, abort_flag, p.status);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) return false;
+    it.b = slot->b;
+    it.tile = slot->tile;
+    it.h = slot->h;
+    it.start = slot->start;
+    it.len = slot->len;
+    it.valid = slot->valid;
+    if (row >= 0 && it.valid) {
+      nlse2 = sVec[row];
+      ndsum = sVec[128 + row];
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(taken);
+    return true;
+  };
+
   if (warp == 9) {
     // ------------------------------------------------------------ producer
+    // Item m: claim and decode it, wait until every warp has read slot m - 1
+    // and the products of item m - 1 that read Q and dO are done, publish
+    // it with its Q and dO, then K(j) and V(j) of its key tiles, each ring
+    // counting key tiles over all items.
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_do);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(in_full, 2 * L::kTileBytes);
+    }
+    bool ok = true;
+    int gk = 0, gv = 0;  // K and V tiles issued so far
+    int last = -1;       // the last item whose Q and dO were issued
+    for (int m = 0;; ++m) {
+      const BwdItem it = claim_item<CAUSAL, VARLEN, false>(p, p.work + 0, p.H);
+      if (lane == 0 && m > 0)
+        ok = mbar_wait(taken, (m - 1) & 1, abort_flag, p.status) &&
+             mbar_wait(qdo_empty, (m - 1) & 1, abort_flag, p.status);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (lane == 0) {
+        slot->b = it.b;
+        slot->tile = it.tile;
+        slot->h = it.h;
+        slot->start = it.start;
+        slot->len = it.len;
+        slot->valid = it.valid;
+        if (it.valid) {
+          const int row0 = VARLEN ? it.start : 0, bc = VARLEN ? 0 : it.b;
+          // the tile's 128 entries of the workspace vectors (a checked build
+          // that finds them outside the workspace copies entries 0..127, so
+          // that the barrier still gets its bytes)
+          size_t vec = (static_cast<size_t>(it.b) * p.H + it.h) * p.Npad + it.tile * 128;
+          if (!in_bounds(vec, 128, static_cast<size_t>(p.B) * p.H * p.Npad, p.status)) vec = 0;
+          mbar_arrive_expect_tx(in_full, 2 * L::kTileBytes + 1024);
 #pragma unroll
-      for (int c = 0; c < L::kChunks; ++c) {
-        tma_load_4d(sQ + c * L::kChunkBytes, &tm_q, in_full, c * 64, h, row0 + t * 128, bc);
-        tma_load_4d(sDO + c * L::kChunkBytes, &tm_do, in_full, c * 64, h, row0 + t * 128, bc);
+          for (int c = 0; c < L::kChunks; ++c) {
+            tma_load_4d(sQ + c * L::kChunkBytes, &tm_q, in_full, c * 64, it.h, row0 + it.tile * 128, bc);
+            tma_load_4d(sDO + c * L::kChunkBytes, &tm_do, in_full, c * 64, it.h, row0 + it.tile * 128,
+                        bc);
+          }
+          bulk_load(sVec, p.nlse2 + vec, 512, in_full);
+          bulk_load(sVec + 128, p.ndsum + vec, 512, in_full);
+        } else {
+          mbar_arrive(in_full);  // no work left: publishes the empty slot
+        }
       }
-      // K(j) then V(j) for every j; each waits for its own ring
-      int k_issued = 0, v_issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int sk = j % SK, sv = j % SV;
-        if (j >= SK && !mbar_wait(&k_empty[sk], ((j / SK) - 1) & 1, abort_flag, p.status)) break;
-        mbar_arrive_expect_tx(&k_full[sk], L::kTileBytes);
+      if (!it.valid) break;
+      last = m;
+      if (lane == 0) {
+        const int row0 = VARLEN ? it.start : 0, bc = VARLEN ? 0 : it.b;
+        const int kvh = it.h / p.group;
+        const int n_kv = CAUSAL ? it.tile + 1 : (it.len + 127) / 128;
+        for (int j = 0; j < n_kv; ++j) {
+          const int sk = gk % SK, sv = gv % SV;
+          if (gk >= SK && !mbar_wait(&k_empty[sk], ((gk / SK) - 1) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&k_full[sk], L::kTileBytes);
 #pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_4d(sK + sk * L::kTileBytes + c * L::kChunkBytes, &tm_k, &k_full[sk], c * 64,
-                      kvh, row0 + j * 128, bc);
-        k_issued = j + 1;
-        if (j >= SV && !mbar_wait(&v_empty[sv], ((j / SV) - 1) & 1, abort_flag, p.status)) break;
-        mbar_arrive_expect_tx(&v_full[sv], L::kTileBytes);
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_4d(sK + sk * L::kTileBytes + c * L::kChunkBytes, &tm_k, &k_full[sk], c * 64,
+                        kvh, row0 + j * 128, bc);
+          ++gk;
+          if (gv >= SV && !mbar_wait(&v_empty[sv], ((gv / SV) - 1) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&v_full[sv], L::kTileBytes);
 #pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_4d(sV + sv * L::kTileBytes + c * L::kChunkBytes, &tm_v, &v_full[sv], c * 64,
-                      kvh, row0 + j * 128, bc);
-        v_issued = j + 1;
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_4d(sV + sv * L::kTileBytes + c * L::kChunkBytes, &tm_v, &v_full[sv], c * 64,
+                        kvh, row0 + j * 128, bc);
+          ++gv;
+        }
       }
-      mbar_drain(in_full, 0, p.status);
-      for (int j = max(0, k_issued - SK); j < k_issued; ++j)
-        mbar_drain(&k_full[j % SK], (j / SK) & 1, p.status);
-      for (int j = max(0, v_issued - SV); j < v_issued; ++j)
-        mbar_drain(&v_full[j % SV], (j / SV) & 1, p.status);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+    }
+    if (!ok && lane == 0) {
+      // a wait ran out: let the copies still in flight land before the CTA
+      // leaves (Q and dO of the last item, K and V of the last tiles issued)
+      if (last >= 0) mbar_drain(in_full, last & 1, p.status);
+      for (int x = max(0, gk - SK); x < gk; ++x) mbar_drain(&k_full[x % SK], (x / SK) & 1, p.status);
+      for (int x = max(0, gv - SV); x < gv; ++x) mbar_drain(&v_full[x % SV], (x / SV) & 1, p.status);
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
     // S lives in TMEM [0,128), dQ in [256, 256 + d), and dP in two buffers,
-    // [128,256) for even key tiles and [384,512) for odd ones.  Per key tile
-    // j: S_{j+1} as soon as the elementwise warps have read S_j (s_read),
-    // then dP_{j+1} into the other buffer, so both run while they finish
-    // tile j; then dQ += dS_j K_j once dS_j (bf16, written over dP_j) is in
-    // TMEM.  dP_{j+2} takes dS_j's buffer only after dQ_j, issued before it
-    // by this thread, has read it.
+    // [128,256) for even key tiles and [384,512) for odd ones (key tiles
+    // counted over the CTA's items).  Per key tile j: S_{j+1} as soon as the
+    // elementwise warps have read S_j (s_read), then dP_{j+1} into the other
+    // buffer, so both run while they finish tile j; then dQ += dS_j K_j once
+    // dS_j (bf16, written over dP_j) is in TMEM.  dP_{j+2} takes dS_j's
+    // buffer only after dQ_j, issued before it by this thread, has read it.
+    // An item's S_0 and dP_0 are issued while the elementwise warps still
+    // store the previous item's dQ; its first dQ product waits for them to
+    // have read it (dq_free).
     const uint32_t q_base = smem_u32(sQ), do_base = smem_u32(sDO);
     const uint32_t k_ring = smem_u32(sK), v_ring = smem_u32(sV);
-    auto issue_dp = [&](int j) -> bool {
-      const int sv = j % SV;
-      if (!mbar_wait_warp(&v_full[sv], (j / SV) & 1, abort_flag, p.status)) return false;
+    auto issue_s = [&](int g) -> bool {
+      const int sk = g % SK;
+      if (!mbar_wait_warp(&k_full[sk], (g / SK) & 1, abort_flag, p.status)) return false;
       tc_fence_after();
-      mma_tile_ss<D>(tmem + ((j & 1) ? 384 : 128), do_base, v_ring + sv * L::kTileBytes);
+      mma_tile_ss<D>(tmem, q_base, k_ring + sk * L::kTileBytes);
+      mma_commit_elect(s_full);
+      return true;
+    };
+    auto issue_dp = [&](int g) -> bool {
+      const int sv = g % SV;
+      if (!mbar_wait_warp(&v_full[sv], (g / SV) & 1, abort_flag, p.status)) return false;
+      tc_fence_after();
+      mma_tile_ss<D>(tmem + ((g & 1) ? 384 : 128), do_base, v_ring + sv * L::kTileBytes);
       mma_commit_elect(dp_full);
       mma_commit_elect(&v_empty[sv]);
       return true;
     };
-    bool ok = mbar_wait_warp(in_full, 0, abort_flag, p.status) &&
-              mbar_wait_warp(&k_full[0], 0, abort_flag, p.status);
-    if (ok) {
+    bool ok = true;
+    int g0 = 0;  // key tiles of the earlier items
+    for (int m = 0; ok; ++m) {
+      BwdItem it;
+      float unused0, unused1;
+      if (!take(m, it, -1, unused0, unused1) || !it.valid) break;
+      const int n_kv = CAUSAL ? it.tile + 1 : (it.len + 127) / 128;
       tc_fence_after();
-      mma_tile_ss<D>(tmem, q_base, k_ring);
-      mma_commit_elect(s_full);
-      ok = issue_dp(0);
-    }
-    for (int j = 0; ok && j < n_kv; ++j) {
-      const int sk = j % SK;
-      if (j + 1 < n_kv) {
-        const int sk1 = (j + 1) % SK;
-        ok = mbar_wait_warp(s_read, j & 1, abort_flag, p.status) &&
-             mbar_wait_warp(&k_full[sk1], ((j + 1) / SK) & 1, abort_flag, p.status);
-        if (!ok) break;
+      ok = issue_s(g0) && issue_dp(g0);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int g = g0 + j;
+        if (j + 1 < n_kv) {
+          ok = mbar_wait_warp(s_read, g & 1, abort_flag, p.status) && issue_s(g + 1) &&
+               issue_dp(g + 1);
+          if (!ok) break;
+        } else {
+          mma_commit_elect(qdo_empty);  // the item's last S and dP read Q and dO
+        }
+        if (!mbar_wait_warp(p_full, g & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        if (j == 0 && m > 0 && !mbar_wait_warp(dq_free, (m - 1) & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        mma_tile_ss<D>(tmem, q_base, k_ring + sk1 * L::kTileBytes);
-        mma_commit_elect(s_full);
-        if (!issue_dp(j + 1)) break;
+        mma_tile_ts<D>(tmem + 256, tmem + ((g & 1) ? 384 : 128), k_ring + (g % SK) * L::kTileBytes,
+                       j > 0);
+        mma_commit_elect(&k_empty[g % SK]);
       }
-      if (!mbar_wait_warp(p_full, j & 1, abort_flag, p.status)) break;
-      tc_fence_after();
-      mma_tile_ts<D>(tmem + 256, tmem + ((j & 1) ? 384 : 128), k_ring + sk * L::kTileBytes, j > 0);
-      mma_commit_elect(&k_empty[sk]);
+      if (!ok) break;
+      mma_commit_elect(dq_done);
+      g0 += n_kv;
     }
-    mma_commit_elect(dq_done);
     mma_commit_elect(drain);
     mbar_drain(drain, 0, p.status);
   } else {
     // ------------------------------------------------------------ elementwise
     const int quad = warp & 3, hf = warp >> 2;  // TMEM lane group, column half
     const int row = quad * 32 + lane;
-    const int qi = t * 128 + row;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem + lane_off, tQ = tmem + 256 + lane_off;
-    const size_t vec = (static_cast<size_t>(b) * p.H + h) * p.Npad + min(qi, p.Npad - 1);
-    const size_t n_vec = static_cast<size_t>(p.B) * p.H * p.Npad;
-    const float nlse2 = checked_load(p.nlse2, vec, n_vec, p.status);  // -lse (log2 units)
-    const float ndsum = checked_load(p.ndsum, vec, n_vec, p.status);  // -D
     const float sl2 = p.scale_log2;
     const float2 sl2x2 = make_float2(sl2, sl2);
-    const float2 nl2 = make_float2(nlse2, nlse2), nd2 = make_float2(ndsum, ndsum);
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      ok = mbar_wait(s_full, j & 1, abort_flag, p.status);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      // keys [0, nvis) of this tile are visible to the row (keys past the
-      // sequence, of the next sequence in a packed batch, are not)
-      const int nvis = min(128, (CAUSAL ? min(len, qi + 1) : len) - j * 128);
-      // P = exp(S * scale - lse) of this half's 64 keys, kept as bf16 pairs
-      // (the values the dQ product uses through dS)
-      // (packed pairs; the mask is applied only in chunks that reach past nvis)
-      uint32_t pp[32];
+    int g0 = 0;
+    for (int m = 0; ok; ++m) {
+      BwdItem it;
+      float nlse2 = 0.f, ndsum = 0.f;  // -lse (log2 units) and -D of the row
+      if (!take(m, it, row, nlse2, ndsum) || !it.valid) break;
+      const int qi = it.tile * 128 + row;
+      const int len = it.len;
+      const int n_kv = CAUSAL ? it.tile + 1 : (len + 127) / 128;
+      const float2 nl2 = make_float2(nlse2, nlse2), nd2 = make_float2(ndsum, ndsum);
+      for (int j = 0; j < n_kv; ++j) {
+        const int g = g0 + j;
+        ok = mbar_wait(s_full, g & 1, abort_flag, p.status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        // keys [0, nvis) of this tile are visible to the row (keys past the
+        // sequence, of the next sequence in a packed batch, are not)
+        const int nvis = min(128, (CAUSAL ? min(len, qi + 1) : len) - j * 128);
+        // P = exp(S * scale - lse) of this half's 64 keys, kept as bf16 pairs
+        // (the values the dQ product uses through dS)
+        // (packed pairs; the mask is applied only in chunks that reach past nvis)
+        uint32_t pp[32];
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c = 2 * hf + cc;
-        uint32_t sv[32];
-        tmem_ld32_wait(tS + c * 32, sv);
-        const bool part = c * 32 + 32 > nvis;
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * hf + cc;
+          uint32_t sv[32];
+          tmem_ld32_wait(tS + c * 32, sv);
+          const bool part = c * 32 + 32 > nvis;
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float2 x =
-              ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sl2x2, nl2);
-          float w0 = ex2(x.x), w1 = ex2(x.y);
-          if (part) {
-            w0 = (c * 32 + e < nvis) ? w0 : 0.f;
-            w1 = (c * 32 + e + 1 < nvis) ? w1 : 0.f;
+          for (int e = 0; e < 32; e += 2) {
+            const float2 x =
+                ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sl2x2, nl2);
+            float w0 = ex2(x.x), w1 = ex2(x.y);
+            if (part) {
+              w0 = (c * 32 + e < nvis) ? w0 : 0.f;
+              w1 = (c * 32 + e + 1 < nvis) ? w1 : 0.f;
+            }
+            pp[cc * 16 + (e >> 1)] = pack_bf16x2(w0, w1);
           }
-          pp[cc * 16 + (e >> 1)] = pack_bf16x2(w0, w1);
         }
+        tc_fence_before();
+        mbar_arrive(s_read);
+        ok = mbar_wait(dp_full, g & 1, abort_flag, p.status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        // dS = P (dP - D), written over this half's dP columns (dP_j in the
+        // buffer of key tile j's parity)
+        const uint32_t tP = tmem + ((g & 1) ? 384 : 128) + lane_off;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * hf + cc;
+          uint32_t dp[32], pk[16];
+          tmem_ld32_wait(tP + c * 32, dp);
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 w = bf16x2_to_float2(pp[cc * 16 + (e >> 1)]);
+            const float2 r = fmul2(
+                w, fadd2(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd2));
+            pk[e >> 1] = pack_bf16x2(r.x, r.y);
+          }
+          tmem_st16(tP + hf * 64 + cc * 16, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_full);
       }
-      tc_fence_before();
-      mbar_arrive(s_read);
-      ok = mbar_wait(dp_full, j & 1, abort_flag, p.status);
+      if (!ok) break;
+      ok = mbar_wait(dq_done, m & 1, abort_flag, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      // dS = P (dP - D), written over this half's dP columns (dP_j in the
-      // buffer of key tile j's parity)
-      const uint32_t tP = tmem + ((j & 1) ? 384 : 128) + lane_off;
+      // this half's dQ columns into registers, TMEM handed back, then the row
+      uint32_t o[D / 64][32];
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c = 2 * hf + cc;
-        uint32_t dp[32], pk[16];
-        tmem_ld32_wait(tP + c * 32, dp);
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float2 w = bf16x2_to_float2(pp[cc * 16 + (e >> 1)]);
-          const float2 r = fmul2(
-              w, fadd2(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd2));
-          pk[e >> 1] = pack_bf16x2(r.x, r.y);
-        }
-        tmem_st16(tP + hf * 64 + cc * 16, pk);
-      }
-      tmem_wait_st();
+      for (int c = 0; c < D / 64; ++c) tmem_ld32_wait(tQ + (hf * (D / 64) + c) * 32, o[c]);
       tc_fence_before();
-      mbar_arrive(p_full);
-    }
-    if (ok) {
-      ok = mbar_wait(dq_done, 0, abort_flag, p.status);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {
-      tc_fence_after();
-      const size_t grow = VARLEN ? static_cast<size_t>(start) + qi : static_cast<size_t>(b) * p.N + qi;
-      const size_t drow = (grow * p.H + h) * D;
+      mbar_arrive(dq_free);
+      const size_t grow =
+          VARLEN ? static_cast<size_t>(it.start) + qi : static_cast<size_t>(it.b) * p.N + qi;
+      const size_t drow = (grow * p.H + it.h) * D;
       const size_t rows = VARLEN ? static_cast<size_t>(p.total_tokens) : static_cast<size_t>(p.B) * p.N;
       uint16_t *dst = static_cast<uint16_t *>(p.dq) + drow;
       const bool row_ok = qi >= len || in_bounds(drow, D, rows * p.H * D, p.status);
+      if (qi < len && row_ok) {
 #pragma unroll
-      for (int c = hf * (D / 64); c < (hf + 1) * (D / 64); ++c) {
-        uint32_t o[32];
-        tmem_ld32_wait(tQ + c * 32, o);
-        if (qi < len && row_ok) store_row_scaled_bf16(dst + c * 32, o, p.scale);
+        for (int c = 0; c < D / 64; ++c) store_row_scaled_bf16(dst + (hf * (D / 64) + c) * 32, o[c], p.scale);
       }
+      g0 += n_kv;
     }
   }
   __syncwarp();
@@ -502,11 +736,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // heaviest key tiles first (causal: tile 0 sees every query tile)
   const int kvh = static_cast<int>(blockIdx.x % p.Hkv);
   const int rest = static_cast<int>(blockIdx.x / p.Hkv);
-  const int jt = rest % p.n_tiles;
-  const int b = rest / p.n_tiles;
+  int b, jt;
+  if (VARLEN && p.longest_first) {
+    b = longest_first_item<CAUSAL, true>(p, rest, jt);
+    if (b < 0) return;
+  } else {
+    jt = rest % p.n_tiles;
+    b = rest / p.n_tiles;
+  }
   // the sequence's rows: a packed batch's key tiles past its end leave at once
+  // (its bounds are reported by the preprocess)
   int start, len;
-  bwd_seq<VARLEN>(p, b, start, len, jt == 0 && kvh == 0 && threadIdx.x == 0);
+  bwd_seq<VARLEN>(p, b, start, len, false);
   const int n_tiles = VARLEN ? (len + 127) / 128 : p.n_tiles;
   if (jt >= n_tiles) return;
   const int row0 = VARLEN ? start : 0;  // first row of the sequence in the tensor maps
@@ -824,11 +1065,17 @@ static cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tdo,
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(dkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  const unsigned grid_kv = static_cast<unsigned>(p.B * p.Hkv * p.n_tiles);
+  // work items: every (sequence, 128-row tile); the longest-first order of a
+  // packed batch enumerates only real tiles, at most ceil(T / 128) + B
+  long long items = static_cast<long long>(p.B) * p.n_tiles;
+  if (VARLEN && p.longest_first)
+    items = std::min(items, (p.total_tokens + 127LL) / 128 + p.B);
+  const unsigned grid_kv = static_cast<unsigned>(items * p.Hkv);
   dkdv<<<grid_kv, kBwdThreads, L::kSmemAlloc, stream>>>(tq, tdo, tk, tv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const unsigned grid_q = static_cast<unsigned>(p.B * p.H * p.n_tiles);
+  // persistent: one CTA per SM at most
+  const unsigned grid_q = static_cast<unsigned>(std::min<long long>(items * p.H, p.num_ctas));
   dq<<<grid_q, kBwdThreads, BwdDqLayout<D>::kSmemAlloc, stream>>>(tq, tdo, tk, tv, p);
   return cudaGetLastError();
 }

@@ -492,10 +492,14 @@ int fa_fwd_fp8(const void *q, const void *k, const void *v, void *out, float *ls
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+// Backward workspace: -lse2 and -D vectors ([B, H, Npad] fp32 each), then a
+// 256-byte block holding the work counters of the persistent kernels.
+constexpr size_t kBwdCounterBytes = 256;
+
 size_t fa_bwd_workspace_size(int B, int H, int N) {
   if (B <= 0 || H <= 0 || N <= 0) return 0;
   const size_t npad = (static_cast<size_t>(N) + 127) / 128 * 128;
-  return 2 * static_cast<size_t>(B) * H * npad * sizeof(float);
+  return 2 * static_cast<size_t>(B) * H * npad * sizeof(float) + kBwdCounterBytes;
 }
 
 int fa_bwd(const void *q, const void *k, const void *v, const void *out, const float *lse,
@@ -535,6 +539,8 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *out, const f
   p.Npad = p.n_tiles * 128;
   p.nlse2 = static_cast<float *>(workspace);
   p.ndsum = p.nlse2 + static_cast<size_t>(B) * H * p.Npad;
+  p.work = reinterpret_cast<unsigned int *>(p.ndsum + static_cast<size_t>(B) * H * p.Npad);
+  p.num_ctas = std::max(1, sm_count());
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
@@ -594,6 +600,8 @@ int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *out, 
   p.Npad = p.n_tiles * 128;
   p.nlse2 = static_cast<float *>(workspace);
   p.ndsum = p.nlse2 + static_cast<size_t>(num_seqs) * H * p.Npad;
+  p.work = reinterpret_cast<unsigned int *>(p.ndsum + static_cast<size_t>(num_seqs) * H * p.Npad);
+  p.num_ctas = std::max(1, sm_count());
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
@@ -606,6 +614,7 @@ int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *out, 
   p.scale_log2 = scale * kLog2e;
   p.cu_seqlens = cu_seqlens;
   p.total_tokens = total_tokens;
+  p.longest_first = num_seqs <= kBwdOrderMaxSeqs;
   cudaError_t e = launch_bwd(tq, tdo, tk, tv, p, d, causal != 0,
                              reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;

@@ -110,6 +110,7 @@ struct PrefillParams {
 // ----------------------------------------------------------------- backward
 
 constexpr int kBwdThreads = 320;  // 8 elementwise warps + 1 MMA warp + 1 TMA warp
+constexpr int kBwdOrderMaxSeqs = 128;  // multiple of 32
 
 struct BwdParams {
   unsigned int *status;   // per-device sticky FA_DEV_* word
@@ -126,6 +127,11 @@ struct BwdParams {
   float scale_log2;       // scale * log2(e)
   const int32_t *cu_seqlens;  // packed batches only: sequence b is rows [cu[b], cu[b + 1])
   int total_tokens;           // packed batches only: T
+  int longest_first;          // packed batches of at most kBwdOrderMaxSeqs sequences: CTAs take
+                              // the tiles in longest-first order
+  unsigned int *work;         // workspace: work counters of the dQ [0] and dK/dV [1] kernels
+                              // (zeroed by the preprocess kernel)
+  int num_ctas;               // CTAs of a persistent kernel (the SM count)
 };
 
 // ------------------------------------------------------------------- decode

@@ -150,9 +150,10 @@ def test_bwd_host_validation(lib):
 def test_bwd_workspace_size():
     import exact_attention_33_gb300 as fa
     # two fp32 vectors (rowsums and rescaled lse) per (batch, head), N padded to 128
-    assert fa.fa_bwd_workspace_size(2, 32, 8192) == 2 * 2 * 32 * 8192 * 4
-    assert fa.fa_bwd_workspace_size(1, 1, 1) == 2 * 128 * 4
-    assert fa.fa_bwd_workspace_size(1, 4, 129) == 2 * 4 * 256 * 4
+    # -lse2 and -D vectors, then 256 bytes of work counters
+    assert fa.fa_bwd_workspace_size(2, 32, 8192) == 2 * 2 * 32 * 8192 * 4 + 256
+    assert fa.fa_bwd_workspace_size(1, 1, 1) == 2 * 128 * 4 + 256
+    assert fa.fa_bwd_workspace_size(1, 4, 129) == 2 * 4 * 256 * 4 + 256
     assert fa.fa_bwd_workspace_size(0, 4, 129) == 0
 
 
