@@ -60,9 +60,10 @@ struct BwdLayout {
   static constexpr int kVecQ = kDO + kStagesO * kTileBytes;  // -lse2 per Q stage
   static constexpr int kVecO = kVecQ + kStagesQ * 512;       // -D per dO stage
   static constexpr int kBar = kVecO + kStagesO * 512;
-  static constexpr int kNumBars = 1 + 2 * kStagesQ + 2 * kStagesO + 6;
+  static constexpr int kNumBars = 1 + 2 * kStagesQ + 2 * kStagesO + 9;
   static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kItem = kMisc + 16;  // the work item slot
+  static constexpr int kBytes = kItem + 32;
   // Room to align the base up to 1 KiB, as much as the 227 KiB limit leaves
   // at d = 128 (the dynamic shared memory of a kernel without static
   // shared memory starts 1 KiB aligned; the kernel checks).
@@ -130,19 +131,57 @@ __device__ __forceinline__ void mma_tile_ts(uint32_t d_t, uint32_t a_t, uint32_t
   __syncwarp();
 }
 
-// Converts a row of 128 fp32 TMEM columns into 64 columns of bf16 pairs is
-// done chunk by chunk in the callers; this packs 32 values.
-__device__ __forceinline__ void store_row_scaled_bf16(void *dst_row, const uint32_t (&o)[32],
-                                                      float mul) {
-  uint4 *dst = reinterpret_cast<uint4 *>(dst_row);
+// Writes one half (D / 2 columns) of the 128 rows of a tile as bf16 times
+// `mul`: lane l holds its row's half, fp32 from TMEM in v (32 columns per
+// v[c]).  Row by row (one row per lane) a warp's 16-byte stores would touch
+// 32 rows at once; instead the lanes of each group of NCH = D / 16 exchange
+// 16-byte chunks (an NCH x NCH transpose by xor butterflies), so that store
+// i of lane l writes chunk l % NCH of the group's row i and every store
+// instruction covers 32 / NCH whole half-rows.  `row_ptr` is this lane's
+// half-row, `row_step` the elements from one row to the next (the rows of a
+// tile are consecutive); a row whose lane has `row_ok` false is not written.
+template <int D>
+__device__ __forceinline__ void store_half_rows_bf16(uint16_t *row_ptr, size_t row_step,
+                                                     bool row_ok, const uint32_t (&v)[D / 64][32],
+                                                     float mul) {
+  constexpr int NCH = D / 16;
+  const int lane = threadIdx.x & 31;
+  uint32_t x[NCH][4];  // chunk c: columns [8c, 8c + 8) of the half
 #pragma unroll
-  for (int v4 = 0; v4 < 4; ++v4) {
-    uint4 w;
-    w.x = pack_bf16x2(__uint_as_float(o[v4 * 8 + 0]) * mul, __uint_as_float(o[v4 * 8 + 1]) * mul);
-    w.y = pack_bf16x2(__uint_as_float(o[v4 * 8 + 2]) * mul, __uint_as_float(o[v4 * 8 + 3]) * mul);
-    w.z = pack_bf16x2(__uint_as_float(o[v4 * 8 + 4]) * mul, __uint_as_float(o[v4 * 8 + 5]) * mul);
-    w.w = pack_bf16x2(__uint_as_float(o[v4 * 8 + 6]) * mul, __uint_as_float(o[v4 * 8 + 7]) * mul);
-    dst[v4] = w;
+  for (int c = 0; c < NCH; ++c)
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const int k = 8 * c + 2 * w;
+      x[c][w] = pack_bf16x2(__uint_as_float(v[k / 32][k % 32]) * mul,
+                            __uint_as_float(v[k / 32][k % 32 + 1]) * mul);
+    }
+  // after the stages lane (base + t) holds chunk t of row (base + c) in x[c]
+#pragma unroll
+  for (int sft = NCH / 2; sft > 0; sft >>= 1) {
+    const bool hi = (lane & sft) != 0;
+#pragma unroll
+    for (int c0 = 0; c0 < NCH; ++c0) {
+      if (c0 & sft) continue;
+      const int c1 = c0 | sft;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, hi ? x[c0][w] : x[c1][w], sft);
+        if (hi)
+          x[c0][w] = recv;
+        else
+          x[c1][w] = recv;
+      }
+    }
+  }
+  const unsigned ok_rows = __ballot_sync(0xffffffffu, row_ok);
+  const int sub = lane % NCH, base = lane - sub;
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) {
+    if ((ok_rows >> (base + i)) & 1u) {
+      uint16_t *dst = row_ptr + static_cast<ptrdiff_t>(base + i - lane) * static_cast<ptrdiff_t>(row_step) +
+                      sub * 8;
+      *reinterpret_cast<uint4 *>(dst) = make_uint4(x[i][0], x[i][1], x[i][2], x[i][3]);
+    }
   }
 }
 
@@ -705,12 +744,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           VARLEN ? static_cast<size_t>(it.start) + qi : static_cast<size_t>(it.b) * p.N + qi;
       const size_t drow = (grow * p.H + it.h) * D;
       const size_t rows = VARLEN ? static_cast<size_t>(p.total_tokens) : static_cast<size_t>(p.B) * p.N;
-      uint16_t *dst = static_cast<uint16_t *>(p.dq) + drow;
-      const bool row_ok = qi >= len || in_bounds(drow, D, rows * p.H * D, p.status);
-      if (qi < len && row_ok) {
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) store_row_scaled_bf16(dst + (hf * (D / 64) + c) * 32, o[c], p.scale);
-      }
+      const bool row_ok = qi < len && in_bounds(drow, D, rows * p.H * D, p.status);
+      store_half_rows_bf16<D>(static_cast<uint16_t *>(p.dq) + drow + hf * (D / 2),
+                              static_cast<size_t>(p.H) * D, row_ok, o, p.scale);
       g0 += n_kv;
     }
   }
@@ -724,6 +760,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ----------------------------------------------------------------------- dK dV
+// Persistent like the dQ kernel: one CTA per SM takes (key tile, KV head)
+// items from the call's second counter.  An item's K and V stay resident;
+// the Q and dO rings (with their vectors) and every barrier of the
+// iteration pipeline count iterations over all of the CTA's items, so the
+// next item's copies and its first S^T and dP^T overlap the previous item's
+// last products and its dV / dK epilogue.
 template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -733,27 +775,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   using L = BwdLayout<D>;
   constexpr int SQ = L::kStagesQ;
   constexpr int SO = L::kStagesO;
-  // heaviest key tiles first (causal: tile 0 sees every query tile)
-  const int kvh = static_cast<int>(blockIdx.x % p.Hkv);
-  const int rest = static_cast<int>(blockIdx.x / p.Hkv);
-  int b, jt;
-  if (VARLEN && p.longest_first) {
-    b = longest_first_item<CAUSAL, true>(p, rest, jt);
-    if (b < 0) return;
-  } else {
-    jt = rest % p.n_tiles;
-    b = rest / p.n_tiles;
-  }
-  // the sequence's rows: a packed batch's key tiles past its end leave at once
-  // (its bounds are reported by the preprocess)
-  int start, len;
-  bwd_seq<VARLEN>(p, b, start, len, false);
-  const int n_tiles = VARLEN ? (len + 127) / 128 : p.n_tiles;
-  if (jt >= n_tiles) return;
-  const int row0 = VARLEN ? start : 0;  // first row of the sequence in the tensor maps
-  const int bc = VARLEN ? 0 : b;        // the maps' outer coordinate
-  const int i0 = CAUSAL ? jt : 0;  // first query tile that sees a key of this tile
-  const int n_it = (n_tiles - i0) * p.group;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -764,7 +785,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     return;
   }
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBar);
-  uint64_t *in_full = bars;          // K and V of this key tile
+  uint64_t *in_full = bars;          // K and V of the item (and its slot)
   uint64_t *q_full = bars + 1;       // [SQ] Q and its -lse2 vector
   uint64_t *q_empty = q_full + SQ;
   uint64_t *o_full = q_empty + SQ;   // [SO] dO and its -D vector
@@ -773,10 +794,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t *dp_full = s_full + 1;
   uint64_t *pt_full = dp_full + 1;  // P^T (bf16) is in TMEM
   uint64_t *p_full = pt_full + 1;   // dS^T (bf16) is in TMEM
-  uint64_t *kv_done = p_full + 1;
+  uint64_t *kv_done = p_full + 1;   // the item's dV and dK are complete in TMEM
   uint64_t *drain = kv_done + 1;
+  uint64_t *kv_empty = drain + 1;   // the item's last products that read K and V are done
+  uint64_t *kv_free = kv_empty + 1;  // the elementwise warps have read the item's dV and dK
+  uint64_t *taken = kv_free + 1;    // the MMA and elementwise warps have read the slot
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
+  volatile BwdItem *slot = reinterpret_cast<volatile BwdItem *>(smem + L::kItem);
   uint8_t *sK = smem + L::kA;
   uint8_t *sV = smem + L::kB;
   uint8_t *sQr = smem + L::kQ;    // Q ring
@@ -802,6 +827,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(p_full, 256);
     mbar_init(kv_done, 1);
     mbar_init(drain, 1);
+    mbar_init(kv_empty, 1);
+    mbar_init(kv_free, 256);
+    mbar_init(taken, 9);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -815,55 +843,114 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // reads the slot of item m once its barrier phase is complete, then tells
+  // the producer (one arrival per warp)
+  auto take = [&](int m, BwdItem &it) -> bool {
+    bool ok = mbar_wait(in_full, m & 1, abort_flag, p.status);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) return false;
+    it.b = slot->b;
+    it.tile = slot->tile;
+    it.h = slot->h;
+    it.start = slot->start;
+    it.len = slot->len;
+    it.valid = slot->valid;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(taken);
+    return true;
+  };
+  // iterations of an item: its query tiles that see a key of the tile
+  // (from the key tile on, causal) times the query heads of the KV head;
+  // iteration it is query head kvh * group + it % group, query tile
+  // i0 + it / group
+  auto iterations = [&](const BwdItem &it) {
+    return ((it.len + 127) / 128 - (CAUSAL ? it.tile : 0)) * p.group;
+  };
+
   if (warp == 9) {
     // ------------------------------------------------------------ producer
-    // Iteration it: query head kvh * group + it % group, query tile
-    // i0 + it / group.
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_do);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(in_full, 2 * L::kTileBytes);
+    }
+    bool ok = true;
+    int gq = 0, go = 0;  // Q and dO stages issued so far
+    int last = -1;       // the last item whose K and V were issued
+    for (int m = 0;; ++m) {
+      const BwdItem it = claim_item<CAUSAL, VARLEN, true>(p, p.work + 1, p.Hkv);
+      if (lane == 0 && m > 0)
+        ok = mbar_wait(taken, (m - 1) & 1, abort_flag, p.status) &&
+             mbar_wait(kv_empty, (m - 1) & 1, abort_flag, p.status);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (lane == 0) {
+        slot->b = it.b;
+        slot->tile = it.tile;
+        slot->h = it.h;
+        slot->start = it.start;
+        slot->len = it.len;
+        slot->valid = it.valid;
+        if (it.valid) {
+          const int row0 = VARLEN ? it.start : 0, bc = VARLEN ? 0 : it.b;
+          mbar_arrive_expect_tx(in_full, 2 * L::kTileBytes);
 #pragma unroll
-      for (int c = 0; c < L::kChunks; ++c) {
-        tma_load_4d(sK + c * L::kChunkBytes, &tm_k, in_full, c * 64, kvh, row0 + jt * 128, bc);
-        tma_load_4d(sV + c * L::kChunkBytes, &tm_v, in_full, c * 64, kvh, row0 + jt * 128, bc);
+          for (int c = 0; c < L::kChunks; ++c) {
+            tma_load_4d(sK + c * L::kChunkBytes, &tm_k, in_full, c * 64, it.h, row0 + it.tile * 128, bc);
+            tma_load_4d(sV + c * L::kChunkBytes, &tm_v, in_full, c * 64, it.h, row0 + it.tile * 128, bc);
+          }
+        } else {
+          mbar_arrive(in_full);  // no work left: publishes the empty slot
+        }
       }
-      // Q(it) then dO(it) for every it; each waits for its own ring
-      int q_issued = 0, o_issued = 0;
-      for (int it = 0; it < n_it; ++it) {
-        const int hq = kvh * p.group + it % p.group;
-        const int i = i0 + it / p.group;
-        // (a checked build that finds the 128 entries outside the workspace
-        // copies entries 0..127 instead, so the barrier still gets its bytes)
-        size_t vec = (static_cast<size_t>(b) * p.H + hq) * p.Npad + i * 128;
-        if (!in_bounds(vec, 128, static_cast<size_t>(p.B) * p.H * p.Npad, p.status)) vec = 0;
-        const int sq = it % SQ, so = it % SO;
-        if (it >= SQ && !mbar_wait(&q_empty[sq], ((it / SQ) - 1) & 1, abort_flag, p.status))
-          break;
-        mbar_arrive_expect_tx(&q_full[sq], L::kTileBytes + 512);
+      if (!it.valid) break;
+      last = m;
+      if (lane == 0) {
+        const int row0 = VARLEN ? it.start : 0, bc = VARLEN ? 0 : it.b;
+        const int i0 = CAUSAL ? it.tile : 0;
+        const int n_it = iterations(it);
+        for (int x = 0; x < n_it; ++x) {
+          const int hq = it.h * p.group + x % p.group;
+          const int i = i0 + x / p.group;
+          // (a checked build that finds the 128 entries outside the workspace
+          // copies entries 0..127 instead, so the barrier still gets its bytes)
+          size_t vec = (static_cast<size_t>(it.b) * p.H + hq) * p.Npad + i * 128;
+          if (!in_bounds(vec, 128, static_cast<size_t>(p.B) * p.H * p.Npad, p.status)) vec = 0;
+          const int sq = gq % SQ, so = go % SO;
+          if (gq >= SQ && !mbar_wait(&q_empty[sq], ((gq / SQ) - 1) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&q_full[sq], L::kTileBytes + 512);
 #pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_4d(sQr + sq * L::kTileBytes + c * L::kChunkBytes, &tm_q, &q_full[sq], c * 64, hq,
-                      row0 + i * 128, bc);
-        bulk_load(sVq + 128 * sq, p.nlse2 + vec, 512, &q_full[sq]);
-        q_issued = it + 1;
-        if (it >= SO && !mbar_wait(&o_empty[so], ((it / SO) - 1) & 1, abort_flag, p.status))
-          break;
-        mbar_arrive_expect_tx(&o_full[so], L::kTileBytes + 512);
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_4d(sQr + sq * L::kTileBytes + c * L::kChunkBytes, &tm_q, &q_full[sq], c * 64, hq,
+                        row0 + i * 128, bc);
+          bulk_load(sVq + 128 * sq, p.nlse2 + vec, 512, &q_full[sq]);
+          ++gq;
+          if (go >= SO && !mbar_wait(&o_empty[so], ((go / SO) - 1) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&o_full[so], L::kTileBytes + 512);
 #pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_4d(sOr + so * L::kTileBytes + c * L::kChunkBytes, &tm_do, &o_full[so], c * 64,
-                      hq, row0 + i * 128, bc);
-        bulk_load(sVo + 128 * so, p.ndsum + vec, 512, &o_full[so]);
-        o_issued = it + 1;
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_4d(sOr + so * L::kTileBytes + c * L::kChunkBytes, &tm_do, &o_full[so], c * 64,
+                        hq, row0 + i * 128, bc);
+          bulk_load(sVo + 128 * so, p.ndsum + vec, 512, &o_full[so]);
+          ++go;
+        }
       }
-      mbar_drain(in_full, 0, p.status);
-      for (int it = max(0, q_issued - SQ); it < q_issued; ++it)
-        mbar_drain(&q_full[it % SQ], (it / SQ) & 1, p.status);
-      for (int it = max(0, o_issued - SO); it < o_issued; ++it)
-        mbar_drain(&o_full[it % SO], (it / SO) & 1, p.status);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+    }
+    if (!ok && lane == 0) {
+      // a wait ran out: let the copies still in flight land before the CTA
+      // leaves (K and V of the last item, Q and dO of the last stages issued)
+      if (last >= 0) mbar_drain(in_full, last & 1, p.status);
+      for (int x = max(0, gq - SQ); x < gq; ++x) mbar_drain(&q_full[x % SQ], (x / SQ) & 1, p.status);
+      for (int x = max(0, go - SO); x < go; ++x) mbar_drain(&o_full[x % SO], (x / SO) & 1, p.status);
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
@@ -871,169 +958,204 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // Per iteration: dV += P^T dO once P^T (bf16, over S^T) is in TMEM; then
     // S^T of the next iteration (issued after dV by this thread, so it
     // overwrites P^T only after dV has read it); dK += dS^T Q once dS^T
-    // (over dP^T) is in TMEM; then dP^T of the next iteration.
+    // (over dP^T) is in TMEM; then dP^T of the next iteration.  An item's
+    // first S^T and dP^T are issued while the elementwise warps still store
+    // the previous item's dV and dK; its first dV product waits for them to
+    // have read both (kv_free).
     const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV);
-    auto q_at = [&](int it) { return smem_u32(sQr + (it % SQ) * L::kTileBytes); };
-    auto do_at = [&](int it) { return smem_u32(sOr + (it % SO) * L::kTileBytes); };
-    bool ok = mbar_wait_warp(in_full, 0, abort_flag, p.status) &&
-              mbar_wait_warp(&q_full[0], 0, abort_flag, p.status) &&
-              mbar_wait_warp(&o_full[0], 0, abort_flag, p.status);
-    if (ok) {
+    auto q_at = [&](int g) { return smem_u32(sQr + (g % SQ) * L::kTileBytes); };
+    auto do_at = [&](int g) { return smem_u32(sOr + (g % SO) * L::kTileBytes); };
+    bool ok = true;
+    int g0 = 0;  // iterations of the earlier items
+    for (int m = 0; ok; ++m) {
+      BwdItem it;
+      if (!take(m, it) || !it.valid) break;
+      const int n_it = iterations(it);
+      ok = mbar_wait_warp(&q_full[g0 % SQ], (g0 / SQ) & 1, abort_flag, p.status) &&
+           mbar_wait_warp(&o_full[g0 % SO], (g0 / SO) & 1, abort_flag, p.status);
+      if (!ok) break;
       tc_fence_after();
-      mma_tile_ss<D>(tmem, k_base, q_at(0));
+      mma_tile_ss<D>(tmem, k_base, q_at(g0));
       mma_commit_elect(s_full);
-      mma_tile_ss<D>(tmem + 128, v_base, do_at(0));
+      mma_tile_ss<D>(tmem + 128, v_base, do_at(g0));
       mma_commit_elect(dp_full);
-    }
-    for (int it = 0; ok && it < n_it; ++it) {
-      if (!mbar_wait_warp(pt_full, it & 1, abort_flag, p.status)) break;
-      tc_fence_after();
-      mma_tile_ts<D>(tmem + 256, tmem, do_at(it), it > 0);
-      if (it + 1 < n_it) {
-        if (!mbar_wait_warp(&q_full[(it + 1) % SQ], ((it + 1) / SQ) & 1, abort_flag, p.status))
+      if (n_it == 1) mma_commit_elect(kv_empty);  // the item's last S^T and dP^T read K and V
+      for (int x = 0; x < n_it; ++x) {
+        const int g = g0 + x;
+        if (!mbar_wait_warp(pt_full, g & 1, abort_flag, p.status)) {
+          ok = false;
           break;
-        tc_fence_after();
-        mma_tile_ss<D>(tmem, k_base, q_at(it + 1));
-        mma_commit_elect(s_full);
-      }
-      if (!mbar_wait_warp(p_full, it & 1, abort_flag, p.status)) break;
-      tc_fence_after();
-      mma_tile_ts<D>(tmem + 256 + D, tmem + 128, q_at(it), it > 0);
-      // Q(it) was last read by dK(it); the dO stage is released here too,
-      // because the elementwise warps read its -D vector until dS^T(it) is
-      // handed over (which dK(it) waited for)
-      mma_commit_elect(&q_empty[it % SQ]);
-      mma_commit_elect(&o_empty[it % SO]);
-      if (it + 1 < n_it) {
-        if (!mbar_wait_warp(&o_full[(it + 1) % SO], ((it + 1) / SO) & 1, abort_flag, p.status))
+        }
+        if (x == 0 && m > 0 && !mbar_wait_warp(kv_free, (m - 1) & 1, abort_flag, p.status)) {
+          ok = false;
           break;
+        }
         tc_fence_after();
-        mma_tile_ss<D>(tmem + 128, v_base, do_at(it + 1));
-        mma_commit_elect(dp_full);
+        mma_tile_ts<D>(tmem + 256, tmem, do_at(g), x > 0);
+        if (x + 1 < n_it) {
+          if (!mbar_wait_warp(&q_full[(g + 1) % SQ], ((g + 1) / SQ) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_tile_ss<D>(tmem, k_base, q_at(g + 1));
+          mma_commit_elect(s_full);
+        }
+        if (!mbar_wait_warp(p_full, g & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        mma_tile_ts<D>(tmem + 256 + D, tmem + 128, q_at(g), x > 0);
+        // Q(g) was last read by dK(g); the dO stage is released here too,
+        // because the elementwise warps read its -D vector until dS^T(g) is
+        // handed over (which dK(g) waited for)
+        mma_commit_elect(&q_empty[g % SQ]);
+        mma_commit_elect(&o_empty[g % SO]);
+        if (x + 1 < n_it) {
+          if (!mbar_wait_warp(&o_full[(g + 1) % SO], ((g + 1) / SO) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_tile_ss<D>(tmem + 128, v_base, do_at(g + 1));
+          mma_commit_elect(dp_full);
+          if (x + 2 == n_it) mma_commit_elect(kv_empty);
+        }
       }
+      if (!ok) break;
+      mma_commit_elect(kv_done);
+      g0 += n_it;
     }
-    mma_commit_elect(kv_done);
     mma_commit_elect(drain);
     mbar_drain(drain, 0, p.status);
   } else {
     // ------------------------------------------------------------ elementwise
     const int quad = warp & 3, hf = warp >> 2;  // TMEM lane group, column half
     const int row = quad * 32 + lane;   // key row of the tile
-    const int kj = jt * 128 + row;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem + lane_off, tP = tmem + 128 + lane_off;
     const uint32_t tV = tmem + 256 + lane_off, tK = tmem + 256 + D + lane_off;
     const float sl2 = p.scale_log2;
     const float2 sl2x2 = make_float2(sl2, sl2);
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int i = i0 + it / p.group;
-      // the stages' vectors arrived with their tiles (async copies): observe
-      // those barriers too before reading them
-      ok = mbar_wait(&q_full[it % SQ], (it / SQ) & 1, abort_flag, p.status) &&
-           mbar_wait(s_full, it & 1, abort_flag, p.status);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      const float *vl = sVq + 128 * (it % SQ);  // -log-sum-exp (log2 units) of the 128 queries
-      const float *vd = sVo + 128 * (it % SO);  // -D of the 128 queries (read after o_full)
-      // queries [qfirst, 128) of this tile see the key (causal); earlier
-      // ones do not.  Queries past N carry -lse2 = -inf, so their weight is 0.
-      const int qfirst = CAUSAL ? max(0, kj - i * 128) : 0;
-      // P^T = exp(S^T * scale - lse[q]) of this half's 64 queries as bf16
-      // pairs, stored over S^T (packed pairs; the mask is applied only in
-      // chunks that start before qfirst)
-      uint32_t pp[32];
+    int g0 = 0;
+    for (int m = 0; ok; ++m) {
+      BwdItem itm;
+      if (!take(m, itm) || !itm.valid) break;
+      const int kj = itm.tile * 128 + row;
+      const int len = itm.len;
+      const int i0 = CAUSAL ? itm.tile : 0;
+      const int n_it = iterations(itm);
+      for (int x = 0; x < n_it; ++x) {
+        const int g = g0 + x;
+        const int i = i0 + x / p.group;
+        // the stages' vectors arrived with their tiles (async copies): observe
+        // those barriers too before reading them
+        ok = mbar_wait(&q_full[g % SQ], (g / SQ) & 1, abort_flag, p.status) &&
+             mbar_wait(s_full, g & 1, abort_flag, p.status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const float *vl = sVq + 128 * (g % SQ);  // -log-sum-exp (log2 units) of the 128 queries
+        const float *vd = sVo + 128 * (g % SO);  // -D of the 128 queries (read after o_full)
+        // queries [qfirst, 128) of this tile see the key (causal); earlier
+        // ones do not.  Queries past the sequence carry -lse2 = -inf, so
+        // their weight is 0.
+        const int qfirst = CAUSAL ? max(0, kj - i * 128) : 0;
+        // P^T = exp(S^T * scale - lse[q]) of this half's 64 queries as bf16
+        // pairs, stored over S^T (packed pairs; the mask is applied only in
+        // chunks that start before qfirst)
+        uint32_t pp[32];
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c = 2 * hf + cc;
-        uint32_t sv[32];
-        tmem_ld32_wait(tS + c * 32, sv);
-        const bool part = c * 32 < qfirst;
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * hf + cc;
+          uint32_t sv[32];
+          tmem_ld32_wait(tS + c * 32, sv);
+          const bool part = c * 32 < qfirst;
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const int q0 = c * 32 + e;
-          const float4 l4 = *reinterpret_cast<const float4 *>(vl + q0);
-          const float2 x0 = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
-                                  sl2x2, make_float2(l4.x, l4.y));
-          const float2 x1 = ffma2(make_float2(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])),
-                                  sl2x2, make_float2(l4.z, l4.w));
-          float w0 = ex2(x0.x), w1 = ex2(x0.y), w2 = ex2(x1.x), w3 = ex2(x1.y);
-          if (part) {
-            w0 = (q0 >= qfirst) ? w0 : 0.f;
-            w1 = (q0 + 1 >= qfirst) ? w1 : 0.f;
-            w2 = (q0 + 2 >= qfirst) ? w2 : 0.f;
-            w3 = (q0 + 3 >= qfirst) ? w3 : 0.f;
+          for (int e = 0; e < 32; e += 4) {
+            const int q0 = c * 32 + e;
+            const float4 l4 = *reinterpret_cast<const float4 *>(vl + q0);
+            const float2 x0 = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                    sl2x2, make_float2(l4.x, l4.y));
+            const float2 x1 = ffma2(make_float2(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])),
+                                    sl2x2, make_float2(l4.z, l4.w));
+            float w0 = ex2(x0.x), w1 = ex2(x0.y), w2 = ex2(x1.x), w3 = ex2(x1.y);
+            if (part) {
+              w0 = (q0 >= qfirst) ? w0 : 0.f;
+              w1 = (q0 + 1 >= qfirst) ? w1 : 0.f;
+              w2 = (q0 + 2 >= qfirst) ? w2 : 0.f;
+              w3 = (q0 + 3 >= qfirst) ? w3 : 0.f;
+            }
+            pp[cc * 16 + (e >> 1)] = pack_bf16x2(w0, w1);
+            pp[cc * 16 + (e >> 1) + 1] = pack_bf16x2(w2, w3);
           }
-          pp[cc * 16 + (e >> 1)] = pack_bf16x2(w0, w1);
-          pp[cc * 16 + (e >> 1) + 1] = pack_bf16x2(w2, w3);
-        }
-        uint32_t chunk[16];
+          uint32_t chunk[16];
 #pragma unroll
-        for (int t2 = 0; t2 < 16; ++t2) chunk[t2] = pp[cc * 16 + t2];
-        tmem_st16(tS + hf * 64 + cc * 16, chunk);
+          for (int t2 = 0; t2 < 16; ++t2) chunk[t2] = pp[cc * 16 + t2];
+          tmem_st16(tS + hf * 64 + cc * 16, chunk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(pt_full);
+        ok = mbar_wait(&o_full[g % SO], (g / SO) & 1, abort_flag, p.status) &&
+             mbar_wait(dp_full, g & 1, abort_flag, p.status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        // dS^T = P^T (dP^T - D[q]), stored over this half's dP^T columns
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * hf + cc;
+          uint32_t dp[32], pd[16];
+          tmem_ld32_wait(tP + c * 32, dp);
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const int q0 = c * 32 + e;
+            const float4 d4 = *reinterpret_cast<const float4 *>(vd + q0);
+            const float2 wa = bf16x2_to_float2(pp[cc * 16 + (e >> 1)]);
+            const float2 wb = bf16x2_to_float2(pp[cc * 16 + (e >> 1) + 1]);
+            const float2 ra = fmul2(
+                wa, fadd2(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
+                          make_float2(d4.x, d4.y)));
+            const float2 rb = fmul2(
+                wb, fadd2(make_float2(__uint_as_float(dp[e + 2]), __uint_as_float(dp[e + 3])),
+                          make_float2(d4.z, d4.w)));
+            pd[e >> 1] = pack_bf16x2(ra.x, ra.y);
+            pd[(e >> 1) + 1] = pack_bf16x2(rb.x, rb.y);
+          }
+          tmem_st16(tP + hf * 64 + cc * 16, pd);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_full);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(pt_full);
-      ok = mbar_wait(&o_full[it % SO], (it / SO) & 1, abort_flag, p.status) &&
-           mbar_wait(dp_full, it & 1, abort_flag, p.status);
+      if (!ok) break;
+      ok = mbar_wait(kv_done, m & 1, abort_flag, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      tc_fence_after();
-      // dS^T = P^T (dP^T - D[q]), stored over this half's dP^T columns
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c = 2 * hf + cc;
-        uint32_t dp[32], pd[16];
-        tmem_ld32_wait(tP + c * 32, dp);
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const int q0 = c * 32 + e;
-          const float4 d4 = *reinterpret_cast<const float4 *>(vd + q0);
-          const float2 wa = bf16x2_to_float2(pp[cc * 16 + (e >> 1)]);
-          const float2 wb = bf16x2_to_float2(pp[cc * 16 + (e >> 1) + 1]);
-          const float2 ra = fmul2(
-              wa, fadd2(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
-                        make_float2(d4.x, d4.y)));
-          const float2 rb = fmul2(
-              wb, fadd2(make_float2(__uint_as_float(dp[e + 2]), __uint_as_float(dp[e + 3])),
-                        make_float2(d4.z, d4.w)));
-          pd[e >> 1] = pack_bf16x2(ra.x, ra.y);
-          pd[(e >> 1) + 1] = pack_bf16x2(rb.x, rb.y);
-        }
-        tmem_st16(tP + hf * 64 + cc * 16, pd);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(p_full);
-    }
-    if (ok) {
-      ok = mbar_wait(kv_done, 0, abort_flag, p.status);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {
       tc_fence_after();
       // key rows past the sequence (the next sequence's, in a packed batch)
-      // are not written
-      const size_t grow = VARLEN ? static_cast<size_t>(start) + kj : static_cast<size_t>(b) * p.N + kj;
-      const size_t orow = (grow * p.Hkv + kvh) * D;
+      // are not written; dV, then dK (TMEM handed back once both are read)
+      const size_t grow =
+          VARLEN ? static_cast<size_t>(itm.start) + kj : static_cast<size_t>(itm.b) * p.N + kj;
+      const size_t orow = (grow * p.Hkv + itm.h) * D;
       const size_t rows = VARLEN ? static_cast<size_t>(p.total_tokens) : static_cast<size_t>(p.B) * p.N;
-      uint16_t *dv = static_cast<uint16_t *>(p.dv) + orow;
-      uint16_t *dk = static_cast<uint16_t *>(p.dk) + orow;
-      const bool row_ok = kj >= len || in_bounds(orow, D, rows * p.Hkv * D, p.status);
+      const bool row_ok = kj < len && in_bounds(orow, D, rows * p.Hkv * D, p.status);
+      const size_t step = static_cast<size_t>(p.Hkv) * D;
+      uint32_t o[D / 64][32];
 #pragma unroll
-      for (int c = hf * (D / 64); c < (hf + 1) * (D / 64); ++c) {
-        uint32_t o[32];
-        tmem_ld32_wait(tV + c * 32, o);
-        if (kj < len && row_ok) store_row_scaled_bf16(dv + c * 32, o, 1.f);
-      }
+      for (int c = 0; c < D / 64; ++c) tmem_ld32_wait(tV + (hf * (D / 64) + c) * 32, o[c]);
+      store_half_rows_bf16<D>(static_cast<uint16_t *>(p.dv) + orow + hf * (D / 2), step, row_ok, o,
+                              1.f);
 #pragma unroll
-      for (int c = hf * (D / 64); c < (hf + 1) * (D / 64); ++c) {
-        uint32_t o[32];
-        tmem_ld32_wait(tK + c * 32, o);
-        if (kj < len && row_ok) store_row_scaled_bf16(dk + c * 32, o, p.scale);
-      }
+      for (int c = 0; c < D / 64; ++c) tmem_ld32_wait(tK + (hf * (D / 64) + c) * 32, o[c]);
+      tc_fence_before();
+      mbar_arrive(kv_free);
+      store_half_rows_bf16<D>(static_cast<uint16_t *>(p.dk) + orow + hf * (D / 2), step, row_ok, o,
+                              p.scale);
+      g0 += n_it;
     }
   }
   __syncwarp();
@@ -1070,7 +1192,7 @@ static cudaError_t launch_bwd_d(const CUtensorMap &tq, const CUtensorMap &tdo,
   long long items = static_cast<long long>(p.B) * p.n_tiles;
   if (VARLEN && p.longest_first)
     items = std::min(items, (p.total_tokens + 127LL) / 128 + p.B);
-  const unsigned grid_kv = static_cast<unsigned>(items * p.Hkv);
+  const unsigned grid_kv = static_cast<unsigned>(std::min<long long>(items * p.Hkv, p.num_ctas));
   dkdv<<<grid_kv, kBwdThreads, L::kSmemAlloc, stream>>>(tq, tdo, tk, tv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
