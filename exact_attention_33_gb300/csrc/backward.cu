@@ -30,6 +30,7 @@
 #include <math_constants.h>
 #include <stdint.h>
 
+#include "bwd_internal.h"
 #include "fa_internal.h"
 #include "ptx.cuh"
 #include "checks.cuh"

@@ -16,6 +16,7 @@
 #include <mutex>
 
 #include "../../include/fa.h"
+#include "bwd_internal.h"
 #include "fa_internal.h"
 #include "ptx.cuh"
 
@@ -32,8 +33,9 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUte
                        const CUtensorMap &tv, const BwdParams &p, int d, bool causal,
                        cudaStream_t stream);
 cudaError_t launch_prefill_fp8(const CUtensorMap &tq, const CUtensorMap &tk,
-                               const CUtensorMap &tv, const PrefillParams &p, bool causal,
-                               int grid, cudaStream_t stream, int kind, int d);
+                               const CUtensorMap &tv, const CUtensorMap &to,
+                               const PrefillParams &p, bool causal, int grid,
+                               cudaStream_t stream, int kind, int d);
 cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
                           int d, cudaStream_t stream);
 cudaError_t launch_call_status(CallStatus *call, unsigned int *dev, cudaStream_t stream);
@@ -427,7 +429,8 @@ static int fwd_varlen(const void *q, const void *k, const void *v, void *out, fl
   p.prefetch_ahead = std::max(0, sm_count()) * (qtiles == 1 ? 2 : 1);  // CTAs resident at once
   const int kind = layout == kHeadPairs ? kKindVarlenHeads : kKindVarlen;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = fp8 ? launch_prefill_fp8(tq, tk, tv, p, causal != 0, static_cast<int>(grid), st, kind, d)
+  cudaError_t e = fp8 ? launch_prefill_fp8(tq, tk, tv, to, p, causal != 0, static_cast<int>(grid), st,
+                                           kind, d)
                       : launch_prefill(tq, tk, tv, tv, to, p, d, causal != 0, kind,
                                        static_cast<int>(grid), st, qtiles);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -466,10 +469,11 @@ int fa_fwd_fp8(const void *q, const void *k, const void *v, void *out, float *ls
   const long long grid = pairs * B * H;
   if (grid > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(N) * H * d >= (1LL << 40)) return FA_ERR_UNSUPPORTED;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   int rc = make_map(&tq, q, d, H, N, B, kPrefillBM, 1, fp8_swz(d));
   if (rc == FA_OK) rc = make_map(&tk, k, d, Hkv, N, B, kPrefillBN, 1, fp8_swz(d));
   if (rc == FA_OK) rc = make_map(&tv, v, d, Hkv, N, B, kPrefillBN, 1, fp8_swz(d));
+  if (rc == FA_OK) rc = make_map(&to, out, d, H, N, B, kPrefillBM);
   if (rc != FA_OK) return rc;
   PrefillParams p{};
   p.status = status_ptr();
@@ -487,7 +491,7 @@ int fa_fwd_fp8(const void *q, const void *k, const void *v, void *out, float *ls
   p.v_descale = v_descale;
   p.causal = causal;
   p.prefetch_ahead = std::max(0, sm_count());
-  cudaError_t e = launch_prefill_fp8(tq, tk, tv, p, causal != 0, static_cast<int>(grid),
+  cudaError_t e = launch_prefill_fp8(tq, tk, tv, to, p, causal != 0, static_cast<int>(grid),
                                      reinterpret_cast<cudaStream_t>(stream), kKindDense, d);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

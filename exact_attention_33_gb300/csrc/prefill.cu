@@ -936,22 +936,31 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
         // A whole bf16 tile goes out through shared memory and one TMA store
         // per 64-column chunk (rows past the end of a dense sequence are
         // clipped by the tensor bounds).  The warpgroup's Q tile is free: its
-        // last S MMA completed before the last S tile was handed over.  A
-        // partial tile of a packed layout, whose tail rows belong to the next
-        // sequence, is written row by row instead.
+        // last S MMA completed before the last S tile was handed over.  An
+        // fp8 Q tile holds half of the bf16 output tile at d = 128, so the
+        // tile leaves in two passes of 64 columns; at d = 64 (a quarter) and
+        // for a partial tile of a packed layout, whose tail rows belong to
+        // the next sequence, the rows are written one by one instead.
+        constexpr int kOutChunkBytes = 128 * 128;  // 128 rows x 64 bf16 columns
+        constexpr int kPasses = FP8 ? 2 : 1;
+        constexpr int kPassCols = D / 32 / kPasses;  // 32-column TMEM chunks per pass
         const bool tma_out =
-            !FP8 && (DENSE || tile_row(i) + kPrefillBM <= len);
+            (!FP8 || D == 128) && (DENSE || tile_row(i) + kPrefillBM <= len);
         if (tma_out) {
-          // All four warps of the tile meet at the barrier below (my_end and
+          // All four warps of the tile meet at the barriers below (my_end and
           // tma_out are the same for the whole tile); a warp whose wait gave
           // up writes nothing, and the status word already marks the call as
           // failed.
           uint8_t *stile = sQ + i * L::kTileBytes;
+          static_assert(kPassCols / 2 * kOutChunkBytes <= L::kTileBytes, "output staging tile");
 #pragma unroll
-          for (int c = 0; ok && c < D / 32; ++c) {
+          for (int pass = 0; pass < kPasses; ++pass) {
+#pragma unroll
+          for (int cc = 0; ok && cc < kPassCols; ++cc) {
+            const int c = pass * kPassCols + cc;
             uint32_t o[32];
             tmem_ld32_wait(tO + c * 32, o);
-            uint8_t *srow = stile + (c >> 1) * L::kChunkBytes + row * 128;
+            uint8_t *srow = stile + (cc >> 1) * kOutChunkBytes + row * 128;
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4) {
               uint4 w;
@@ -973,10 +982,14 @@ __global__ void __launch_bounds__(PrefillShape<QT>::kThreads, PrefillShape<QT>::
           if (row == 0 && ok) {
             const int orow = (DENSE ? 0 : seq_start) + tile_row(i);
 #pragma unroll
-            for (int c = 0; c < L::kChunks; ++c)
-              tma_store_4d(&tm_o, stile + c * L::kChunkBytes, c * L::kChunkElems, hi, orow, b);
+            for (int c = 0; c < kPassCols / 2; ++c)
+              tma_store_4d(&tm_o, stile + c * kOutChunkBytes, (pass * kPassCols / 2 + c) * 64, hi,
+                           orow, b);
             tma_store_commit();
             tma_store_wait_read();
+          }
+          // the next pass reuses the staging tile once the copies have read it
+          if (pass + 1 < kPasses) named_bar_sync(1 + i, 128);
           }
         }
         size_t out_row;
@@ -1186,31 +1199,34 @@ static cudaError_t launch_prefill_k(const CUtensorMap &tq, const CUtensorMap &tk
 }
 
 // FP8 prefill, d = 64 or 128: dense batches and packed sequences (row pairs
-// or head pairs); the output leaves by row stores, so no output map is needed.
+// or head pairs); `to` is the bf16 output map (used at d = 128).
 template <int D, int KIND>
 static cudaError_t launch_prefill_fp8_k(const CUtensorMap &tq, const CUtensorMap &tk,
-                                        const CUtensorMap &tv, const PrefillParams &p, bool causal,
-                                        int grid, cudaStream_t stream) {
-  return causal ? launch_prefill_t<D, true, KIND, true>(tq, tk, tv, tv, tq, p, grid, stream)
-                : launch_prefill_t<D, false, KIND, true>(tq, tk, tv, tv, tq, p, grid, stream);
+                                        const CUtensorMap &tv, const CUtensorMap &to,
+                                        const PrefillParams &p, bool causal, int grid,
+                                        cudaStream_t stream) {
+  return causal ? launch_prefill_t<D, true, KIND, true>(tq, tk, tv, tv, to, p, grid, stream)
+                : launch_prefill_t<D, false, KIND, true>(tq, tk, tv, tv, to, p, grid, stream);
 }
 
 template <int D>
 static cudaError_t launch_prefill_fp8_d(const CUtensorMap &tq, const CUtensorMap &tk,
-                                        const CUtensorMap &tv, const PrefillParams &p, bool causal,
-                                        int grid, cudaStream_t stream, int kind) {
+                                        const CUtensorMap &tv, const CUtensorMap &to,
+                                        const PrefillParams &p, bool causal, int grid,
+                                        cudaStream_t stream, int kind) {
   if (kind == kKindVarlen)
-    return launch_prefill_fp8_k<D, kKindVarlen>(tq, tk, tv, p, causal, grid, stream);
+    return launch_prefill_fp8_k<D, kKindVarlen>(tq, tk, tv, to, p, causal, grid, stream);
   if (kind == kKindVarlenHeads)
-    return launch_prefill_fp8_k<D, kKindVarlenHeads>(tq, tk, tv, p, causal, grid, stream);
-  return launch_prefill_fp8_k<D, kKindDense>(tq, tk, tv, p, causal, grid, stream);
+    return launch_prefill_fp8_k<D, kKindVarlenHeads>(tq, tk, tv, to, p, causal, grid, stream);
+  return launch_prefill_fp8_k<D, kKindDense>(tq, tk, tv, to, p, causal, grid, stream);
 }
 
 cudaError_t launch_prefill_fp8(const CUtensorMap &tq, const CUtensorMap &tk,
-                               const CUtensorMap &tv, const PrefillParams &p, bool causal,
-                               int grid, cudaStream_t stream, int kind, int d) {
-  return d == 64 ? launch_prefill_fp8_d<64>(tq, tk, tv, p, causal, grid, stream, kind)
-                 : launch_prefill_fp8_d<128>(tq, tk, tv, p, causal, grid, stream, kind);
+                               const CUtensorMap &tv, const CUtensorMap &to,
+                               const PrefillParams &p, bool causal, int grid,
+                               cudaStream_t stream, int kind, int d) {
+  return d == 64 ? launch_prefill_fp8_d<64>(tq, tk, tv, to, p, causal, grid, stream, kind)
+                 : launch_prefill_fp8_d<128>(tq, tk, tv, to, p, causal, grid, stream, kind);
 }
 
 cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
