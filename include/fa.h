@@ -163,7 +163,10 @@ int fa_fwd_varlen_fp8(const void *q, const void *k, const void *v, void *out, fl
  *                      scale and causal flag)
  *   workspace        : caller-owned device memory of at least
  *                      fa_bwd_workspace_size(B, H, N) bytes, 256-byte aligned;
- *                      overwritten (fp32 rowsums and rescaled lse)
+ *                      overwritten (fp32 rowsums and rescaled lse, then the
+ *                      work counters of the two persistent gradient kernels,
+ *                      which the call zeroes itself); one call at a time per
+ *                      workspace
  * Supported: d in {64, 128}.  All buffers device memory; asynchronous on
  * `stream`.  Errors as for fa_fwd; FA_ERR_WORKSPACE for a missing, small or
  * misaligned workspace.
