@@ -163,7 +163,7 @@ def test_backward_full_size_sampled(fa):
 
 
 # ------------------------------------------------------------- packed batches
-def run_varlen(fa, lengths, H, Hkv, d, causal, seed, pad_rows=0):
+def run_varlen(fa, lengths, H, Hkv, d, causal, seed, pad_rows=0, max_seqlen=None):
     """fa_bwd_varlen on a packed batch against the packed gradient oracle,
     one sequence at a time (each sequence's gradients at the tolerance of
     its own scale).  ``pad_rows`` extra rows after the last sequence belong
@@ -172,7 +172,7 @@ def run_varlen(fa, lengths, H, Hkv, d, causal, seed, pad_rows=0):
     inp = W.varlen_inputs(lengths, H, Hkv, d, seed=seed)
     T = inp.total_tokens
     cu = inp.cu_seqlens
-    max_len = int(max(lengths))
+    max_len = int(max(lengths)) if max_seqlen is None else max_seqlen
     do_bits = W.normal_bf16_bits((T, H, d), seed, 3)
     pad = lambda bits, h: np.concatenate([bits, W.normal_bf16_bits((pad_rows, h, d), seed, 9)])
     q, k, v = dev_bf16(pad(inp.q, H)), dev_bf16(pad(inp.k, Hkv)), dev_bf16(pad(inp.v, Hkv))
@@ -219,6 +219,19 @@ def test_backward_varlen_rows_outside_sequences(fa):
 def test_backward_varlen_many_tiles(fa):
     """Sequences of 1000 to 2100 rows (8 to 17 tiles each way)."""
     run_varlen(fa, [1000, 2100, 1537], 4, 1, 128, True, seed=212)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_varlen_many_sequences(fa, causal):
+    """More sequences (150) than the longest-first order covers: the tiles are
+    claimed sequence by sequence, past each sequence's end claimed again."""
+    lengths = np.random.default_rng(215).integers(0, 300, size=150)
+    run_varlen(fa, list(lengths), 2, 1, 64, causal, seed=215)
+
+
+def test_backward_varlen_loose_max_seqlen(fa):
+    """A max_seqlen far above the longest sequence (levels with no tile)."""
+    run_varlen(fa, [100, 37, 260], 4, 2, 128, True, seed=216, max_seqlen=1000)
 
 
 def test_backward_varlen_matches_dense(fa):
