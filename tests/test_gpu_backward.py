@@ -272,3 +272,38 @@ def test_backward_varlen_bad_cu_seqlens_flagged(fa):
         fa.fa_bwd_varlen(q, k, v, out, lse, q, cu, 20, workspace=small)
     assert e.value.status == -4
     assert_device_clean()
+
+
+def test_backward_varlen_full_size_sampled(fa):
+    """The packed backward leg's launch at full size (the varlen workload: 32
+    sequences of U[64, 4096] tokens, H 16 / Hkv 4, d 128, causal).  The
+    oracle computes the full gradients of two seeded (sequence, KV group)
+    slices (the group's 4 query heads), which are compared with the kernels'."""
+    torch = torch_mod()
+    cfg = W.WORKLOADS["varlen_gqa_d128"]
+    lengths = W.varlen_lengths(cfg["num_seqs"], cfg["len_lo"], cfg["len_hi"])
+    H, Hkv, d = cfg["H"], cfg["Hkv"], cfg["d"]
+    inp = W.varlen_inputs(lengths, H, Hkv, d, seed=0)
+    T = inp.total_tokens
+    do_bits = W.normal_bf16_bits((T, H, d), 0, 3)
+    q, k, v, do = dev_bf16(inp.q), dev_bf16(inp.k), dev_bf16(inp.v), dev_bf16(do_bits)
+    cu = dev_i32(inp.cu_seqlens)
+    max_len = int(np.max(lengths))
+    out, lse = fa.fa_fwd_varlen(q, k, v, cu, max_len, causal=True)
+    dq, dk, dv = fa.fa_bwd_varlen(q, k, v, out, lse, do, cu, max_len, causal=True)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(17)
+    group = H // Hkv
+    for s in rng.choice(len(lengths), 2, replace=False):
+        g = int(rng.integers(0, Hkv))
+        a, e = int(inp.cu_seqlens[s]), int(inp.cu_seqlens[s + 1])
+        hs = slice(g * group, (g + 1) * group)
+        rq, rk, rv = oracle.attention_backward_one(
+            f64(inp.q[a:e, hs]), f64(inp.k[a:e, g:g + 1]), f64(inp.v[a:e, g:g + 1]),
+            f64(do_bits[a:e, hs]), causal=True)
+        what = f"full seq {s} ({e - a} rows) kv group {g}"
+        errs = [check_grad("dq", host_f64(dq[a:e, hs]), rq, what),
+                check_grad("dk", host_f64(dk[a:e, g:g + 1]), rk, what),
+                check_grad("dv", host_f64(dv[a:e, g:g + 1]), rv, what)]
+        print(f"{what}: relative RMS errors dq {errs[0]:.2e} dk {errs[1]:.2e} dv {errs[2]:.2e}")
+    assert_device_clean()
