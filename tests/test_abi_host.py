@@ -147,10 +147,38 @@ def test_bwd_host_validation(lib):
     assert call(ws=ctypes.c_void_p(0x10010)) == -4   # not 256-byte aligned
 
 
+def test_bwd_varlen_host_validation(lib):
+    import exact_attention_33_gb300  # noqa: F401  (sets argtypes)
+    f = lib.fa_bwd_varlen
+
+    def call(q=P, lse=P, cu=P, ws=P, ws_bytes=1 << 30, S=3, T=500, max_len=300, H=4, Hkv=2,
+             d=128, causal=1, scale=0.1):
+        return f(q, P, P, P, lse, P, P, P, P, cu, S, T, max_len, H, Hkv, d, scale, causal, ws,
+                 ws_bytes, NULL)
+    assert call(q=NULL) == -1
+    assert call(lse=NULL) == -1
+    assert call(cu=NULL) == -1
+    assert call(q=P_BAD) == -1
+    assert call(cu=ctypes.c_void_p(0x10002)) == -1   # cu_seqlens not 4-byte aligned
+    assert call(S=-1) == -1
+    assert call(T=-1) == -1
+    assert call(max_len=-1) == -1
+    assert call(H=3) == -1
+    assert call(causal=5) == -1
+    assert call(scale=float("nan")) == -1
+    assert call(d=96) == -2
+    assert call(S=0) == 0
+    assert call(T=0) == 0
+    assert call(max_len=0) == 0
+    assert call(ws=NULL) == -4
+    assert call(ws_bytes=16) == -4
+    assert call(ws=ctypes.c_void_p(0x10010)) == -4   # not 256-byte aligned
+
+
 def test_bwd_workspace_size():
     import exact_attention_33_gb300 as fa
-    # two fp32 vectors (rowsums and rescaled lse) per (batch, head), N padded to 128
-    # -lse2 and -D vectors, then 256 bytes of work counters
+    # -lse2 and -D vectors per (batch, head), N padded to 128, then 256 bytes of
+    # work counters
     assert fa.fa_bwd_workspace_size(2, 32, 8192) == 2 * 2 * 32 * 8192 * 4 + 256
     assert fa.fa_bwd_workspace_size(1, 1, 1) == 2 * 128 * 4 + 256
     assert fa.fa_bwd_workspace_size(1, 4, 129) == 2 * 4 * 256 * 4 + 256
