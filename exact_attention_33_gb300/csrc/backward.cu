@@ -7,19 +7,25 @@
 // with P recomputed tile by tile from Q, K and the forward log-sum-exp, so
 // neither P nor S ever reaches HBM (the same IO argument as the forward).
 //
-// Three kernels:
-//   bwd_preprocess   D and the log-sum-exp in log2 units, per (b, h, row).
-//   bwd_dq           one CTA per (b, h, 128-row query tile); streams the
+// Three kernels, for dense batches and for packed batches of sequences
+// (cu_seqlens; each sequence sees only its own keys):
+//   bwd_preprocess   -D and -log-sum-exp in log2 units, per (b, h, row); also
+//                    zeroes the work counters of the two kernels after it.
+//   bwd_dq           per (b, h, 128-row query tile) work item; streams the
 //                    key tiles: S = Q K^T and dP = dO V^T (tcgen05, TMEM),
 //                    dS in registers, dQ += dS K (A = dS from TMEM).
-//   bwd_dkdv         one CTA per (b, kv head, 128-key tile); streams the
+//   bwd_dkdv         per (b, kv head, 128-key tile) work item; streams the
 //                    query tiles of every query head of the group:
 //                    S^T = K Q^T and dP^T = V dO^T, then dV += P^T dO and
 //                    dK += dS^T Q (A from TMEM), so the group's sum stays in
 //                    TMEM and no atomics are needed.
+// bwd_dq and bwd_dkdv are persistent: one CTA per SM claims work items from
+// a counter, heaviest first, and every barrier of its pipeline counts tiles
+// over all of its items.
 // Roles per CTA: warps 0-7 elementwise (warps w and w + 4 share the TMEM
 // lanes of rows 32 (w % 4) .. + 31 and take the lower and upper 64 columns),
-// warp 8 issues the MMAs (converged, elect.sync), warp 9 is the TMA producer.
+// warp 8 issues the MMAs (converged, elect.sync), warp 9 claims items and is
+// the TMA producer.
 // The bf16 operands the elementwise warps write (P, dS) land in the columns
 // each half has already read: keys 0-63 in columns [0, 32), keys 64-127 in
 // [64, 96) of the region, so the TMEM-sourced MMAs read them at that split.
