@@ -81,6 +81,13 @@ def test_backward_small(fa, d, causal, B, N, H, Hkv):
     run_case(fa, B, N, H, Hkv, d, causal, seed=90 + N)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_wide_group(fa, causal):
+    """Eight query heads per KV head: each dK/dV item runs 8 iterations per
+    query tile and sums the whole group in TMEM."""
+    run_case(fa, 1, 300, 8, 1, 128, causal, seed=98)
+
+
 def test_backward_medium(fa):
     """Many tiles in both directions (16 query and 16 key tiles)."""
     run_case(fa, 1, 2048, 2, 1, 128, True, seed=95)
